@@ -1,0 +1,487 @@
+#!/usr/bin/env python
+"""Paged decode-attention benchmark on one GB300 (replicas for N > 1).
+
+Workload: the continuous-batching rollout with Qwen3-4B head shapes — 64
+slots, 32 q / 8 kv heads, head_dim 128, page 64, max_seq 1024, prompts
+U[100, 400], each sequence stopping at a seeded length and its slot and
+pages reused at once (fragmented placement). A step is one layer's decode
+step: q/k RMSNorm + RoPE, the K/V append, split-KV attention and combine.
+
+value      algorithmic KV-read bytes of the attention (K+V of every key,
+           q in, out, table entries) / device time of the whole step, GB/s;
+           inputs resident in HBM, 4+ layer caches cycled so every step's
+           keys come from DRAM (working set > 4x L2).
+roofline   the same bytes / the attention kernels' own time, vs the measured
+           HBM copy bandwidth.
+e2e        the same metric through the public Python API with pinned host
+           inputs copied in and the output read back every step.
+cpu_baseline / --impl reference: the float64 CPU oracle on a bounded sample.
+"""
+from __future__ import annotations
+
+import os
+
+for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import argparse  # noqa: E402
+import hashlib  # noqa: E402
+import json  # noqa: E402
+import math  # noqa: E402
+import statistics  # noqa: E402
+import subprocess  # noqa: E402
+import sys  # noqa: E402
+import time  # noqa: E402
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as wl  # noqa: E402
+
+METRIC = "paged decode-attn KV-read GB/s (% of GB300 HBM peak); µs per decode step"
+UNIT = "GB/s"
+WORKLOAD_DESC = ("rollout continuous batching, Qwen3-4B heads: B=64 slots, 32 q / 8 kv heads, "
+                 "head_dim 128, page 64, max_seq 1024, prompts U[100,400], seeded stops with "
+                 "slot/page reuse, q/k RMSNorm + RoPE theta 1e6")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=4000)
+    ap.add_argument("--warmup", type=int, default=16)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=400)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--num-splits", type=int, default=0)
+    ap.add_argument("--no-clocks", action="store_true")
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------- helpers --
+def attn_bytes(seq_lens: np.ndarray, B, Hq, Hkv, D, ps) -> int:
+    """Algorithmic bytes of one paged_decode_attn call: K and V of every key
+    read once, q read, out written, one table entry per page."""
+    n = seq_lens.astype(np.int64)
+    return int(Hkv * n.sum() * D * 2 * 2 + B * Hq * D * 2 * 2 + (-(-n // ps)).sum() * 4)
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except OSError:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
+
+
+def profile_traffic(kernel_key: str):
+    """DRAM bytes per launch from a committed ncu capture, if the kernel
+    source is unchanged since the capture."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f).get(kernel_key)
+    except (OSError, ValueError):
+        return None
+    if not rec:
+        return None
+    src = os.path.join(ROOT, "paged_kv_decode_pagetable_gb300", "csrc", "decode_attn.cu")
+    with open(src, "rb") as f:
+        digest = hashlib.sha256(f.read()).hexdigest()[:16]
+    if rec.get("source_sha256_16") != digest:
+        return None
+    return rec.get("bytes_per_launch_full")
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, enabled: bool, index: int):
+        self.proc = None
+        if not enabled:
+            return
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "20", "-i", str(index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.05)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def rollout_metadata(w, total_steps):
+    """Runs the schedule through a host-only PageTable; per-step tables and
+    row metadata (what the device would hold after each step's pt_* calls)."""
+    import paged_kv_decode_pagetable_gb300 as pkv
+    from paged_kv_decode_pagetable_gb300 import engine
+    sched = wl.rollout_schedule(w, steps=total_steps)
+    pt = pkv.PageTable(w.max_batch_size, w.page_size, w.n_pages, w.max_pages_per_seq)
+    drv = engine.RolloutDriver(pt, sched)
+    tables, bidx, pos, lens = [], [], [], []
+    for _ in range(total_steps):
+        m = drv.next_step()
+        tables.append(pt.host_table().numpy())
+        bidx.append(m.batch_idx)
+        pos.append(m.input_pos)
+        lens.append(m.seq_lens)
+    return (np.stack(tables), np.stack(bidx), np.stack(pos), np.stack(lens))
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def reduce_max(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def reduce_sum(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------ CPU oracle ----
+class PagePool:
+    """Random float32 pages (all kv heads) that sampled rows point into."""
+
+    def __init__(self, w, rng, D=128, pages=64):
+        self.pages = pages
+        self.kc = rng.standard_normal((w.n_kv_heads, pages * w.page_size, D)).astype(np.float32)
+        self.vc = rng.standard_normal((w.n_kv_heads, pages * w.page_size, D)).astype(np.float32)
+
+
+def oracle_sample(w, lens_rows, rng, seconds, pool, min_rows=1):
+    """Times the oracle's attention for rows with the given lengths (cycled),
+    their pages drawn from `pool`, until `seconds` of CPU time have been spent
+    inside the oracle; returns (bytes, seconds, rows)."""
+    import oracle
+    D, Hq, Hkv, ps = 128, w.n_q_heads, w.n_kv_heads, w.page_size
+    pool_pages, kc, vc = pool.pages, pool.kc, pool.vc
+    total_bytes, elapsed, rows = 0, 0.0, 0
+    i = 0
+    while (elapsed < seconds or rows < min_rows) and rows < 10 ** 7:
+        L = int(lens_rows[i % len(lens_rows)])
+        i += 1
+        nb = -(-L // ps)
+        table = np.zeros((2, nb), np.int32)
+        table[1] = rng.integers(0, pool_pages, size=nb)
+        q = rng.standard_normal((1, Hq, D))
+        t0 = time.perf_counter()
+        oracle.decode_attention(q, kc, vc, table, [1], [L], 0, D ** -0.5, ps)
+        elapsed += time.perf_counter() - t0
+        total_bytes += attn_bytes(np.array([L]), 1, Hq, Hkv, D, ps)
+        rows += 1
+    return total_bytes, elapsed, rows
+
+
+def run_reference(args, world, rank):
+    """The CPU oracle as the reference arm: each step a bounded sample of the
+    step's rows (two rows), warm-up steps untimed."""
+    if rank != 0:
+        return
+    w = wl.ROLLOUT
+    total = args.warmup + args.steps
+    sched = wl.rollout_schedule(w, steps=total)
+    # lengths per step from the schedule alone (no allocator needed for lengths)
+    length = [r.prompt_len for r in sched.first]
+    rng = np.random.default_rng(w.seed(99))
+    pool = PagePool(w, rng)
+    tot_bytes, tot_s, rows = 0, 0.0, 0
+    for t in range(total):
+        for lane, r in sched.start[t]:
+            length[lane] = r.prompt_len
+        lens = np.array(length) + 1
+        sample = lens[[(2 * t) % w.batch, (2 * t + 1) % w.batch]]
+        b, s, n = oracle_sample(w, sample, rng, 0.0, pool, min_rows=2)
+        if t >= args.warmup:
+            tot_bytes, tot_s, rows = tot_bytes + b, tot_s + s, rows + n
+        length = [L + 1 for L in length]
+    value = tot_bytes / tot_s / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": tot_s / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD_DESC, "global_batch": w.batch,
+                   "sample": "2 rows per step (of 64), oracle on host cores",
+                   "parallelism": "replicas"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"{rows} rows over {args.steps} steps (2 rows/step), "
+                                   "float64 NumPy, single thread"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- GPU arm ---
+def run_ours(args, world, rank, local):
+    import paged_kv_decode_pagetable_gb300 as pkv
+    from paged_kv_decode_pagetable_gb300 import engine
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (the product path has no CPU fallback)")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pkv.load_library()
+    w = wl.ROLLOUT
+    spec = engine.LayerSpec(w.layers[0].head_dim, w.layers[0].theta, 0, True, True)
+    B, Hq, Hkv, D, ps = w.batch, w.n_q_heads, w.n_kv_heads, spec.head_dim, w.page_size
+    W, K = args.warmup, args.steps
+    total = W + K
+
+    tables, bidx, pos, lens = rollout_metadata(w, total)
+    step_bytes = np.array([attn_bytes(lens[t], B, Hq, Hkv, D, ps) for t in range(total)])
+    d_tables = torch.from_numpy(tables).to(dev)
+    d_bidx = torch.from_numpy(bidx).to(dev)
+    d_pos = torch.from_numpy(pos).to(dev)
+    d_lens = torch.from_numpy(lens).to(dev)
+
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 126 * 2 ** 20) or 126 * 2 ** 20
+    kv_step = float(np.mean(step_bytes))
+    n_layers = max(2, math.ceil(4 * l2 / kv_step))
+    caches = [engine.alloc_cache(Hkv, w.n_pages, ps, D, dev, fill="randn") for _ in range(n_layers)]
+
+    g = torch.Generator(device=dev)
+    g.manual_seed(w.seed(rank))
+    q = torch.randn((B, Hq, D), generator=g, device=dev).to(torch.bfloat16)
+    k = torch.randn((B, Hkv, D), generator=g, device=dev).to(torch.bfloat16)
+    v = torch.randn((B, Hkv, D), generator=g, device=dev).to(torch.bfloat16)
+    gq = (1 + 0.1 * torch.randn(D, generator=g, device=dev)).to(torch.bfloat16)
+    gk = (1 + 0.1 * torch.randn(D, generator=g, device=dev)).to(torch.bfloat16)
+    out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws = engine.AttnWorkspace(B, Hq, Hkv, D, w.max_pages_per_seq, ps, 0, dev, args.num_splits)
+
+    class Geom:
+        n_slots, max_pages_per_seq, page_size, n_pages = (w.n_slots, w.max_pages_per_seq, ps,
+                                                          w.n_pages)
+        dev_table = None
+
+    def step(t):
+        kc, vc = caches[t % n_layers]
+        engine.decode_layer_step(spec, Geom, kc, vc, q, k, v, d_bidx[t], d_pos[t], d_lens[t], out,
+                                 ws, gq, gk, w.eps, err=err, table=d_tables[t])
+
+    def attn_only(t):
+        kc, vc = caches[t % n_layers]
+        pkv.paged_decode_attn(q, kc, vc, d_tables[t], w.n_slots, w.max_pages_per_seq, ps,
+                              w.n_pages, d_bidx[t], d_lens[t], 0, D ** -0.5, ws.splits, ws.buf,
+                              out, err)
+
+    # warm-up: W eager steps (first use of every kernel), then capture
+    for t in range(W):
+        step(t)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for t in range(W, total):
+            step(t)
+    graph_attn = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph_attn):
+        for t in range(W, total):
+            attn_only(t)
+    torch.cuda.synchronize()
+
+    stream = torch.cuda.current_stream()
+    sampler = ClockSampler(not args.no_clocks, local)
+    barrier(world)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    graph.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop()
+    t_step_ms = e0.elapsed_time(e1)
+
+    # attention kernels alone over the same steps (after one untimed replay)
+    graph_attn.replay()
+    torch.cuda.synchronize()
+    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a0.record(stream)
+    graph_attn.replay()
+    a1.record(stream)
+    torch.cuda.synchronize()
+    t_attn_ms = a0.elapsed_time(a1)
+    errv = pkv.pkv_read_error_word(err)
+    if errv != 0:
+        raise SystemExit(f"device error word {errv}")
+
+    timed_bytes = float(step_bytes[W:].sum())
+    t_max = reduce_max(t_step_ms, world)
+    value = reduce_sum(timed_bytes, world) / (t_max * 1e-3) / 1e9
+    attn_gbs = timed_bytes / (t_attn_ms * 1e-3) / 1e9
+    peaks, peak_kind = measured_peaks()
+    peak = float(peaks.get("hbm_gbs", 6800.0))
+    launches_per_step = 3 + (1 if ws.splits > 1 else 0)
+
+    # ---- end to end through the public API: pinned host in, output back ----
+    e2e = run_e2e(args, w, spec, engine, pkv, caches, n_layers, tables, bidx, pos, lens,
+                  step_bytes, gq, gk, ws, dev, world)
+
+    # ---- CPU oracle baseline on a bounded sample (rank 0, N=1 only) ----
+    cpu = None
+    if rank == 0 and world == 1:
+        rng = np.random.default_rng(w.seed(7))
+        b, s, n = oracle_sample(w, lens[W], rng, args.cpu_seconds, PagePool(w, rng))
+        cpu = {"value": b / s / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"{n} rows with the lengths of timed step 0's batch (cycled), float64 "
+                         f"NumPy on 1 host thread, {s:.1f} s"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+            "warmup": W, "ms_per_step": t_max / K, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": WORKLOAD_DESC, "global_batch": B * world, "seq_len": "100-1024",
+                       "num_splits": ws.splits, "layer_caches_cycled": n_layers,
+                       "l2_policy": f"inputs larger than L2: {n_layers} layer caches of "
+                                    f"{caches[0][0].numel() * 4 / 2**20:.0f} MiB cycled; "
+                                    f"{kv_step / 2**20:.0f} MiB of K/V read per step",
+                       "us_per_step": t_max / K * 1e3, "attn_us_per_call": t_attn_ms / K * 1e3,
+                       "parallelism": f"replicas x{world}"},
+            "roofline": {"bound": "hbm", "achieved": attn_gbs, "peak": peak, "unit": "GB/s",
+                         "frac": attn_gbs / peak, "peak_kind": peak_kind,
+                         "kernel": "decode_split_kernel<128> + combine_kernel",
+                         "traffic": profile_traffic("rollout_decode_split_128")},
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": K * launches_per_step,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+
+
+def run_e2e(args, w, spec, engine, pkv, caches, n_layers, tables, bidx, pos, lens, step_bytes,
+            gq, gk, ws, dev, world):
+    B, Hq, Hkv, D = w.batch, w.n_q_heads, w.n_kv_heads, spec.head_dim
+    n = min(args.e2e_steps, args.steps)
+    W = args.warmup
+    ring = 4
+    gen = torch.Generator().manual_seed(w.seed(3))
+    host_q = [torch.randn((B, Hq, D), generator=gen).to(torch.bfloat16).pin_memory() for _ in range(ring)]
+    host_k = [torch.randn((B, Hkv, D), generator=gen).to(torch.bfloat16).pin_memory() for _ in range(ring)]
+    host_v = [torch.randn((B, Hkv, D), generator=gen).to(torch.bfloat16).pin_memory() for _ in range(ring)]
+    h_tables = torch.from_numpy(tables).pin_memory()
+    h_meta = torch.from_numpy(np.stack([bidx, pos, lens], axis=1)).pin_memory()   # [T][3][B]
+    h_out = torch.empty((B, Hq, D), dtype=torch.bfloat16).pin_memory()
+    q = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=dev)
+    k = torch.empty((B, Hkv, D), dtype=torch.bfloat16, device=dev)
+    v = torch.empty((B, Hkv, D), dtype=torch.bfloat16, device=dev)
+    d_table = torch.empty(tables.shape[1:], dtype=torch.int32, device=dev)
+    d_meta = torch.empty((3, B), dtype=torch.int32, device=dev)
+    out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=dev)
+
+    class Geom:
+        n_slots, max_pages_per_seq, page_size, n_pages = (w.n_slots, w.max_pages_per_seq,
+                                                          w.page_size, w.n_pages)
+        dev_table = None
+
+    def one(t):
+        j = t % ring
+        q.copy_(host_q[j], non_blocking=True)
+        k.copy_(host_k[j], non_blocking=True)
+        v.copy_(host_v[j], non_blocking=True)
+        d_table.copy_(h_tables[t], non_blocking=True)
+        d_meta.copy_(h_meta[t], non_blocking=True)
+        kc, vc = caches[t % n_layers]
+        engine.decode_layer_step(spec, Geom, kc, vc, q, k, v, d_meta[0], d_meta[1], d_meta[2],
+                                 out, ws, gq, gk, w.eps, table=d_table)
+        h_out.copy_(out, non_blocking=True)
+
+    for t in range(min(W, 8)):
+        one(t)
+    torch.cuda.synchronize()
+    barrier(world)
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for t in range(W, W + n):
+        one(t)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = reduce_max(e0.elapsed_time(e1), world)
+    byts = reduce_sum(float(step_bytes[W:W + n].sum()), world)
+    h2d = (B * Hq * D + 2 * B * Hkv * D) * 2 + tables[0].nbytes + 3 * B * 4
+    return {"value": byts / (ms * 1e-3) / 1e9, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(B * Hq * D * 2), "steps": n,
+            "ms_per_step": ms / n}
+
+
+def main():
+    args = parse_args()
+    world, rank, local = dist_setup(args)
+    try:
+        if args.impl == "reference":
+            run_reference(args, world, rank)
+        else:
+            run_ours(args, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            if dist.is_initialized():
+                dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,196 @@
+/*
+ * pkv.h — C ABI of libpkv: paged-KV single-token decode attention on one
+ * GB300 (sm_103a).
+ *
+ * The method follows three public web pages:
+ *   [P1] "unsloth: compare main...flex-moe-qwen3" (commit message on the
+ *        PageTable +1 capacity fix; unsloth/inference/flex_gemma4_moe.py:
+ *        rotary helpers, attention forward, decode block masks, CUDA-graph
+ *        capture and the continuous-batching loop);
+ *   [P3] "unsloth: compare main...transformers-continuous-batching-qwen3"
+ *        (scripts/benchmarks/flex_paged_attention.py: PagedKVCache and
+ *        PageTable; scripts/benchmarks/README.md).
+ *
+ * Conventions shared by every call
+ *   - Every call returns an int status: PKV_OK (0) or a negative PKV_E_*.
+ *     A failed call leaves all state unchanged and records a message that
+ *     pkv_last_error() returns (thread-local).
+ *   - bf16 tensors are passed as pkv_bf16 (the raw 16-bit pattern).
+ *   - Device pointers are caller-owned (allocated by the caller, e.g. with
+ *     PyTorch). No call allocates or frees device memory.
+ *   - Kernels are enqueued asynchronously on the given stream (a
+ *     cudaStream_t passed as void*; NULL = legacy default stream). Only
+ *     pkv_read_error_word() synchronizes.
+ *   - Kernel launches use a grid that depends only on the scalar arguments,
+ *     and read per-step metadata (positions, lengths, table) from device
+ *     memory, so a fixed-shape call can be captured in a CUDA graph.
+ *   - Device-side faults are never raised on purpose: an invalid index read
+ *     from device memory sets a bit in the caller's int32 error word
+ *     (atomic OR) and the access is skipped.
+ *
+ * Cache layout (per layer, [P3] PagedKVCache): k_cache and v_cache are bf16
+ * [Hkv][n_pages * page_size][D], row-major. Physical page p of kv head g is
+ * the contiguous block of rows [p*page_size, (p+1)*page_size) of head g.
+ * The page table is int32 [n_slots][max_pages_per_seq], row-major, with
+ * n_slots = max_batch_size + 1; entry [s][j] is the physical page holding
+ * logical tokens [j*page_size, (j+1)*page_size) of slot s, or -1.
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t pkv_bf16;
+typedef struct pkv_pt pkv_pt;
+
+/* status codes */
+#define PKV_OK 0
+#define PKV_E_NO_SLOT (-1)   /* no free slot */
+#define PKV_E_NO_PAGES (-2)  /* too few free pages */
+#define PKV_E_BAD_SLOT (-3)  /* slot 0, out of range, or not allocated */
+#define PKV_E_BAD_ARG (-4)   /* shape, alignment, or pointer argument */
+#define PKV_E_CUDA (-5)      /* a CUDA runtime call failed */
+
+/* device error-word bits */
+#define PKV_ERR_POS 1          /* position negative or beyond the table row */
+#define PKV_ERR_PAGE_RANGE 2   /* table entry >= n_pages */
+#define PKV_ERR_PAGE_NEG 4     /* table entry < 0 (unreserved block) */
+#define PKV_ERR_SLOT 8         /* batch index outside [0, n_slots) */
+#define PKV_ERR_TIMEOUT 16     /* a bounded wait on a copy gave up */
+
+/* ---------------------------------------------------------------------
+ * PageTable allocator (host) — [P3] PageTable.__init__ / can_reserve /
+ * allocate / reserve / erase, with the +1 capacity rule of [P1]'s commit
+ * message.
+ *
+ * Slot 0 is a no-op padding slot and page 0 a dummy page; row 0 of the
+ * table is all 0. Slots 1..max_batch_size are usable. Free slots and free
+ * pages are LIFO stacks (initially [N..1] and [n_pages-1..1]). reserve takes
+ * the last k entries of the free-page list, in list order, for the next k
+ * logical blocks; free pushes the slot and appends the slot's pages in
+ * reverse order. A freed slot's device row is left stale until it is
+ * assigned again.
+ *
+ * Device mirror: if dev_table is non-NULL it must point to caller-owned
+ * int32 device memory of n_slots * max_pages_per_seq entries, 4-byte
+ * aligned. pt_create writes the whole table; pt_assign writes the assigned
+ * row; pt_reserve writes the new entries. These are cudaMemcpyAsync copies
+ * from pageable host memory on the handle's stream: they may synchronize
+ * with that stream, and must not be issued while the stream is capturing a
+ * CUDA graph. With dev_table NULL the allocator is host-only (no CUDA call).
+ * ------------------------------------------------------------------- */
+int pt_create(int max_batch_size, int page_size, int n_pages,
+              int max_pages_per_seq, int32_t *dev_table, void *stream,
+              pkv_pt **out);
+int pt_destroy(pkv_pt *pt);
+int pt_set_stream(pkv_pt *pt, void *stream);
+/* slot < 0: can a new request of seq_len tokens be admitted (a free slot
+ * and enough pages)?  slot >= 1: can that live slot grow to seq_len? */
+int pt_can_reserve(const pkv_pt *pt, int seq_len, int slot, int *ok);
+/* allocate a slot and reserve seq_len tokens for it (all or nothing) */
+int pt_assign(pkv_pt *pt, int seq_len, int *slot_out);
+/* grow a live slot's capacity to >= seq_len (no-op if it already fits) */
+int pt_reserve(pkv_pt *pt, int slot, int seq_len);
+/* release a live slot and its pages */
+int pt_free(pkv_pt *pt, int slot);
+/* tokens reserved for a slot (0 for a free slot) */
+int pt_capacity(const pkv_pt *pt, int slot, int *tokens);
+/* pages of a slot in logical order (host mirror); *n receives the count */
+int pt_pages(const pkv_pt *pt, int slot, int32_t *host_out, int max, int *n);
+int pt_free_pages(const pkv_pt *pt, int *n);
+/* the free-page stack, bottom first (the next reserve takes from the end) */
+int pt_free_page_list(const pkv_pt *pt, int32_t *host_out, int max, int *n);
+/* copy of the host mirror, n_slots * max_pages_per_seq entries */
+int pt_host_table(const pkv_pt *pt, int32_t *host_out, int max);
+
+/* ---------------------------------------------------------------------
+ * kv_append — decode scatter of the step's new K/V ([P3] PageTable.assign):
+ *   block = input_pos[b] / page_size, offset = input_pos[b] % page_size,
+ *   row   = table[batch_idx[b]][block] * page_size + offset,
+ *   k_cache[h][row][:] = k[b][h][:], v_cache[h][row][:] = v[b][h][:].
+ * k, v: bf16 [B][Hkv][D]; batch_idx (NULL = identity) and input_pos: int32
+ * [B]; rows may share a slot (a multi-token fill). Rows whose address is
+ * invalid set PKV_ERR_* bits in err_word (may be NULL) and are skipped.
+ * Requires D % 8 == 0 and 16-byte aligned k, v, k_cache, v_cache.
+ * ------------------------------------------------------------------- */
+int kv_append(const pkv_bf16 *k, const pkv_bf16 *v, const int32_t *batch_idx,
+              const int32_t *input_pos, int B, const int32_t *dev_table,
+              int n_slots, int max_pages_per_seq, int page_size, int n_pages,
+              pkv_bf16 *k_cache, pkv_bf16 *v_cache, int Hkv, int D,
+              int32_t *err_word, void *stream);
+
+/* ---------------------------------------------------------------------
+ * qk_norm_rope — per-head RMSNorm then RoPE, in place ([P1] attention
+ * forward: q_norm / k_norm on the head axis before rotary; rotary helpers
+ * _rotate_half / _apply_rotary_full):
+ *   r = x / sqrt(mean(x^2) + eps) * gamma        (skipped if gamma is NULL)
+ *   phi_i = pos[b] * theta^(-2i/D),  i < D/2
+ *   y_i = r_i cos phi_i - r_{i+D/2} sin phi_i
+ *   y_{i+D/2} = r_{i+D/2} cos phi_i + r_i sin phi_i
+ * q: bf16 [B][Hq][D], k: bf16 [B][Hkv][D] (k may be NULL with Hkv 0),
+ * gamma_q / gamma_k: bf16 [D] or NULL, pos: int32 [B]. Arithmetic is fp32
+ * with a single rounding to bf16 per output. Requires D even, 2 <= D <= 1024,
+ * theta > 0.
+ * ------------------------------------------------------------------- */
+int qk_norm_rope(pkv_bf16 *q, pkv_bf16 *k, const pkv_bf16 *gamma_q,
+                 const pkv_bf16 *gamma_k, const int32_t *pos, float theta,
+                 float eps, int B, int Hq, int Hkv, int D, void *stream);
+
+/* ---------------------------------------------------------------------
+ * paged_decode_attn — GQA single-token decode attention over the paged
+ * cache ([P1] attention forward: flex_attention(q, k, v, scale,
+ * block_mask, enable_gqa=True) with the decode masks of _decode_block_mask).
+ * For row b: slot = batch_idx[b] (NULL = b), L = seq_lens[b] (tokens
+ * including the one just appended, i.e. input_pos + 1), keys
+ * j in [lo, L) with lo = max(0, L - window) if window > 0 else 0.
+ * Query head h reads kv head h / (Hq / Hkv).
+ *   out[b][h] = sum_j softmax_j(scale * q[b][h] . k_j) v_j
+ * Rows with L <= 0 or slot 0 give exact zeros.
+ *
+ * Split-KV: each (row, kv head) key range is cut into num_splits parts
+ * processed by separate CTAs that each write an fp32 partial output and
+ * log-sum-exp to the workspace; a combine kernel merges them. num_splits 0
+ * picks paged_decode_attn_splits(). The workspace must hold
+ * paged_decode_attn_workspace(B, Hq, D, splits) bytes (16-byte aligned;
+ * may be NULL when that is 0).
+ *
+ * q: bf16 [B][Hq][D], out: bf16 [B][Hq][D], caches and table as above.
+ * Requires D in {64, 128, 256, 512}, 1 <= Hq/Hkv <= 8, Hq % Hkv == 0,
+ * page_size a power of two >= 8, and 16-byte aligned q, out, caches.
+ * Table entries that are negative or >= n_pages inside a row's key range
+ * set PKV_ERR_PAGE_* (that row's output is then unspecified); L beyond
+ * max_pages_per_seq * page_size sets PKV_ERR_POS and is clamped.
+ * ------------------------------------------------------------------- */
+int paged_decode_attn(const pkv_bf16 *q, const pkv_bf16 *k_cache,
+                      const pkv_bf16 *v_cache, const int32_t *dev_table,
+                      int n_slots, int max_pages_per_seq, int page_size,
+                      int n_pages, const int32_t *batch_idx,
+                      const int32_t *seq_lens, int window, float scale, int B,
+                      int Hq, int Hkv, int D, int num_splits, void *workspace,
+                      size_t workspace_bytes, pkv_bf16 *out,
+                      int32_t *err_word, void *stream);
+/* the split count num_splits = 0 resolves to for this shape (depends only on
+ * the arguments and the device's SM count) */
+int paged_decode_attn_splits(int B, int Hkv, int D, int max_pages_per_seq,
+                             int page_size, int window, int *num_splits);
+/* workspace bytes needed for num_splits splits (0 when num_splits == 1) */
+size_t paged_decode_attn_workspace(int B, int Hq, int D, int num_splits);
+
+/* ---------------------------------------------------------------------
+ * Utilities
+ * ------------------------------------------------------------------- */
+/* synchronize the stream, then copy the device error word to *host_out */
+int pkv_read_error_word(const int32_t *err_word, void *stream,
+                        int32_t *host_out);
+/* message of the last failed call on this thread ("" if none) */
+const char *pkv_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PKV_H */
