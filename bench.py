@@ -58,6 +58,8 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--num-splits", type=int, default=0)
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="layer caches to cycle (0: enough for 4x L2)")
     return ap.parse_args()
 
 
@@ -297,7 +299,7 @@ def run_ours(args, world, rank, local):
     props = torch.cuda.get_device_properties(dev)
     l2 = getattr(props, "L2_cache_size", 126 * 2 ** 20) or 126 * 2 ** 20
     kv_step = float(np.mean(step_bytes))
-    n_layers = max(2, math.ceil(4 * l2 / kv_step))
+    n_layers = args.layers or max(2, math.ceil(4 * l2 / kv_step))
     caches = [engine.alloc_cache(Hkv, w.n_pages, ps, D, dev, fill="randn") for _ in range(n_layers)]
 
     g = torch.Generator(device=dev)
