@@ -182,6 +182,30 @@ int paged_decode_attn_splits(int B, int Hkv, int D, int max_pages_per_seq,
 size_t paged_decode_attn_workspace(int B, int Hq, int D, int num_splits);
 
 /* ---------------------------------------------------------------------
+ * paged_decode_attn_noalloc — paged_decode_attn without a caller workspace.
+ * The pages have no counterpart to this call; it exists for callers that
+ * cannot allocate device memory (a plain C program linking only this
+ * library with no device allocator, or a plugin whose host framework owns
+ * all device memory and hands out no scratch). Same arguments and results
+ * as paged_decode_attn minus workspace / workspace_bytes. The split
+ * partials go to a fixed 32 MiB scratch array in the library's device
+ * image, held by every GPU that loads the library until the process exits;
+ * calls whose partials need more (see paged_decode_attn_workspace) fail with
+ * PKV_E_BAD_ARG. The first call on a device looks up the scratch address
+ * (cudaGetSymbolAddress) with that device current; make it before any
+ * stream capture begins. All calls share the scratch: calls whose kernels
+ * overlap on the GPU race and must be serialized by the caller. Nothing in
+ * the scratch needs clearing between calls. No device memory is allocated.
+ * ------------------------------------------------------------------- */
+int paged_decode_attn_noalloc(const pkv_bf16 *q, const pkv_bf16 *k_cache,
+                              const pkv_bf16 *v_cache, const int32_t *dev_table,
+                              int n_slots, int max_pages_per_seq, int page_size,
+                              int n_pages, const int32_t *batch_idx,
+                              const int32_t *seq_lens, int window, float scale,
+                              int B, int Hq, int Hkv, int D, int num_splits,
+                              pkv_bf16 *out, int32_t *err_word, void *stream);
+
+/* ---------------------------------------------------------------------
  * Utilities
  * ------------------------------------------------------------------- */
 /* synchronize the stream, then copy the device error word to *host_out */

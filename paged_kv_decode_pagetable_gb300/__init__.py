@@ -82,6 +82,9 @@ _SIGS = {
     "paged_decode_attn": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_int, _c_int, _c_int, _c_int,
                                    _c_p, _c_p, _c_int, _c_f, _c_int, _c_int, _c_int, _c_int,
                                    _c_int, _c_p, _c_sz, _c_p, _c_p, _c_p]),
+    "paged_decode_attn_noalloc": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_int, _c_int, _c_int,
+                                           _c_int, _c_p, _c_p, _c_int, _c_f, _c_int, _c_int,
+                                           _c_int, _c_int, _c_int, _c_p, _c_p, _c_p]),
     "paged_decode_attn_splits": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
                                           ctypes.POINTER(_c_int)]),
     "paged_decode_attn_workspace": (_c_sz, [_c_int, _c_int, _c_int, _c_int]),
@@ -327,6 +330,24 @@ def paged_decode_attn(q, k_cache, v_cache, dev_table, n_slots, max_pages_per_seq
         page_size, n_pages, _ptr(batch_idx), _ptr(seq_lens), int(window), float(scale), B, Hq,
         Hkv, D, int(num_splits), _ptr(workspace), ws_bytes, _ptr(out), _ptr(err_word),
         _stream(stream)), "paged_decode_attn")
+
+
+def paged_decode_attn_noalloc(q, k_cache, v_cache, dev_table, n_slots, max_pages_per_seq,
+                              page_size, n_pages, batch_idx, seq_lens, window, scale, num_splits,
+                              out, err_word=None, stream=None) -> None:
+    """paged_decode_attn for callers that cannot allocate device memory: the
+    split partials go to the library's fixed 32 MiB device scratch instead
+    of a caller workspace. Calls share that scratch, so calls that overlap on
+    the GPU must be serialized by the caller."""
+    _bf16(q, "q"), _bf16(k_cache, "k_cache"), _bf16(v_cache, "v_cache"), _bf16(out, "out")
+    _i32(dev_table, "dev_table"), _i32(batch_idx, "batch_idx"), _i32(seq_lens, "seq_lens")
+    B, Hq, D = q.shape
+    Hkv = k_cache.shape[0]
+    _check(load_library().paged_decode_attn_noalloc(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(dev_table), n_slots, max_pages_per_seq,
+        page_size, n_pages, _ptr(batch_idx), _ptr(seq_lens), int(window), float(scale), B, Hq,
+        Hkv, D, int(num_splits), _ptr(out), _ptr(err_word), _stream(stream)),
+        "paged_decode_attn_noalloc")
 
 
 def pkv_read_error_word(err_word, stream=None) -> int:
