@@ -375,7 +375,7 @@ def run_ours(args, world, rank, local):
     attn_gbs = timed_bytes / (t_attn_ms * 1e-3) / 1e9
     peaks, peak_kind = measured_peaks()
     peak = float(peaks.get("hbm_gbs", 6800.0))
-    launches_per_step = 3 + (1 if ws.splits > 1 else 0)
+    launches_per_step = 3 + (1 if ws.max_parts > 1 else 0)
 
     # ---- end to end through the public API: pinned host in, output back ----
     e2e = run_e2e(args, w, spec, engine, pkv, caches, n_layers, tables, bidx, pos, lens,
@@ -396,7 +396,8 @@ def run_ours(args, world, rank, local):
             "warmup": W, "ms_per_step": t_max / K, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": WORKLOAD_DESC, "global_batch": B * world, "seq_len": "100-1024",
-                       "num_splits": ws.splits, "layer_caches_cycled": n_layers,
+                       "num_splits": ws.splits or "auto (length-balanced parts)",
+                       "max_parts_per_row": ws.max_parts, "layer_caches_cycled": n_layers,
                        "l2_policy": f"inputs larger than L2: {n_layers} layer caches of "
                                     f"{caches[0][0].numel() * 4 / 2**20:.0f} MiB cycled; "
                                     f"{kv_step / 2**20:.0f} MiB of K/V read per step",
@@ -404,8 +405,8 @@ def run_ours(args, world, rank, local):
                        "parallelism": f"replicas x{world}"},
             "roofline": {"bound": "hbm", "achieved": attn_gbs, "peak": peak, "unit": "GB/s",
                          "frac": attn_gbs / peak, "peak_kind": peak_kind,
-                         "kernel": "decode_split_kernel<128> + combine_kernel",
-                         "traffic": profile_traffic("rollout_decode_split_128")},
+                         "kernel": "decode_attn_kernel<128> + combine_kernel",
+                         "traffic": profile_traffic("rollout_decode_attn_128")},
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": K * launches_per_step,

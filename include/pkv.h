@@ -152,16 +152,22 @@ int qk_norm_rope(pkv_bf16 *q, pkv_bf16 *k, const pkv_bf16 *gamma_q,
  *   out[b][h] = sum_j softmax_j(scale * q[b][h] . k_j) v_j
  * Rows with L <= 0 or slot 0 give exact zeros.
  *
- * Split-KV: each (row, kv head) key range is cut into num_splits parts
- * processed by separate CTAs that each write an fp32 partial output and
- * log-sum-exp to the workspace; a combine kernel merges them. num_splits 0
- * picks paged_decode_attn_splits(). The workspace must hold
- * paged_decode_attn_workspace(B, Hq, D, splits) bytes (16-byte aligned;
- * may be NULL when that is 0).
- *
+ * Split-KV: the (row, kv head) key ranges are cut into parts of whole
+ * 64-key tiles processed by persistent CTAs; a row cut into several parts
+ * gets fp32 partial outputs and log-sum-exps in the workspace that a combine
+ * kernel merges. num_splits 0 (automatic) picks one part size for the call
+ * on the device from the actual lengths so that all SMs get the same amount
+ * of work; num_splits S > 0 cuts every row into at most S equal parts.
+ * The workspace must hold paged_decode_attn_workspace(B, Hq, D, P) bytes
+ * (16-byte aligned; may be NULL when that is 0), with P = S for a fixed
+ * split count or P = paged_decode_attn_splits(...) for the automatic mode.
+ * Every workspace field is written by a call before that call reads it, so
+ * the workspace needs no initialisation; calls sharing one workspace must
+ * not overlap on the GPU.
  * q: bf16 [B][Hq][D], out: bf16 [B][Hq][D], caches and table as above.
  * Requires D in {64, 128, 256, 512}, 1 <= Hq/Hkv <= 8, Hq % Hkv == 0,
- * page_size a power of two >= 8, and 16-byte aligned q, out, caches.
+ * page_size a power of two >= 8, B <= 2048, and 16-byte aligned q, out,
+ * caches.
  * Table entries that are negative or >= n_pages inside a row's key range
  * set PKV_ERR_PAGE_* (that row's output is then unspecified); L beyond
  * max_pages_per_seq * page_size sets PKV_ERR_POS and is clamped.
@@ -174,11 +180,12 @@ int paged_decode_attn(const pkv_bf16 *q, const pkv_bf16 *k_cache,
                       int Hq, int Hkv, int D, int num_splits, void *workspace,
                       size_t workspace_bytes, pkv_bf16 *out,
                       int32_t *err_word, void *stream);
-/* the split count num_splits = 0 resolves to for this shape (depends only on
- * the arguments and the device's SM count) */
+/* the most parts a row can be cut into by the automatic mode (num_splits 0):
+ * one per 64-key tile of the longest row the table allows (of the window plus
+ * one when window > 0); size the workspace with it */
 int paged_decode_attn_splits(int B, int Hkv, int D, int max_pages_per_seq,
                              int page_size, int window, int *num_splits);
-/* workspace bytes needed for num_splits splits (0 when num_splits == 1) */
+/* workspace bytes for up to num_splits parts per row (0 when num_splits <= 1) */
 size_t paged_decode_attn_workspace(int B, int Hq, int D, int num_splits);
 
 /* ---------------------------------------------------------------------

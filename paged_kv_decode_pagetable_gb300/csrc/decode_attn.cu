@@ -7,23 +7,31 @@
 // With L = pos + 1 the keys of row b are [lo, L), lo = max(0, L - W).
 //
 // Design (GB300):
-//   * grid (split, kv head, row); one CTA of 4 warps streams its share of
-//     the row's keys once for all G <= 8 query heads of the GQA group;
-//   * keys are processed in tiles of 64; each tile's K and V are staged in
-//     shared memory by TMA (cp.async.bulk.tensor, 128-byte swizzle), one
-//     box per (page segment, 64-column chunk), with separate K / V
-//     mbarriers and an NS-deep ring so the next tiles are in flight while
-//     the current one is computed;
-//   * S^T = K q^T and O^T = V^T P^T run on the tensor cores
+//   * work: the key tiles (64 keys) of every (row, kv head). In the default
+//     (balanced) mode the (row, kv head, tile) sequence is flattened from
+//     the actual lengths and every persistent CTA takes the same number of
+//     consecutive tiles; a fixed split count (each row cut into S equal
+//     parts) is also accepted. A (row, head) finished inside one CTA writes
+//     the output directly; one that straddles CTAs leaves fp32 partials +
+//     log2-sum-exp that a combine kernel merges;
+//   * persistent CTAs (a fixed grid of SMs x CTAs/SM), each with one
+//     producer warp and four consumer warps. The producer streams, across
+//     all of the CTA's work without pausing, the query rows (cp.async.bulk)
+//     and the K and V tiles (cp.async.bulk.tensor, one box per page segment
+//     and 64-column chunk, 128-byte swizzle) into rings of shared-memory
+//     stages guarded by full / empty mbarriers, looking up the page ids of
+//     the next run of tiles before it waits on the current one;
+//   * the kernel and the combine are launched as programmatic dependents of
+//     the previous kernel in the stream (griddepcontrol), so launch latency
+//     and barrier set-up overlap the previous kernel's tail;
+//   * consumers compute S^T = K q^T and O^T = V^T P^T on the tensor cores
 //     (mma.sync m16n8k16 bf16 -> fp32) with keys / head-dim on M and the
-//     query heads on N, so no head padding beyond N = 8 is paid;
-//   * online softmax in the exp2 domain with a CTA-wide running max; P is
-//     exchanged through a 1 KB shared buffer;
-//   * each split writes an fp32 partial output and its log2-sum-exp; a
-//     combine kernel merges splits (skipped when there is one split);
-//   * every wait is bounded; a wait that gives up sets PKV_ERR_TIMEOUT and
-//     the CTA drains its copies and exits. Invalid table entries are
-//     reported through the error word and never dereferenced.
+//     <= 8 query heads of the GQA group on N, with an online softmax in the
+//     exp2 domain and a CTA-wide running max (P through a 1 KB buffer);
+//   * every mbarrier wait is bounded; a wait that gives up sets
+//     PKV_ERR_TIMEOUT, the CTA stops issuing, drains its copies and exits.
+//     Invalid table entries are reported in the error word and never
+//     dereferenced.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -35,26 +43,34 @@
 
 namespace {
 
-constexpr int kT = 64;          // keys per tile
-constexpr int kWarps = 4;
-constexpr int kThreads = kWarps * 32;
-constexpr int kMaxG = 8;        // query heads per kv head (MMA N)
-constexpr int kSpinLimit = 1 << 21;
+constexpr int kT = 64;               // keys per tile
+constexpr int kCWarps = 4;           // consumer warps
+constexpr int kCThreads = kCWarps * 32;
+constexpr int kThreads = kCThreads + 32;   // + producer warp
+constexpr int kMaxG = 8;             // query heads per kv head (MMA N)
+constexpr int kMaxRows = 512;        // rows per call (row cache kept in smem)
+constexpr int kSpinLimit = 1 << 22;
 
 template <int D>
 struct Cfg {
-  static constexpr int NS = D <= 64 ? 4 : D <= 128 ? 3 : D <= 256 ? 2 : 1;
+  static constexpr int NS = D <= 64 ? 6 : D <= 128 ? 3 : D <= 256 ? 3 : 1;
   static constexpr int CHUNKS = D / 64;             // 128-byte column chunks
-  static constexpr int CHUNK_BYTES = kT * 128;      // one chunk of one tile
+  static constexpr int CHUNK_BYTES = kT * 128;      // one column chunk of a tile
   static constexpr int STAGE_BYTES = kT * D * 2;
+  static constexpr int Q_ROW = D * 2 + 16;          // padded: conflict-free B-fragment loads
+  static constexpr int Q_BYTES = kMaxG * Q_ROW;
   static constexpr int OFF_V = NS * STAGE_BYTES;
-  static constexpr int OFF_P = 2 * NS * STAGE_BYTES;
-  static constexpr int OFF_RED = OFF_P + kT * 16;            // 2 x [4][8] f32
-  static constexpr int OFF_BAR = OFF_RED + 2 * kWarps * kMaxG * 4;
-  static constexpr int OFF_MASK = OFF_BAR + 2 * NS * 8;      // 2 x NS u32
-  static constexpr int OFF_FLAG = OFF_MASK + 2 * NS * 4;
-  static constexpr int SMEM = OFF_FLAG + 16 + 1024;          // + alignment slack
-  static constexpr int MIN_BLOCKS = D <= 128 ? 2 : 1;
+  static constexpr int OFF_Q = 2 * NS * STAGE_BYTES;
+  static constexpr int OFF_P = OFF_Q + 2 * Q_BYTES;
+  static constexpr int OFF_RED = OFF_P + kT * 16;                // 2 x [4][8] f32
+  static constexpr int OFF_BAR = OFF_RED + 2 * kCWarps * kMaxG * 4;
+  static constexpr int N_BARS = 4 * NS + 4;
+  static constexpr int OFF_MASK = OFF_BAR + N_BARS * 8;           // 2 x NS u32
+  static constexpr int OFF_MISC = OFF_MASK + 2 * NS * 4;          // abort flag
+  static constexpr int OFF_ROWS = OFF_MISC + 16;                  // int2 [kMaxRows]
+  static constexpr int OFF_PRE = OFF_ROWS + kMaxRows * 8;         // int [kMaxRows + 1]
+  static constexpr int SMEM = OFF_PRE + (kMaxRows + 1) * 4 + 1024;  // + alignment
+  static constexpr int CTAS_PER_SM = D <= 128 ? 2 : 1;
 };
 
 // ---------------------------------------------------------------- PTX ----
@@ -69,6 +85,9 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
                "r"(bytes)
                : "memory");
 }
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -80,11 +99,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Bounded wait: gives up after kSpinLimit polls (each poll may suspend the
-// thread for a hardware-defined interval).
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  for (int i = 0; i < kSpinLimit; ++i)
+// Bounded wait. Gives up after kSpinLimit polls (each poll may suspend the
+// thread for a hardware-defined time) or as soon as the CTA aborts.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                          volatile int *abort_flag) {
+  for (int i = 0; i < kSpinLimit; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 63) == 63 && *abort_flag) return false;
+  }
   return false;
 }
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *tm,
@@ -95,8 +117,21 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *tm,
       "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(bar)
       : "memory");
 }
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void prefetch_l2(const void *ptr) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
+}
 __device__ __forceinline__ void fence_proxy_async() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void consumer_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kCThreads) : "memory");
 }
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1,
                                         uint32_t &r2, uint32_t &r3) {
@@ -124,381 +159,652 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t *>(&v);
 }
 
-// byte offset of 16-byte chunk `chunk` (8 bf16 along D) of tile row `r`
-// inside one stage laid out by TMA with SWIZZLE_128B: column chunks of 64
-// elements are separate [kT][128 B] blocks; inside a 1024-byte atom the
-// 16-byte unit index is XORed with the row index mod 8.
+// Byte offset of 16-byte chunk `chunk` (8 bf16 along D) of tile row `r` in a
+// stage written by TMA with SWIZZLE_128B: 64-column chunks are separate
+// [kT][128 B] blocks; inside a 1024-byte atom the 16-byte unit index is
+// XORed with the row index mod 8.
 __device__ __forceinline__ uint32_t swz(int r, int chunk) {
   return static_cast<uint32_t>((chunk >> 3) * (kT * 128) + r * 128 +
                                (((chunk & 7) ^ (r & 7)) << 4));
 }
 
-// ------------------------------------------------------------- kernel ----
-template <int D>
-__global__ void __launch_bounds__(kThreads, Cfg<D>::MIN_BLOCKS)
-    decode_split_kernel(const __grid_constant__ CUtensorMap tmK,
-                        const __grid_constant__ CUtensorMap tmV,
-                        const __nv_bfloat16 *__restrict__ q,
-                        const int32_t *__restrict__ table, int n_slots,
-                        int max_pages, int log2_ps, int n_pages,
-                        const int32_t *__restrict__ batch_idx,
-                        const int32_t *__restrict__ seq_lens, int window,
-                        float scale_log2, int Hq, int G, int S,
-                        float *__restrict__ o_part, float *__restrict__ lse_part,
-                        __nv_bfloat16 *__restrict__ out, int32_t *__restrict__ err) {
-  using C = Cfg<D>;
-  const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int gid = lane >> 2, tig = lane & 3;
-  const int ps = 1 << log2_ps;
-  const bool reporter = (s == 0 && g == 0 && tid == 0);
+// ------------------------------------------------------- row geometry ----
+struct Problem {
+  const int32_t *table, *batch_idx, *seq_lens;
+  int n_slots, max_pages, log2_ps, n_pages, window, B, Hq, Hkv, G;
+  int fixed_splits;   // > 0: each row cut into at most this many parts; 0: balanced
+  int max_parts;      // partial slots per (row, head) in the workspace
+};
 
-  // ---- this CTA's key range (identical in every thread) ----
-  int slot = batch_idx ? batch_idx[b] : b;
-  int L = seq_lens[b];
+struct RowInfo {
+  int slot, L, lo, t_first, n_tiles;
+};
+
+// Row b's slot, clamped length and key-tile range, read from global memory;
+// errors are reported by the caller-selected thread.
+__device__ __forceinline__ RowInfo row_info(const Problem &p, int b, int32_t *err,
+                                            bool report) {
+  RowInfo r;
+  r.slot = p.batch_idx ? p.batch_idx[b] : b;
+  r.L = p.seq_lens[b];
   bool empty = false;
-  if (slot < 0 || slot >= n_slots) {
-    if (reporter && err) atomicOr(err, PKV_ERR_SLOT);
+  if (r.slot < 0 || r.slot >= p.n_slots) {
+    if (report && err) atomicOr(err, PKV_ERR_SLOT);
     empty = true;
   }
-  const int Lmax = max_pages << log2_ps;
-  if (L > Lmax || L < 0) {
-    if (reporter && err) atomicOr(err, PKV_ERR_POS);
-    L = L < 0 ? 0 : Lmax;
+  const int Lmax = p.max_pages << p.log2_ps;
+  if (r.L > Lmax || r.L < 0) {
+    if (report && err) atomicOr(err, PKV_ERR_POS);
+    r.L = r.L < 0 ? 0 : Lmax;
   }
-  if (slot == 0 || L <= 0) empty = true;
-  const int lo = window > 0 ? max(0, L - window) : 0;
-  const int t_first = lo / kT, t_end = (L + kT - 1) / kT;
-  const int per = (t_end - t_first + S - 1) / S;
-  const int ta = t_first + s * per, tb = min(t_end, ta + per);
-  const int k0 = max(lo, ta * kT), k1 = min(L, tb * kT);
-  const size_t head0 = static_cast<size_t>(b) * Hq + static_cast<size_t>(g) * G;
+  if (r.slot == 0 || r.L <= 0) empty = true;
+  r.lo = p.window > 0 ? max(0, r.L - p.window) : 0;
+  r.t_first = r.lo / kT;
+  r.n_tiles = empty ? 0 : (r.L + kT - 1) / kT - r.t_first;
+  return r;
+}
 
-  if (empty || ta >= tb) {
-    if (S == 1) {
-      for (int i = tid; i < G * D; i += kThreads)
-        out[head0 * D + i] = __float2bfloat16_rn(0.f);
-    } else if (tid < G) {
-      lse_part[(head0 + tid) * S + s] = -INFINITY;
-    }
-    return;
+// Same, from the per-CTA shared-memory copy {slot, clamped L}.
+__device__ __forceinline__ RowInfo row_cached(const Problem &p, int2 c) {
+  RowInfo r;
+  r.slot = c.x;
+  r.L = c.y;
+  r.lo = p.window > 0 ? max(0, r.L - p.window) : 0;
+  r.t_first = r.lo / kT;
+  r.n_tiles = (r.slot <= 0 || r.L <= 0) ? 0 : (r.L + kT - 1) / kT - r.t_first;
+  return r;
+}
+
+__device__ __forceinline__ int fixed_parts(int n_tiles, int S) {
+  if (n_tiles <= 0) return 0;
+  const int ch = (n_tiles + S - 1) / S;
+  return (n_tiles + ch - 1) / ch;
+}
+
+// largest b in [0, B) with scale * pre[b] <= x (pre non-decreasing, pre[0] = 0);
+// the host guarantees Hkv * (tiles of all rows) < 2^31
+__device__ __forceinline__ int find_row(const int *pre, int B, int scale, int x) {
+  int lo = 0, hi = B;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (scale * pre[mid] <= x) lo = mid; else hi = mid;
   }
+  return lo;
+}
+
+// A run of key tiles of one (row, kv head) processed by one CTA.
+struct Unit {
+  int b, g, slot, ta, tb, k0, k1, part, parts;
+};
+
+// Walks this CTA's units. Balanced mode: the (row, kv head, tile) sequence
+// is flattened and every CTA owns the same number of consecutive tiles
+// (q = ceil(total / CTAs)); a (row, head) that straddles CTAs is finished
+// by the combine kernel. Fixed mode: units are (row, part, head) with each
+// row cut into at most S equal parts, dealt out in equal counts.
+struct UnitIter {
+  int pos, end;   // balanced: flattened tile index; fixed: unit index
+  int q;          // balanced: tiles per CTA
+};
+
+__device__ __forceinline__ bool next_unit(const Problem &p, const int2 *rows, const int *pre,
+                                          UnitIter &it, Unit &w) {
+  if (it.pos >= it.end) return false;
+  if (p.fixed_splits == 0) {
+    const int b = find_row(pre, p.B, p.Hkv, it.pos);
+    const RowInfo r = row_cached(p, rows[b]);
+    const int tiles = pre[b + 1] - pre[b];
+    const int within = it.pos - p.Hkv * pre[b];
+    w.g = within / tiles;
+    const int t0 = within - w.g * tiles;
+    const int n = min(tiles - t0, it.end - it.pos);
+    const int s_rh = p.Hkv * pre[b] + w.g * tiles;
+    const int first_cta = s_rh / it.q, last_cta = (s_rh + tiles - 1) / it.q;
+    w.b = b;
+    w.slot = r.slot;
+    w.ta = r.t_first + t0;
+    w.tb = w.ta + n;
+    w.parts = last_cta - first_cta + 1;
+    w.part = it.pos / it.q - first_cta;
+    w.k0 = max(r.lo, w.ta * kT);
+    w.k1 = min(r.L, w.tb * kT);
+    it.pos += n;
+  } else {
+    const int rc = it.pos / p.Hkv;
+    w.g = it.pos - rc * p.Hkv;
+    const int b = find_row(pre, p.B, 1, rc);
+    const RowInfo r = row_cached(p, rows[b]);
+    const int ch = (r.n_tiles + p.fixed_splits - 1) / p.fixed_splits;
+    w.b = b;
+    w.slot = r.slot;
+    w.part = rc - pre[b];
+    w.parts = pre[b + 1] - pre[b];
+    w.ta = r.t_first + w.part * ch;
+    w.tb = min(r.t_first + r.n_tiles, w.ta + ch);
+    w.k0 = max(r.lo, w.ta * kT);
+    w.k1 = min(r.L, w.tb * kT);
+    it.pos += 1;
+  }
+  return true;
+}
+
+// ------------------------------------------------------------- kernel ----
+template <int D>
+__global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
+    decode_attn_kernel(const __grid_constant__ CUtensorMap tmK,
+                       const __grid_constant__ CUtensorMap tmV,
+                       const __nv_bfloat16 *__restrict__ q, const Problem p,
+                       float scale_log2, float *__restrict__ o_part,
+                       float *__restrict__ lse_part, int *__restrict__ parts_out,
+                       __nv_bfloat16 *__restrict__ out, int32_t *__restrict__ err) {
+  using Cf = Cfg<D>;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const uint32_t sK = smem_u32(sm), sV = sK + C::OFF_V, sP = sK + C::OFF_P;
-  float *red_max = reinterpret_cast<float *>(sm + C::OFF_RED);
-  float *red_sum = red_max + kWarps * kMaxG;
-  const uint32_t barK = sK + C::OFF_BAR, barV = barK + C::NS * 8;
-  uint32_t *kmask = reinterpret_cast<uint32_t *>(sm + C::OFF_MASK);
-  uint32_t *vmask = kmask + C::NS;
-  volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + C::OFF_FLAG);
+  const uint32_t sK = smem_u32(sm), sV = sK + Cf::OFF_V, sQ = sK + Cf::OFF_Q;
+  const uint32_t sP = sK + Cf::OFF_P;
+  float *red_max = reinterpret_cast<float *>(sm + Cf::OFF_RED);
+  float *red_sum = red_max + kCWarps * kMaxG;
+  const uint32_t bar0 = sK + Cf::OFF_BAR;
+  // barrier layout: fullK[NS] emptyK[NS] fullV[NS] emptyV[NS] fullQ[2] emptyQ[2]
+  const uint32_t fullK = bar0, emptyK = bar0 + 8 * Cf::NS, fullV = bar0 + 16 * Cf::NS,
+                 emptyV = bar0 + 24 * Cf::NS, fullQ = bar0 + 32 * Cf::NS,
+                 emptyQ = fullQ + 16;
+  uint32_t *kmask = reinterpret_cast<uint32_t *>(sm + Cf::OFF_MASK);
+  uint32_t *vmask = kmask + Cf::NS;
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + Cf::OFF_MISC);
+  int2 *rows = reinterpret_cast<int2 *>(sm + Cf::OFF_ROWS);
+  int *pre = reinterpret_cast<int *>(sm + Cf::OFF_PRE);
 
-  const int box_rows = ps < kT ? ps : kT;
-  const int boxes = kT / box_rows;
-  const uint32_t all_boxes = boxes == 32 ? 0xffffffffu : ((1u << boxes) - 1u);
-  const int n_local = tb - ta;
-  const int32_t *trow = table + static_cast<size_t>(slot) * max_pages;
-
-  // producer (thread 0): stage tile t of K (is_v=0) or V (is_v=1)
-  auto issue = [&](int t, int stage, int is_v) {
-    const CUtensorMap *tm = is_v ? &tmV : &tmK;
-    const uint32_t dst0 = (is_v ? sV : sK) + stage * C::STAGE_BYTES;
-    const uint32_t bar = (is_v ? barV : barK) + stage * 8;
-    uint32_t mask = 0;
-    int rows[kT / 8];
-    for (int i = 0; i < boxes; ++i) {
-      const int key = t * kT + i * box_rows;
-      rows[i] = -1;
-      if (key + box_rows <= k0 || key >= k1) continue;
-      const int page = trow[key >> log2_ps];
-      if (page < 0) {
-        if (err) atomicOr(err, PKV_ERR_PAGE_NEG);
-        continue;
-      }
-      if (page >= n_pages) {
-        if (err) atomicOr(err, PKV_ERR_PAGE_RANGE);
-        continue;
-      }
-      rows[i] = ((g * n_pages + page) << log2_ps) + (key & (ps - 1));
-      mask |= 1u << i;
-    }
-    (is_v ? vmask : kmask)[stage] = mask;
-    mbar_expect_tx(bar, static_cast<uint32_t>(__popc(mask)) * C::CHUNKS * box_rows * 128);
-    for (int i = 0; i < boxes; ++i) {
-      if (rows[i] < 0) continue;
-#pragma unroll
-      for (int cc = 0; cc < C::CHUNKS; ++cc)
-        tma_load_2d(dst0 + cc * C::CHUNK_BYTES + i * box_rows * 128, tm, cc * 64,
-                    rows[i], bar);
-    }
-  };
-
+  // ---- set-up: barriers, row cache, per-row tile or part prefix sums ----
   if (tid == 0) {
-    for (int i = 0; i < C::NS; ++i) {
-      mbar_init(barK + i * 8, 1);
-      mbar_init(barV + i * 8, 1);
+    for (int i = 0; i < Cf::NS; ++i) {
+      mbar_init(fullK + 8 * i, 1);
+      mbar_init(emptyK + 8 * i, 1);
+      mbar_init(fullV + 8 * i, 1);
+      mbar_init(emptyV + 8 * i, kCWarps);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(fullQ + 8 * i, 1);
+      mbar_init(emptyQ + 8 * i, kCWarps);
     }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     fence_proxy_async();
   }
-  __syncthreads();
-  // copies issued / completions observed, tracked by thread 0 only
-  int issued_k = 0, issued_v = 0, waited_k = 0, waited_v = 0;
-  if (tid == 0) {
-    for (; issued_k < min(C::NS, n_local); ++issued_k) issue(ta + issued_k, issued_k, 0);
-    for (; issued_v < min(C::NS - 1, n_local); ++issued_v) issue(ta + issued_v, issued_v, 1);
-  }
-
-  // Q^T as MMA B fragments (N = head gid, K = head dim), zero for gid >= G
-  constexpr int KS = D / 16;
-  uint32_t qb[KS][2];
+  // Warm L2 with the row metadata and the page table while the previous
+  // kernel finishes: prefetches only pull lines into L2 (the point of
+  // coherence), so they cannot observe stale data; the reads that count
+  // come after the grid dependency wait.
   {
-    const bool hv = gid < G;
-    const uint32_t *qrow =
-        reinterpret_cast<const uint32_t *>(q + (head0 + (hv ? gid : 0)) * D);
+    const int gt = blockIdx.x * kThreads + tid, gs = gridDim.x * kThreads;
+    for (int i = gt * 32; i < p.B; i += gs * 32) {
+      prefetch_l2(p.seq_lens + i);
+      if (p.batch_idx) prefetch_l2(p.batch_idx + i);
+    }
+    const long long tbl = 1LL * p.n_slots * p.max_pages;
+    const long long tlim = tbl < (1LL << 20) ? tbl : (1LL << 20);
+    for (long long i = 32LL * gt; i < tlim; i += 32LL * gs) prefetch_l2(p.table + i);
+  }
+  pkv_grid_dependency_sync();
+  for (int b = tid; b < p.B; b += kThreads) {
+    const RowInfo r = row_info(p, b, err, blockIdx.x == 0);
+    rows[b] = make_int2(r.n_tiles > 0 ? r.slot : -1, r.L);
+    pre[b + 1] = p.fixed_splits > 0 ? fixed_parts(r.n_tiles, p.fixed_splits) : r.n_tiles;
+  }
+  __syncthreads();
+  if (warp == 0) {  // inclusive scan of pre[1..B] in chunks of 32
+    int carry = 0;
+    for (int base = 0; base < p.B; base += 32) {
+      const int i = base + lane;
+      int v = i < p.B ? pre[i + 1] : 0;
 #pragma unroll
-    for (int ks = 0; ks < KS; ++ks) {
-      qb[ks][0] = hv ? qrow[(16 * ks + 2 * tig) >> 1] : 0u;
-      qb[ks][1] = hv ? qrow[(16 * ks + 8 + 2 * tig) >> 1] : 0u;
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += t;
+      }
+      if (i < p.B) pre[i + 1] = v + carry;
+      carry += __shfl_sync(0xffffffffu, v, 31);
+    }
+    if (lane == 0) pre[0] = 0;
+  }
+  __syncthreads();
+  UnitIter it0;
+  {
+    const int total = p.Hkv * pre[p.B];
+    if (p.fixed_splits == 0) {
+      const int grid = static_cast<int>(gridDim.x);
+      it0.q = total > 0 ? (total + grid - 1) / grid : 1;
+      it0.pos = static_cast<int>(min(static_cast<long long>(total), 1LL * it0.q * blockIdx.x));
+      it0.end = min(total, it0.pos + it0.q);
+    } else {
+      it0.q = 1;
+      it0.pos = static_cast<int>(1LL * total * blockIdx.x / gridDim.x);
+      it0.end = static_cast<int>(1LL * total * (blockIdx.x + 1) / gridDim.x);
+    }
+    if (parts_out) {  // parts per (row, kv head) for the combine, spread over the CTAs
+      for (int rh = blockIdx.x + gridDim.x * tid; rh < p.B * p.Hkv; rh += gridDim.x * kThreads) {
+        const int b = rh / p.Hkv, g = rh - b * p.Hkv;
+        const int n = pre[b + 1] - pre[b];
+        int parts = n;
+        if (p.fixed_splits == 0 && n > 0) {
+          const int s_rh = p.Hkv * pre[b] + g * n;
+          parts = (s_rh + n - 1) / it0.q - s_rh / it0.q + 1;
+        }
+        parts_out[rh] = parts;
+      }
     }
   }
 
-  constexpr int MT = D / 64;  // 16-row m-tiles of this warp's D/4 slice
-  float o[MT][4];
-#pragma unroll
-  for (int mt = 0; mt < MT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
-  float m_run0 = -INFINITY, m_run1 = -INFINITY, l_run0 = 0.f, l_run1 = 0.f;
-  const int h0 = 2 * tig, h1 = 2 * tig + 1;
-  const bool hv0 = h0 < G, hv1 = h1 < G;
-  int lt = 0;
-  bool aborted = false;
+  // rows with no key: zero output (rows spread over the CTAs)
+  if (warp < kCWarps) {
+    for (int b = blockIdx.x; b < p.B; b += gridDim.x) {
+      if (pre[b + 1] != pre[b]) continue;
+      __nv_bfloat16 *o = out + static_cast<size_t>(b) * p.Hq * D;
+      for (int i = tid; i < p.Hq * D; i += kCThreads) o[i] = __float2bfloat16_rn(0.f);
+    }
+  }
 
-  for (; lt < n_local; ++lt) {
-    const int t = ta + lt, st = lt % C::NS;
-    const uint32_t par = (lt / C::NS) & 1;
-    if (mbar_wait(barK + st * 8, par))
-      waited_k = lt + 1;
-    else
-      *abort_flag = 1;
-    const uint32_t km = kmask[st];
-    const uint32_t kbase = sK + st * C::STAGE_BYTES;
+  const int ps = 1 << p.log2_ps;
+  const int box_rows = ps < kT ? ps : kT;
+  const int boxes = kT / box_rows;
+  const uint32_t all_boxes = (1u << boxes) - 1u;
 
-    // ---- S^T[16 keys x 8 heads] for keys 16*warp .. +15 of the tile ----
-    float sacc[4] = {0.f, 0.f, 0.f, 0.f};
-    {
-      const int mi = lane >> 3;
-      const int r = 16 * warp + ((mi & 1) << 3) + (lane & 7);
-#pragma unroll
-      for (int ks = 0; ks < KS; ++ks) {
-        uint32_t a0, a1, a2, a3;
-        ldsm_x4(kbase + swz(r, 2 * ks + (mi >> 1)), a0, a1, a2, a3);
-        mma_bf16(sacc, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+  if (warp == kCWarps) {
+    // ======================== producer (one warp) ========================
+    // Lane j looks up box j of a unit (a page segment of one tile); the
+    // lookups for the next unit are issued before the current unit's copies
+    // so that their latency hides behind the ring that is already in flight.
+    // box_page issues the table load only; box_row checks the entry when
+    // it is used, so a look-ahead load never stalls the warp.
+    auto box_page = [&](const Unit &u, int j) -> int {
+      const int n_boxes = (u.tb - u.ta) * boxes;
+      if (j >= n_boxes) return -1;
+      const int t = u.ta + j / boxes, i = j % boxes;
+      const int key = t * kT + i * box_rows;
+      if (key + box_rows <= u.k0 || key >= u.k1) return -1;
+      const int32_t *trow = p.table + static_cast<size_t>(u.slot) * p.max_pages;
+      return __ldg(trow + (key >> p.log2_ps));
+    };
+    auto box_row = [&](const Unit &u, int j, int page) -> int {
+      const int n_boxes = (u.tb - u.ta) * boxes;
+      if (j >= n_boxes) return -1;
+      const int t = u.ta + j / boxes, i = j % boxes;
+      const int key = t * kT + i * box_rows;
+      if (key + box_rows <= u.k0 || key >= u.k1) return -1;
+      if (page < 0) {
+        if (err) atomicOr(err, PKV_ERR_PAGE_NEG);
+        return -1;
       }
-    }
-    const int kr_lo = 16 * warp + gid, kr_hi = kr_lo + 8;
-    const int key_lo = t * kT + kr_lo, key_hi = t * kT + kr_hi;
-    const bool v_lo = key_lo >= k0 && key_lo < k1 && ((km >> (kr_lo / box_rows)) & 1u);
-    const bool v_hi = key_hi >= k0 && key_hi < k1 && ((km >> (kr_hi / box_rows)) & 1u);
-    float s00 = (v_lo && hv0) ? sacc[0] * scale_log2 : -INFINITY;
-    float s01 = (v_lo && hv1) ? sacc[1] * scale_log2 : -INFINITY;
-    float s10 = (v_hi && hv0) ? sacc[2] * scale_log2 : -INFINITY;
-    float s11 = (v_hi && hv1) ? sacc[3] * scale_log2 : -INFINITY;
-    float mx0 = fmaxf(s00, s10), mx1 = fmaxf(s01, s11);
-#pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-    }
-    if (gid == 0) {
-      red_max[warp * kMaxG + h0] = mx0;
-      red_max[warp * kMaxG + h1] = mx1;
-    }
-    __syncthreads();  // (1) K stage consumed; maxima visible
-    if (*abort_flag) {
-      aborted = true;
-      break;
-    }
-    if (tid == 0) {
-      fence_proxy_async();
-      if (issued_k < n_local) {
-        issue(ta + issued_k, issued_k % C::NS, 0);
-        ++issued_k;
+      if (page >= p.n_pages) {
+        if (err) atomicOr(err, PKV_ERR_PAGE_RANGE);
+        return -1;
       }
-      if (issued_v < n_local && issued_v <= lt + C::NS - 1) {
-        issue(ta + issued_v, issued_v % C::NS, 1);
-        ++issued_v;
+      return ((u.g * p.n_pages + page) << p.log2_ps) + (key & (ps - 1));
+    };
+    UnitIter it = it0;
+    Unit w, wn;
+    int it_k = 0, it_v = 0, it_q = 0;
+    bool ok = true;
+    bool have = next_unit(p, rows, pre, it, w);
+    int page_first = have ? box_page(w, lane) : -1;
+    while (ok && have) {
+      bool have_next = false, looked_ahead = false;
+      int page_next = -1;
+      const int n_boxes = (w.tb - w.ta) * boxes;
+      // query rows of the GQA group, one bulk copy per head into padded rows
+      {
+        const int qs = it_q & 1;
+        if (lane == 0) {
+          ok = mbar_wait(emptyQ + 8 * qs, ((it_q >> 1) & 1) ^ 1, abort_flag);
+          if (ok) mbar_expect_tx(fullQ + 8 * qs, static_cast<uint32_t>(p.G * D * 2));
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        if (lane < p.G)
+          bulk_load(sQ + qs * Cf::Q_BYTES + lane * Cf::Q_ROW,
+                    q + ((static_cast<size_t>(w.b) * p.Hq + static_cast<size_t>(w.g) * p.G +
+                          lane) * D),
+                    static_cast<uint32_t>(D * 2), fullQ + 8 * qs);
+        ++it_q;
       }
-    }
-    float mt0 = red_max[h0], mt1 = red_max[h1];
+      for (int base = 0; base < n_boxes && ok; base += 32) {
+        const int row = box_row(w, base + lane, base == 0 ? page_first : box_page(w, base + lane));
+        const int tiles_here = min(32, n_boxes - base) / boxes;
+        for (int tt = 0; tt < tiles_here && ok; ++tt) {
+          uint32_t mask = 0;
+          int r0 = -1, r1 = -1, r2 = -1, r3 = -1, r4 = -1, r5 = -1, r6 = -1, r7 = -1;
 #pragma unroll
-    for (int w = 1; w < kWarps; ++w) {
-      mt0 = fmaxf(mt0, red_max[w * kMaxG + h0]);
-      mt1 = fmaxf(mt1, red_max[w * kMaxG + h1]);
-    }
-    const float mn0 = fmaxf(m_run0, mt0), mn1 = fmaxf(m_run1, mt1);
-    const float mu0 = mn0 == -INFINITY ? 0.f : mn0;
-    const float mu1 = mn1 == -INFINITY ? 0.f : mn1;
-    const float p00 = exp2f(s00 - mu0), p01 = exp2f(s01 - mu1);
-    const float p10 = exp2f(s10 - mu0), p11 = exp2f(s11 - mu1);
-    {
-      uint32_t *pt = reinterpret_cast<uint32_t *>(sm + C::OFF_P);
-      pt[kr_lo * 4 + tig] = pack_bf16(p00, p01);
-      pt[kr_hi * 4 + tig] = pack_bf16(p10, p11);
-    }
-    float sm0 = p00 + p10, sm1 = p01 + p11;
+          for (int i = 0; i < kT / 8; ++i) {
+            const int v = __shfl_sync(0xffffffffu, row, (tt * boxes + (i < boxes ? i : 0)) & 31);
+            const int rv = i < boxes ? v : -1;
+            if (rv >= 0) mask |= 1u << i;
+            switch (i) {
+              case 0: r0 = rv; break; case 1: r1 = rv; break; case 2: r2 = rv; break;
+              case 3: r3 = rv; break; case 4: r4 = rv; break; case 5: r5 = rv; break;
+              case 6: r6 = rv; break; default: r7 = rv; break;
+            }
+          }
+          if (lane == 0) {
+            const uint32_t bytes =
+                static_cast<uint32_t>(__popc(mask)) * Cf::CHUNKS * box_rows * 128;
+            for (int kv = 0; kv < 2 && ok; ++kv) {
+              const int itx = kv ? it_v : it_k;
+              const int st = itx % Cf::NS;
+              const uint32_t par = ((itx / Cf::NS) & 1) ^ 1;
+              if (!mbar_wait((kv ? emptyV : emptyK) + 8 * st, par, abort_flag)) {
+                ok = false;
+                break;
+              }
+              (kv ? vmask : kmask)[st] = mask;
+              const uint32_t full = (kv ? fullV : fullK) + 8 * st;
+              mbar_expect_tx(full, bytes);
+              const uint32_t dst0 = (kv ? sV : sK) + st * Cf::STAGE_BYTES;
+              const CUtensorMap *tm = kv ? &tmV : &tmK;
 #pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-      sm0 += __shfl_xor_sync(0xffffffffu, sm0, off);
-      sm1 += __shfl_xor_sync(0xffffffffu, sm1, off);
-    }
-    if (gid == 0) {
-      red_sum[warp * kMaxG + h0] = sm0;
-      red_sum[warp * kMaxG + h1] = sm1;
-    }
-    // ---- V tile: wait, then clear rows of keys outside [k0, k1) ----
-    if (mbar_wait(barV + st * 8, par))
-      waited_v = lt + 1;
-    else
-      *abort_flag = 1;
-    const uint32_t vm = vmask[st];
-    const uint32_t vbase = sV + st * C::STAGE_BYTES;
-    const bool full_tile = t * kT >= k0 && t * kT + kT <= k1 && vm == all_boxes;
-    if (!full_tile) {
-      const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-      for (int i = tid; i < kT * (D / 8); i += kThreads) {
-        const int r = i / (D / 8), c = i % (D / 8);
-        const int key = t * kT + r;
-        const bool valid = key >= k0 && key < k1 && ((vm >> (r / box_rows)) & 1u);
-        if (!valid)
-          *reinterpret_cast<uint4 *>(sm + C::OFF_V + st * C::STAGE_BYTES +
-                                     (c >> 3) * (kT * 128) + r * 128 + (c & 7) * 16) = z;
-      }
-      fence_proxy_async();
-    }
-    __syncthreads();  // (2) P, sums and V visible
-    if (*abort_flag) {
-      aborted = true;
-      break;
-    }
-    float ts0 = 0.f, ts1 = 0.f;
+              for (int i = 0; i < kT / 8; ++i) {
+                const int rv = i == 0 ? r0 : i == 1 ? r1 : i == 2 ? r2 : i == 3 ? r3
+                             : i == 4 ? r4 : i == 5 ? r5 : i == 6 ? r6 : r7;
+                if (rv < 0) continue;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-      ts0 += red_sum[w * kMaxG + h0];
-      ts1 += red_sum[w * kMaxG + h1];
-    }
-    const float al0 = exp2f(m_run0 - mu0), al1 = exp2f(m_run1 - mu1);
-    l_run0 = l_run0 * al0 + ts0;
-    l_run1 = l_run1 * al1 + ts1;
-    m_run0 = mn0;
-    m_run1 = mn1;
-    // ---- O^T[warp's D/4 slice x 8 heads] += V^T P^T ----
-#pragma unroll
-    for (int mt = 0; mt < MT; ++mt) {
-      o[mt][0] *= al0;
-      o[mt][1] *= al1;
-      o[mt][2] *= al0;
-      o[mt][3] *= al1;
-    }
-#pragma unroll
-    for (int kp = 0; kp < kT / 32; ++kp) {
-      uint32_t b0, b1, b2, b3;
-      ldsm_x4_t(sP + (32 * kp + lane) * 16, b0, b1, b2, b3);
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        const int ks = 2 * kp + half;
-        const uint32_t bb0 = half ? b2 : b0, bb1 = half ? b3 : b1;
-        const int mi = lane >> 3;
-        const int r = 16 * ks + ((mi >> 1) << 3) + (lane & 7);
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt) {
-          const int dchunk = (warp * (D / 4) + 16 * mt) / 8 + (mi & 1);
-          uint32_t a0, a1, a2, a3;
-          ldsm_x4_t(vbase + swz(r, dchunk), a0, a1, a2, a3);
-          mma_bf16(o[mt], a0, a1, a2, a3, bb0, bb1);
+                for (int cc = 0; cc < Cf::CHUNKS; ++cc)
+                  tma_load_2d(dst0 + cc * Cf::CHUNK_BYTES + i * box_rows * 128, tm, cc * 64,
+                              rv, full);
+              }
+              if (kv) ++it_v; else ++it_k;
+            }
+          }
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!looked_ahead) {  // next unit's table lookups, once this one is moving
+            looked_ahead = true;
+            have_next = next_unit(p, rows, pre, it, wn);
+            page_next = have_next ? box_page(wn, lane) : -1;
+          }
         }
       }
+      if (!looked_ahead) {
+        have_next = next_unit(p, rows, pre, it, wn);
+        page_next = have_next ? box_page(wn, lane) : -1;
+      }
+      w = wn;
+      page_first = page_next;
+      have = have_next;
     }
-  }
-
-  if (aborted) {
-    if (tid == 0) {
+    if (lane != 0) return;
+    if (!ok) {
+      *abort_flag = 1;
       if (err) atomicOr(err, PKV_ERR_TIMEOUT);
-      // drain every copy still in flight before the CTA's smem is released
-      for (int i = waited_k; i < issued_k; ++i)
-        (void)mbar_wait(barK + (i % C::NS) * 8, (i / C::NS) & 1);
-      for (int i = waited_v; i < issued_v; ++i)
-        (void)mbar_wait(barV + (i % C::NS) * 8, (i / C::NS) & 1);
+    }
+    // drain: the last phase armed on every stage must land before exit
+    volatile int no_abort = 0;
+    for (int s = 0; s < Cf::NS; ++s) {
+      if (it_k > s) {
+        const int last = s + ((it_k - 1 - s) / Cf::NS) * Cf::NS;
+        (void)mbar_wait(fullK + 8 * s, (last / Cf::NS) & 1, &no_abort);
+      }
+      if (it_v > s) {
+        const int last = s + ((it_v - 1 - s) / Cf::NS) * Cf::NS;
+        (void)mbar_wait(fullV + 8 * s, (last / Cf::NS) & 1, &no_abort);
+      }
+    }
+    for (int s = 0; s < 2; ++s) {
+      if (it_q > s) {
+        const int last = s + ((it_q - 1 - s) / 2) * 2;
+        (void)mbar_wait(fullQ + 8 * s, (last / 2) & 1, &no_abort);
+      }
     }
     return;
   }
 
-  // ---- epilogue ----
-  const float il0 = l_run0 > 0.f ? 1.f / l_run0 : 0.f;
-  const float il1 = l_run1 > 0.f ? 1.f / l_run1 : 0.f;
+  // ============================== consumers ==============================
+  const int gid = lane >> 2, tig = lane & 3;
+  const int h0 = 2 * tig, h1 = 2 * tig + 1;
+  const bool hv0 = h0 < p.G, hv1 = h1 < p.G;
+  constexpr int KS = D / 16;
+  constexpr int MT = D / 64;  // 16-row m-tiles of this warp's D/4 slice
+  int it = 0, it_q = 0;
+  bool failed = false;
+  UnitIter units = it0;
+  Unit w;
+
+  while (next_unit(p, rows, pre, units, w)) {
+    uint32_t qb[KS][2];
+    {
+      const int qs = it_q & 1;
+      if (!mbar_wait(fullQ + 8 * qs, (it_q >> 1) & 1, abort_flag)) {
+        failed = true;
+        *abort_flag = 1;
+      }
+      const bool hv = gid < p.G;
+      const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
+          sm + Cf::OFF_Q + qs * Cf::Q_BYTES + (hv ? gid : 0) * Cf::Q_ROW);
 #pragma unroll
-  for (int mt = 0; mt < MT; ++mt) {
-    const int d = warp * (D / 4) + 16 * mt + gid;
-    if (S == 1) {
-      if (hv0) {
-        out[(head0 + h0) * D + d] = __float2bfloat16_rn(o[mt][0] * il0);
-        out[(head0 + h0) * D + d + 8] = __float2bfloat16_rn(o[mt][2] * il0);
+      for (int ks = 0; ks < KS; ++ks) {
+        qb[ks][0] = hv ? qrow[(16 * ks + 2 * tig) >> 1] : 0u;
+        qb[ks][1] = hv ? qrow[(16 * ks + 8 + 2 * tig) >> 1] : 0u;
       }
-      if (hv1) {
-        out[(head0 + h1) * D + d] = __float2bfloat16_rn(o[mt][1] * il1);
-        out[(head0 + h1) * D + d + 8] = __float2bfloat16_rn(o[mt][3] * il1);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(emptyQ + 8 * qs);
+      ++it_q;
+    }
+    float o[MT][4];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+    float m_run0 = -INFINITY, m_run1 = -INFINITY, l_run0 = 0.f, l_run1 = 0.f;
+
+    for (int t = w.ta; t < w.tb; ++t, ++it) {
+      const int st = it % Cf::NS;
+      const uint32_t par = (it / Cf::NS) & 1;
+      if (!mbar_wait(fullK + 8 * st, par, abort_flag)) {
+        failed = true;
+        *abort_flag = 1;
       }
-    } else {
-      if (hv0) {
-        float *op = o_part + ((head0 + h0) * S + s) * D;
-        op[d] = o[mt][0] * il0;
-        op[d + 8] = o[mt][2] * il0;
+      const uint32_t km = kmask[st];
+      const uint32_t kbase = sK + st * Cf::STAGE_BYTES;
+
+      // ---- S^T[16 keys x 8 heads], keys 16*warp .. +15 of the tile ----
+      float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+      {
+        const int mi = lane >> 3;
+        const int r = 16 * warp + ((mi & 1) << 3) + (lane & 7);
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4(kbase + swz(r, 2 * ks + (mi >> 1)), a0, a1, a2, a3);
+          mma_bf16(sacc, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+        }
       }
-      if (hv1) {
-        float *op = o_part + ((head0 + h1) * S + s) * D;
-        op[d] = o[mt][1] * il1;
-        op[d + 8] = o[mt][3] * il1;
+      const int kr_lo = 16 * warp + gid, kr_hi = kr_lo + 8;
+      const int key_lo = t * kT + kr_lo, key_hi = t * kT + kr_hi;
+      const bool v_lo = key_lo >= w.k0 && key_lo < w.k1 && ((km >> (kr_lo / box_rows)) & 1u);
+      const bool v_hi = key_hi >= w.k0 && key_hi < w.k1 && ((km >> (kr_hi / box_rows)) & 1u);
+      const float s00 = (v_lo && hv0) ? sacc[0] * scale_log2 : -INFINITY;
+      const float s01 = (v_lo && hv1) ? sacc[1] * scale_log2 : -INFINITY;
+      const float s10 = (v_hi && hv0) ? sacc[2] * scale_log2 : -INFINITY;
+      const float s11 = (v_hi && hv1) ? sacc[3] * scale_log2 : -INFINITY;
+      float mx0 = fmaxf(s00, s10), mx1 = fmaxf(s01, s11);
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+      }
+      if (gid == 0) {
+        red_max[warp * kMaxG + h0] = mx0;
+        red_max[warp * kMaxG + h1] = mx1;
+      }
+      consumer_sync();  // (1) K stage consumed; maxima visible
+      if (tid == 0) mbar_arrive(emptyK + 8 * st);
+      float mt0 = red_max[h0], mt1 = red_max[h1];
+#pragma unroll
+      for (int ww = 1; ww < kCWarps; ++ww) {
+        mt0 = fmaxf(mt0, red_max[ww * kMaxG + h0]);
+        mt1 = fmaxf(mt1, red_max[ww * kMaxG + h1]);
+      }
+      const float mn0 = fmaxf(m_run0, mt0), mn1 = fmaxf(m_run1, mt1);
+      const float mu0 = mn0 == -INFINITY ? 0.f : mn0;
+      const float mu1 = mn1 == -INFINITY ? 0.f : mn1;
+      const float p00 = exp2f(s00 - mu0), p01 = exp2f(s01 - mu1);
+      const float p10 = exp2f(s10 - mu0), p11 = exp2f(s11 - mu1);
+      {
+        uint32_t *pt = reinterpret_cast<uint32_t *>(sm + Cf::OFF_P);
+        pt[kr_lo * 4 + tig] = pack_bf16(p00, p01);
+        pt[kr_hi * 4 + tig] = pack_bf16(p10, p11);
+      }
+      float sm0 = p00 + p10, sm1 = p01 + p11;
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        sm0 += __shfl_xor_sync(0xffffffffu, sm0, off);
+        sm1 += __shfl_xor_sync(0xffffffffu, sm1, off);
+      }
+      if (gid == 0) {
+        red_sum[warp * kMaxG + h0] = sm0;
+        red_sum[warp * kMaxG + h1] = sm1;
+      }
+      // ---- V tile: wait, then clear the rows of keys outside [k0, k1) ----
+      if (!mbar_wait(fullV + 8 * st, par, abort_flag)) {
+        failed = true;
+        *abort_flag = 1;
+      }
+      const uint32_t vm = vmask[st];
+      const uint32_t vbase = sV + st * Cf::STAGE_BYTES;
+      const bool full_tile = t * kT >= w.k0 && t * kT + kT <= w.k1 && vm == all_boxes;
+      if (!full_tile) {
+        const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+        for (int i = tid; i < kT * (D / 8); i += kCThreads) {
+          const int r = i / (D / 8), c = i % (D / 8);
+          const int key = t * kT + r;
+          const bool valid = key >= w.k0 && key < w.k1 && ((vm >> (r / box_rows)) & 1u);
+          if (!valid)
+            *reinterpret_cast<uint4 *>(sm + Cf::OFF_V + st * Cf::STAGE_BYTES +
+                                       (c >> 3) * (kT * 128) + r * 128 + (c & 7) * 16) = z;
+        }
+        fence_proxy_async();
+      }
+      consumer_sync();  // (2) P, sums and V visible
+      float ts0 = 0.f, ts1 = 0.f;
+#pragma unroll
+      for (int ww = 0; ww < kCWarps; ++ww) {
+        ts0 += red_sum[ww * kMaxG + h0];
+        ts1 += red_sum[ww * kMaxG + h1];
+      }
+      const float al0 = exp2f(m_run0 - mu0), al1 = exp2f(m_run1 - mu1);
+      l_run0 = l_run0 * al0 + ts0;
+      l_run1 = l_run1 * al1 + ts1;
+      m_run0 = mn0;
+      m_run1 = mn1;
+      // ---- O^T[warp's D/4 slice x 8 heads] += V^T P^T ----
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        o[mt][0] *= al0;
+        o[mt][1] *= al1;
+        o[mt][2] *= al0;
+        o[mt][3] *= al1;
+      }
+#pragma unroll
+      for (int kp = 0; kp < kT / 32; ++kp) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(sP + (32 * kp + lane) * 16, b0, b1, b2, b3);
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          const int ks = 2 * kp + half;
+          const uint32_t bb0 = half ? b2 : b0, bb1 = half ? b3 : b1;
+          const int mi = lane >> 3;
+          const int r = 16 * ks + ((mi >> 1) << 3) + (lane & 7);
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt) {
+            const int dchunk = (warp * (D / 4) + 16 * mt) / 8 + (mi & 1);
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4_t(vbase + swz(r, dchunk), a0, a1, a2, a3);
+            mma_bf16(o[mt], a0, a1, a2, a3, bb0, bb1);
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(emptyV + 8 * st);
+    }
+
+    if (failed) continue;
+    // ---- epilogue: direct output for one-part rows, else a partial ----
+    const float il0 = l_run0 > 0.f ? 1.f / l_run0 : 0.f;
+    const float il1 = l_run1 > 0.f ? 1.f / l_run1 : 0.f;
+    const size_t head0 = static_cast<size_t>(w.b) * p.Hq + static_cast<size_t>(w.g) * p.G;
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+      const int d = warp * (D / 4) + 16 * mt + gid;
+      if (w.parts == 1) {
+        if (hv0) {
+          out[(head0 + h0) * D + d] = __float2bfloat16_rn(o[mt][0] * il0);
+          out[(head0 + h0) * D + d + 8] = __float2bfloat16_rn(o[mt][2] * il0);
+        }
+        if (hv1) {
+          out[(head0 + h1) * D + d] = __float2bfloat16_rn(o[mt][1] * il1);
+          out[(head0 + h1) * D + d + 8] = __float2bfloat16_rn(o[mt][3] * il1);
+        }
+      } else {
+        if (hv0) {
+          float *op = o_part + ((head0 + h0) * p.max_parts + w.part) * D;
+          op[d] = o[mt][0] * il0;
+          op[d + 8] = o[mt][2] * il0;
+        }
+        if (hv1) {
+          float *op = o_part + ((head0 + h1) * p.max_parts + w.part) * D;
+          op[d] = o[mt][1] * il1;
+          op[d + 8] = o[mt][3] * il1;
+        }
       }
     }
-  }
-  if (S > 1 && warp == 0 && gid == 0) {
-    if (hv0) lse_part[(head0 + h0) * S + s] = l_run0 > 0.f ? m_run0 + log2f(l_run0) : -INFINITY;
-    if (hv1) lse_part[(head0 + h1) * S + s] = l_run1 > 0.f ? m_run1 + log2f(l_run1) : -INFINITY;
+    if (w.parts > 1 && warp == 0 && gid == 0) {
+      if (hv0)
+        lse_part[(head0 + h0) * p.max_parts + w.part] =
+            l_run0 > 0.f ? m_run0 + log2f(l_run0) : -INFINITY;
+      if (hv1)
+        lse_part[(head0 + h1) * p.max_parts + w.part] =
+            l_run1 > 0.f ? m_run1 + log2f(l_run1) : -INFINITY;
+    }
   }
 }
 
-// Merge the splits of one (row, head): weights 2^(lse_s - max), skipping
-// empty splits (lse = -inf); a row with no key gives zeros.
+// Merge the parts of one (row, head) with weights 2^(lse_c - max), skipping
+// parts without keys (lse = -inf). (Row, head) pairs handled by one CTA were
+// written by the attention kernel itself. One warp per (row, head); the part
+// count and the log-sum-exps are loaded together, then each lane merges four
+// consecutive output columns.
 __global__ void combine_kernel(const float *__restrict__ o_part,
                                const float *__restrict__ lse_part,
-                               __nv_bfloat16 *__restrict__ out, int rows, int S,
-                               int D) {
+                               const int *__restrict__ parts_in, const Problem p, int D,
+                               __nv_bfloat16 *__restrict__ out) {
+  pkv_grid_dependency_sync();
   const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
-  if (r >= rows) return;
-  const float *lse = lse_part + static_cast<size_t>(r) * S;
-  float m = -INFINITY;
-  for (int s = lane; s < S; s += 32) m = fmaxf(m, lse[s]);
+  if (r >= p.B * p.Hq) return;
+  const int b = r / p.Hq, g = (r - b * p.Hq) / p.G;
+  const float *lse = lse_part + static_cast<size_t>(r) * p.max_parts;
+  const int parts = __ldcg(parts_in + b * p.Hkv + g);
+  float my_lse = lane < p.max_parts ? __ldcg(lse + lane) : -INFINITY;
+  if (parts <= 1) return;
+  if (lane >= parts) my_lse = -INFINITY;
+  float m = my_lse;
+  for (int s = 32 + lane; s < parts; s += 32) m = fmaxf(m, __ldcg(lse + s));
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-  const float *op = o_part + static_cast<size_t>(r) * S * D;
+  const float *op = o_part + static_cast<size_t>(r) * p.max_parts * D;
   __nv_bfloat16 *orow = out + static_cast<size_t>(r) * D;
   for (int d = 4 * lane; d < D; d += 128) {
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     float wsum = 0.f;
     if (m != -INFINITY) {
-      for (int s = 0; s < S; ++s) {
-        const float l = lse[s];
-        if (l == -INFINITY) continue;
-        const float w = exp2f(l - m);
-        const float4 v = *reinterpret_cast<const float4 *>(op + static_cast<size_t>(s) * D + d);
-        wsum += w;
-        acc.x = fmaf(w, v.x, acc.x);
-        acc.y = fmaf(w, v.y, acc.y);
-        acc.z = fmaf(w, v.z, acc.z);
-        acc.w = fmaf(w, v.w, acc.w);
+#pragma unroll 4
+      for (int s = 0; s < parts; ++s) {
+        const float l = s < 32 ? __shfl_sync(0xffffffffu, my_lse, s) : __ldcg(lse + s);
+        const float4 v = __ldcg(reinterpret_cast<const float4 *>(op + static_cast<size_t>(s) * D + d));
+        const float wgt = l == -INFINITY ? 0.f : exp2f(l - m);
+        wsum += wgt;
+        acc.x = fmaf(wgt, v.x, acc.x);
+        acc.y = fmaf(wgt, v.y, acc.y);
+        acc.z = fmaf(wgt, v.z, acc.z);
+        acc.w = fmaf(wgt, v.w, acc.w);
       }
     }
     const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
@@ -520,12 +826,12 @@ EncodeTiledFn encode_fn() {
   static std::once_flag once;
   static EncodeTiledFn fn = nullptr;
   std::call_once(once, [] {
-    void *p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
-                                         cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult qr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                         cudaEnableDefault, &qr) == cudaSuccess &&
+        qr == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
   });
   return fn;
 }
@@ -557,7 +863,7 @@ int set_smem_attr() {
   if (dev < 0 || dev >= 64) return pkv::fail(PKV_E_CUDA, "device id out of range");
   std::lock_guard<std::mutex> lock(mu);
   if (!done[dev]) {
-    PKV_CUDA_CHECK(cudaFuncSetAttribute(decode_split_kernel<D>,
+    PKV_CUDA_CHECK(cudaFuncSetAttribute(decode_attn_kernel<D>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         Cfg<D>::SMEM));
     done[dev] = true;
@@ -566,57 +872,54 @@ int set_smem_attr() {
 }
 
 template <int D>
-int launch_split(const CUtensorMap &tmK, const CUtensorMap &tmV, const pkv_bf16 *q,
-                 const int32_t *table, int n_slots, int max_pages, int log2_ps,
-                 int n_pages, const int32_t *batch_idx, const int32_t *seq_lens,
-                 int window, float scale_log2, int B, int Hq, int Hkv, int S,
-                 float *o_part, float *lse_part, pkv_bf16 *out, int32_t *err,
-                 cudaStream_t stream) {
+int launch_attn(const CUtensorMap &tmK, const CUtensorMap &tmV, const pkv_bf16 *q,
+                const Problem &p, float scale_log2, float *o_part, float *lse_part,
+                int *parts, pkv_bf16 *out, int32_t *err, cudaStream_t stream) {
   int st = set_smem_attr<D>();
   if (st != PKV_OK) return st;
-  dim3 grid(S, Hkv, B);
-  decode_split_kernel<D><<<grid, kThreads, Cfg<D>::SMEM, stream>>>(
-      tmK, tmV, reinterpret_cast<const __nv_bfloat16 *>(q), table, n_slots, max_pages,
-      log2_ps, n_pages, batch_idx, seq_lens, window, scale_log2, Hq, Hq / Hkv, S,
-      o_part, lse_part, reinterpret_cast<__nv_bfloat16 *>(out), err);
-  PKV_CUDA_CHECK(cudaGetLastError());
+  const int sms = pkv::sm_count();
+  if (sms <= 0) return pkv::fail(PKV_E_CUDA, "paged_decode_attn: no SM count");
+  const int grid = sms * Cfg<D>::CTAS_PER_SM;
+  PKV_CUDA_CHECK(pkv::launch_pdl(decode_attn_kernel<D>, dim3(grid), dim3(kThreads),
+                                 Cfg<D>::SMEM, stream, tmK, tmV,
+                                 reinterpret_cast<const __nv_bfloat16 *>(q), p, scale_log2,
+                                 o_part, lse_part, parts,
+                                 reinterpret_cast<__nv_bfloat16 *>(out), err));
   return PKV_OK;
 }
 
-int ctas_per_sm(int D) { return D <= 64 ? 3 : D <= 128 ? 2 : 1; }
-
-int auto_splits(int B, int Hkv, int D, int max_pages, int page_size, int window) {
-  long long max_keys = 1LL * max_pages * page_size;
-  if (window > 0 && window < max_keys) max_keys = window + kT - 1;
-  int max_tiles = static_cast<int>((max_keys + kT - 1) / kT);
-  int sms = pkv::sm_count();
-  if (sms <= 0) sms = 148;
-  long long target = 2LL * sms * ctas_per_sm(D);
-  long long work = 1LL * (B > 0 ? B : 1) * Hkv;
-  int S = static_cast<int>((target + work - 1) / work);
-  int cap = (max_tiles + 1) / 2;  // at least ~2 tiles per split
-  if (S > cap) S = cap;
-  if (S < 1) S = 1;
-  return S;
+// Upper bound on the parts a row is cut into: the fixed split count, or in
+// the automatic mode one part per 64-key tile of the longest possible row.
+int max_parts_for(int max_pages, int page_size, int window, int num_splits) {
+  const long long max_keys = 1LL * max_pages * page_size;
+  long long tiles = (max_keys + kT - 1) / kT;
+  if (window > 0 && window < max_keys) tiles = (window + kT - 1) / kT + 1;
+  if (num_splits > 0) return static_cast<int>(num_splits < tiles ? num_splits : tiles);
+  return static_cast<int>(tiles);
 }
 
 }  // namespace
 
 extern "C" {
 
+// Workspace layout: [parts per (row, kv head): B*Hq ints, 256-byte padded]
+// [o_part fp32 B*Hq*P*D][lse_part fp32 B*Hq*P]; every field is written by a
+// call before it is read, so the workspace needs no initialisation.
+size_t parts_bytes(int B, int Hq) {
+  return (static_cast<size_t>(B) * Hq * sizeof(int) + 255) & ~size_t(255);
+}
+
 size_t paged_decode_attn_workspace(int B, int Hq, int D, int num_splits) {
   if (num_splits <= 1 || B <= 0 || Hq <= 0 || D <= 0) return 0;
-  size_t rows = static_cast<size_t>(B) * Hq * num_splits;
-  size_t o_bytes = rows * D * sizeof(float);
-  o_bytes = (o_bytes + 15) & ~size_t(15);
-  return o_bytes + rows * sizeof(float);
+  const size_t rows = static_cast<size_t>(B) * Hq * num_splits;
+  return parts_bytes(B, Hq) + rows * D * sizeof(float) + rows * sizeof(float);
 }
 
 int paged_decode_attn_splits(int B, int Hkv, int D, int max_pages_per_seq,
                              int page_size, int window, int *num_splits) {
-  if (!num_splits || Hkv < 1 || max_pages_per_seq < 1 || page_size < 1)
+  if (!num_splits || Hkv < 1 || max_pages_per_seq < 1 || page_size < 1 || B < 0 || D < 1)
     return pkv::fail(PKV_E_BAD_ARG, "paged_decode_attn_splits: bad argument");
-  *num_splits = auto_splits(B, Hkv, D, max_pages_per_seq, page_size, window);
+  *num_splits = max_parts_for(max_pages_per_seq, page_size, window, 0);
   return pkv::ok();
 }
 
@@ -636,8 +939,8 @@ int paged_decode_attn(const pkv_bf16 *q, const pkv_bf16 *k_cache,
     return pkv::fail(PKV_E_BAD_ARG, "paged_decode_attn: page_size must be a power of two >= 8");
   if (B < 0 || n_slots < 1 || max_pages_per_seq < 1 || n_pages < 1 || num_splits < 0)
     return pkv::fail(PKV_E_BAD_ARG, "paged_decode_attn: bad size argument");
-  if (B > 65535 || Hkv > 65535)
-    return pkv::fail(PKV_E_BAD_ARG, "paged_decode_attn: B and Hkv must be <= 65535");
+  if (B > kMaxRows)
+    return pkv::fail(PKV_E_BAD_ARG, "paged_decode_attn: B must be <= %d", kMaxRows);
   if (static_cast<long long>(max_pages_per_seq) * page_size > (1LL << 30))
     return pkv::fail(PKV_E_BAD_ARG, "paged_decode_attn: table row too long");
   const long long rows = 1LL * Hkv * n_pages * page_size;
@@ -651,22 +954,25 @@ int paged_decode_attn(const pkv_bf16 *q, const pkv_bf16 *k_cache,
   if (!pkv::aligned16(q) || !pkv::aligned16(out) || !pkv::aligned16(k_cache) ||
       !pkv::aligned16(v_cache))
     return pkv::fail(PKV_E_BAD_ARG, "paged_decode_attn: tensors must be 16-byte aligned");
-  int S = num_splits ? num_splits
-                     : auto_splits(B, Hkv, D, max_pages_per_seq, page_size, window);
-  if (S > 65535) return pkv::fail(PKV_E_BAD_ARG, "paged_decode_attn: too many splits");
-  const size_t need = paged_decode_attn_workspace(B, Hq, D, S);
+  {
+    const long long row_tiles = (1LL * max_pages_per_seq * page_size + kT - 1) / kT + 1;
+    if (1LL * B * Hkv * row_tiles >= (1LL << 31))
+      return pkv::fail(PKV_E_BAD_ARG, "paged_decode_attn: B * Hkv * tiles per row too large");
+  }
+  const int max_parts = max_parts_for(max_pages_per_seq, page_size, window, num_splits);
+  const size_t need = paged_decode_attn_workspace(B, Hq, D, max_parts);
   if (need > 0) {
     if (!workspace || workspace_bytes < need)
       return pkv::fail(PKV_E_BAD_ARG, "paged_decode_attn: workspace needs %zu bytes", need);
     if (!pkv::aligned16(workspace))
       return pkv::fail(PKV_E_BAD_ARG, "paged_decode_attn: workspace must be 16-byte aligned");
   }
-  float *o_part = static_cast<float *>(workspace);
-  float *lse_part = nullptr;
+  int *parts = nullptr;
+  float *o_part = nullptr, *lse_part = nullptr;
   if (need > 0) {
-    size_t o_bytes = static_cast<size_t>(B) * Hq * S * D * sizeof(float);
-    o_bytes = (o_bytes + 15) & ~size_t(15);
-    lse_part = reinterpret_cast<float *>(static_cast<char *>(workspace) + o_bytes);
+    parts = static_cast<int *>(workspace);
+    o_part = reinterpret_cast<float *>(static_cast<char *>(workspace) + parts_bytes(B, Hq));
+    lse_part = o_part + static_cast<size_t>(B) * Hq * max_parts * D;
   }
   const int box_rows = page_size < kT ? page_size : kT;
   CUtensorMap tmK, tmV;
@@ -676,37 +982,48 @@ int paged_decode_attn(const pkv_bf16 *q, const pkv_bf16 *k_cache,
   if (st != PKV_OK) return st;
   int log2_ps = 0;
   while ((1 << log2_ps) < page_size) ++log2_ps;
+  Problem p;
+  p.table = dev_table;
+  p.batch_idx = batch_idx;
+  p.seq_lens = seq_lens;
+  p.n_slots = n_slots;
+  p.max_pages = max_pages_per_seq;
+  p.log2_ps = log2_ps;
+  p.n_pages = n_pages;
+  p.window = window;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.G = Hq / Hkv;
+  // with at most one part per row no partial is ever written
+  p.fixed_splits = max_parts == 1 ? 1 : num_splits;
+  p.max_parts = max_parts;
   const float scale_log2 = scale * 1.4426950408889634f;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   switch (D) {
     case 64:
-      st = launch_split<64>(tmK, tmV, q, dev_table, n_slots, max_pages_per_seq, log2_ps,
-                            n_pages, batch_idx, seq_lens, window, scale_log2, B, Hq, Hkv,
-                            S, o_part, lse_part, out, err_word, s);
+      st = launch_attn<64>(tmK, tmV, q, p, scale_log2, o_part, lse_part, parts, out, err_word, s);
       break;
     case 128:
-      st = launch_split<128>(tmK, tmV, q, dev_table, n_slots, max_pages_per_seq, log2_ps,
-                             n_pages, batch_idx, seq_lens, window, scale_log2, B, Hq, Hkv,
-                             S, o_part, lse_part, out, err_word, s);
+      st = launch_attn<128>(tmK, tmV, q, p, scale_log2, o_part, lse_part, parts, out, err_word, s);
       break;
     case 256:
-      st = launch_split<256>(tmK, tmV, q, dev_table, n_slots, max_pages_per_seq, log2_ps,
-                             n_pages, batch_idx, seq_lens, window, scale_log2, B, Hq, Hkv,
-                             S, o_part, lse_part, out, err_word, s);
+      st = launch_attn<256>(tmK, tmV, q, p, scale_log2, o_part, lse_part, parts, out, err_word, s);
       break;
     default:
-      st = launch_split<512>(tmK, tmV, q, dev_table, n_slots, max_pages_per_seq, log2_ps,
-                             n_pages, batch_idx, seq_lens, window, scale_log2, B, Hq, Hkv,
-                             S, o_part, lse_part, out, err_word, s);
+      st = launch_attn<512>(tmK, tmV, q, p, scale_log2, o_part, lse_part, parts, out, err_word, s);
       break;
   }
   if (st != PKV_OK) return st;
-  if (S > 1) {
+  if (max_parts > 1) {
     const int rows_bh = B * Hq;
     const int wpb = 4;
-    combine_kernel<<<(rows_bh + wpb - 1) / wpb, wpb * 32, 0, s>>>(
-        o_part, lse_part, reinterpret_cast<__nv_bfloat16 *>(out), rows_bh, S, D);
-    PKV_CUDA_CHECK(cudaGetLastError());
+    PKV_CUDA_CHECK(pkv::launch_pdl(combine_kernel, dim3((rows_bh + wpb - 1) / wpb),
+                                   dim3(wpb * 32), 0, s,
+                                   static_cast<const float *>(o_part),
+                                   static_cast<const float *>(lse_part),
+                                   static_cast<const int *>(parts), p, D,
+                                   reinterpret_cast<__nv_bfloat16 *>(out)));
   }
   return pkv::ok();
 }

@@ -69,12 +69,13 @@ int paged_decode_attn_noalloc(const pkv_bf16 *q, const pkv_bf16 *k_cache,
                               const int32_t *seq_lens, int window, float scale,
                               int B, int Hq, int Hkv, int D, int num_splits,
                               pkv_bf16 *out, int32_t *err_word, void *stream) {
+  if (num_splits < 0) return pkv::fail(PKV_E_BAD_ARG, "paged_decode_attn_noalloc: num_splits < 0");
+  // most parts a row can be cut into: the fixed count, or the automatic bound
   int splits = num_splits;
   if (splits == 0) {
     int st = paged_decode_attn_splits(B, Hkv, D, max_pages_per_seq, page_size, window, &splits);
     if (st != PKV_OK) return st;
   }
-  if (splits < 0) return pkv::fail(PKV_E_BAD_ARG, "paged_decode_attn_noalloc: num_splits < 0");
   const size_t need = paged_decode_attn_workspace(B, Hq, D, splits);
   if (need > kNoallocScratchBytes)
     return pkv::fail(PKV_E_BAD_ARG,
@@ -87,7 +88,7 @@ int paged_decode_attn_noalloc(const pkv_bf16 *q, const pkv_bf16 *k_cache,
   if (st != PKV_OK) return st;
   return paged_decode_attn(q, k_cache, v_cache, dev_table, n_slots, max_pages_per_seq,
                            page_size, n_pages, batch_idx, seq_lens, window, scale, B, Hq, Hkv,
-                           D, splits, scratch, kNoallocScratchBytes, out, err_word, stream);
+                           D, num_splits, scratch, kNoallocScratchBytes, out, err_word, stream);
 }
 
 }  // extern "C"

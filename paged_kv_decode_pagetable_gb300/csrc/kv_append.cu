@@ -28,6 +28,7 @@ __global__ void kv_append_kernel(const uint4 *__restrict__ k,
                                  int n_pages, uint4 *__restrict__ k_cache,
                                  uint4 *__restrict__ v_cache, int Hkv,
                                  int chunks_per_head, int32_t *err) {
+  pkv_grid_dependency_sync();
   // linear index over [2 (k|v)][B][Hkv][chunks_per_head]
   long long per_tensor = 1LL * B * Hkv * chunks_per_head;
   long long i = blockIdx.x * 1LL * blockDim.x + threadIdx.x;
@@ -90,12 +91,11 @@ extern "C" int kv_append(const pkv_bf16 *k, const pkv_bf16 *v,
   int threads = 256;
   long long blocks = (total + threads - 1) / threads;
   if (blocks > 0x7fffffffLL) return pkv::fail(PKV_E_BAD_ARG, "kv_append: too large");
-  kv_append_kernel<<<static_cast<unsigned>(blocks), threads, 0,
-                     static_cast<cudaStream_t>(stream)>>>(
-      reinterpret_cast<const uint4 *>(k), reinterpret_cast<const uint4 *>(v),
-      batch_idx, input_pos, dev_table, B, n_slots, max_pages_per_seq,
-      page_size, n_pages, reinterpret_cast<uint4 *>(k_cache),
-      reinterpret_cast<uint4 *>(v_cache), Hkv, chunks, err_word);
-  PKV_CUDA_CHECK(cudaGetLastError());
+  PKV_CUDA_CHECK(pkv::launch_pdl(
+      kv_append_kernel, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0,
+      static_cast<cudaStream_t>(stream), reinterpret_cast<const uint4 *>(k),
+      reinterpret_cast<const uint4 *>(v), batch_idx, input_pos, dev_table, B, n_slots,
+      max_pages_per_seq, page_size, n_pages, reinterpret_cast<uint4 *>(k_cache),
+      reinterpret_cast<uint4 *>(v_cache), Hkv, chunks, err_word));
   return pkv::ok();
 }

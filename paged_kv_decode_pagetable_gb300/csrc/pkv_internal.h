@@ -1,10 +1,13 @@
 // Internal helpers shared by the libpkv translation units (host side).
 #pragma once
 
+#include <cuda_runtime.h>
+
 #include <cstdarg>
 #include <cstdint>
 #include <cstdio>
 #include <string>
+#include <utility>
 
 #include "../../include/pkv.h"
 
@@ -23,7 +26,40 @@ inline bool aligned16(const void *p) {
 }
 inline bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
 
+// Launches a kernel that may begin while the previous kernel of the stream
+// is still running (programmatic dependent launch). Every kernel launched
+// this way executes griddepcontrol.wait before it touches global memory, so
+// it observes the same ordering as a plain launch; only the launch latency
+// and the set-up of shared memory overlap the previous kernel's tail.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 }  // namespace pkv
+
+#ifdef __CUDACC__
+// Waits until the previous kernel of the stream has completed and its
+// memory is visible (a no-op for a plain launch), then lets the next kernel
+// of the stream be scheduled. Called by every thread before any global
+// memory access; the next kernel can only start once all CTAs of this one
+// have passed this point, so it never takes resources they still need.
+__device__ __forceinline__ void pkv_grid_dependency_sync() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+#endif
 
 #define PKV_CUDA_CHECK(call)                                                  \
   do {                                                                        \

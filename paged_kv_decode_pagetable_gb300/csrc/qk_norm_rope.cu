@@ -27,6 +27,7 @@ __global__ void qk_norm_rope_kernel(__nv_bfloat16 *__restrict__ q,
                                     const int32_t *__restrict__ pos,
                                     float log2_theta, float eps, int B, int Hq,
                                     int Hkv, int D) {
+  pkv_grid_dependency_sync();
   const int warps_per_block = blockDim.x >> 5;
   const long long w = blockIdx.x * 1LL * warps_per_block + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
@@ -96,12 +97,11 @@ extern "C" int qk_norm_rope(pkv_bf16 *q, pkv_bf16 *k, const pkv_bf16 *gamma_q,
   const long long warps = 1LL * B * (Hq + Hkv);
   const int threads = 256, wpb = threads / 32;
   long long blocks = (warps + wpb - 1) / wpb;
-  qk_norm_rope_kernel<<<static_cast<unsigned>(blocks), threads, 0,
-                        static_cast<cudaStream_t>(stream)>>>(
-      reinterpret_cast<__nv_bfloat16 *>(q), reinterpret_cast<__nv_bfloat16 *>(k),
-      reinterpret_cast<const __nv_bfloat16 *>(gamma_q),
-      reinterpret_cast<const __nv_bfloat16 *>(gamma_k), pos, log2f(theta), eps,
-      B, Hq, Hkv, D);
-  PKV_CUDA_CHECK(cudaGetLastError());
+  PKV_CUDA_CHECK(pkv::launch_pdl(
+      qk_norm_rope_kernel, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0,
+      static_cast<cudaStream_t>(stream), reinterpret_cast<__nv_bfloat16 *>(q),
+      reinterpret_cast<__nv_bfloat16 *>(k), reinterpret_cast<const __nv_bfloat16 *>(gamma_q),
+      reinterpret_cast<const __nv_bfloat16 *>(gamma_k), pos, log2f(theta), eps, B, Hq, Hkv,
+      D));
   return pkv::ok();
 }

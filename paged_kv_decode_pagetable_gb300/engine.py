@@ -45,13 +45,17 @@ def alloc_cache(Hkv: int, n_pages: int, page_size: int, D: int, device, fill: st
 
 
 class AttnWorkspace:
-    """Split count and workspace for one (B, Hq, Hkv, D, table, window) shape."""
+    """Split mode and workspace for one (B, Hq, Hkv, D, table, window) shape.
+
+    num_splits 0 is the automatic, length-balanced mode; the workspace is
+    sized for the most parts a row can be cut into in that mode."""
 
     def __init__(self, B, Hq, Hkv, D, max_pages_per_seq, page_size, window, device,
                  num_splits: int = 0):
-        self.splits = num_splits or paged_decode_attn_splits(B, Hkv, D, max_pages_per_seq,
-                                                             page_size, window)
-        n = paged_decode_attn_workspace(B, Hq, D, self.splits)
+        self.splits = num_splits
+        self.max_parts = num_splits or paged_decode_attn_splits(B, Hkv, D, max_pages_per_seq,
+                                                                page_size, window)
+        n = paged_decode_attn_workspace(B, Hq, D, self.max_parts)
         self.buf = torch.empty(n, dtype=torch.uint8, device=device) if n else None
 
 

@@ -80,10 +80,10 @@ def run_attn(pkv, case, dev, window, scale, splits, err=None, out=None, q=None):
     d = case.device(dev)
     if q is not None:
         d["q"] = q
-    S = splits or pkv.paged_decode_attn_splits(case.B, case.Hkv, case.D, case.max_pages,
+    P = splits or pkv.paged_decode_attn_splits(case.B, case.Hkv, case.D, case.max_pages,
                                                case.ps, window)
-    ws_n = pkv.paged_decode_attn_workspace(case.B, case.Hq, case.D, S)
-    ws = torch.empty(max(ws_n, 16), dtype=torch.uint8, device=dev) if ws_n else None
+    ws_n = pkv.paged_decode_attn_workspace(case.B, case.Hq, case.D, P)
+    ws = torch.zeros(max(ws_n, 16), dtype=torch.uint8, device=dev) if ws_n else None
     if out is None:
         out = torch.full((case.B, case.Hq, case.D), float("nan"), dtype=torch.bfloat16, device=dev)
     if err is None:

@@ -226,7 +226,7 @@ def test_attention_error_bits_without_fault(dev):
 
 def test_bad_arguments_rejected_before_launch(dev):
     rng = np.random.default_rng(10)
-    case = PagedCase(rng, 2, 4, 1, 64, 16, [10, 10])
+    case = PagedCase(rng, 2, 4, 1, 64, 16, [100, 100])     # two 64-key tiles per row
     d = case.device(dev)
     out = torch.empty((2, 4, 64), dtype=torch.bfloat16, device=dev)
 
@@ -257,8 +257,9 @@ def test_graph_replay_is_bit_identical_to_eager(dev):
     k_new, v_new = wl.randn_bf16(rng, (B, Hkv, D)).to(dev), wl.randn_bf16(rng, (B, Hkv, D)).to(dev)
     gq, gk = wl.gamma_bf16(rng, D).to(dev), wl.gamma_bf16(rng, D).to(dev)
     pos = torch.from_numpy(lens0.astype(np.int32)).to(dev)
-    S = pkv.paged_decode_attn_splits(B, Hkv, D, case.max_pages, ps, 0)
-    ws = torch.empty(max(pkv.paged_decode_attn_workspace(B, Hq, D, S), 16), dtype=torch.uint8,
+    S = 0    # automatic, length-balanced parts
+    P = pkv.paged_decode_attn_splits(B, Hkv, D, case.max_pages, ps, 0)
+    ws = torch.zeros(max(pkv.paged_decode_attn_workspace(B, Hq, D, P), 16), dtype=torch.uint8,
                      device=dev)
     bufs = dict(q=d["q"].clone(), k=k_new.clone(), kc=d["kc"].clone(), vc=d["vc"].clone(),
                 out=torch.empty((B, Hq, D), dtype=torch.bfloat16, device=dev))

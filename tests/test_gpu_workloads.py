@@ -171,7 +171,7 @@ def test_tiny_workload_permuted_pages(dev):
     for S in (0, 1, 2, 3):
         nsp = S or pkv.paged_decode_attn_splits(2, 1, D, w.max_pages_per_seq, w.page_size, 0)
         n = pkv.paged_decode_attn_workspace(2, 2, D, nsp)
-        ws = torch.empty(n, dtype=torch.uint8, device=dev) if n else None
+        ws = torch.zeros(n, dtype=torch.uint8, device=dev) if n else None
         out = torch.empty((2, 2, D), dtype=torch.bfloat16, device=dev)
         pkv.paged_decode_attn(q.to(dev), dkc, dvc, d(table), w.n_slots, w.max_pages_per_seq,
                               w.page_size, w.n_pages, d(bidx), d(pos + 1), 0, 0.125, S, ws, out)
