@@ -79,9 +79,10 @@ def measured_peaks():
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
 
 
-def profile_traffic(kernel_key: str):
-    """DRAM bytes per launch from a committed ncu capture, if the kernel
-    source is unchanged since the capture."""
+def profile_traffic(kernel_key: str, mean_alg_bytes: float):
+    """DRAM bytes per launch from a committed ncu capture (the captured
+    launches' measured/algorithmic ratio scaled to this run's mean launch),
+    or None when the kernel source changed since the capture."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
@@ -95,7 +96,7 @@ def profile_traffic(kernel_key: str):
         digest = hashlib.sha256(f.read()).hexdigest()[:16]
     if rec.get("source_sha256_16") != digest:
         return None
-    return rec.get("bytes_per_launch_full")
+    return float(rec["dram_over_algorithmic"]) * mean_alg_bytes
 
 
 class ClockSampler:
@@ -406,7 +407,8 @@ def run_ours(args, world, rank, local):
             "roofline": {"bound": "hbm", "achieved": attn_gbs, "peak": peak, "unit": "GB/s",
                          "frac": attn_gbs / peak, "peak_kind": peak_kind,
                          "kernel": "decode_attn_kernel<128> + combine_kernel",
-                         "traffic": profile_traffic("rollout_decode_attn_128")},
+                         "traffic": profile_traffic("rollout_decode_attn_128",
+                                                    float(step_bytes[W:].mean()))},
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": K * launches_per_step,
