@@ -142,6 +142,26 @@ int qk_norm_rope(pkv_bf16 *q, pkv_bf16 *k, const pkv_bf16 *gamma_q,
                  float eps, int B, int Hq, int Hkv, int D, void *stream);
 
 /* ---------------------------------------------------------------------
+ * qk_norm_rope_append — qk_norm_rope followed by kv_append in one kernel
+ * (the write-then-attend prologue of [P1]'s attention forward: q/k norm,
+ * rotary, then the paged write of [P3] PageTable.assign). Results are
+ * identical to the two calls in sequence: q and k are rotated in place, then
+ * k (rotated) and v (unchanged) are scattered to row
+ * table[batch_idx[b]][input_pos[b] / page_size] * page_size + input_pos[b] %
+ * page_size of every kv head's cache, with the same checks and error bits.
+ * pos for the rotation is input_pos. Requires Hkv >= 1, D even <= 1024,
+ * theta > 0; gains both given or both NULL (no norm).
+ * ------------------------------------------------------------------- */
+int qk_norm_rope_append(pkv_bf16 *q, pkv_bf16 *k, const pkv_bf16 *v,
+                        const pkv_bf16 *gamma_q, const pkv_bf16 *gamma_k,
+                        const int32_t *batch_idx, const int32_t *input_pos,
+                        float theta, float eps, int B, int Hq, int Hkv, int D,
+                        const int32_t *dev_table, int n_slots,
+                        int max_pages_per_seq, int page_size, int n_pages,
+                        pkv_bf16 *k_cache, pkv_bf16 *v_cache, int32_t *err_word,
+                        void *stream);
+
+/* ---------------------------------------------------------------------
  * paged_decode_attn — GQA single-token decode attention over the paged
  * cache ([P1] attention forward: flex_attention(q, k, v, scale,
  * block_mask, enable_gqa=True) with the decode masks of _decode_block_mask).

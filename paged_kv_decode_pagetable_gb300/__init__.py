@@ -79,6 +79,9 @@ _SIGS = {
                            _c_int, _c_p, _c_p, _c_int, _c_int, _c_p, _c_p]),
     "qk_norm_rope": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_p, _c_f, _c_f, _c_int, _c_int,
                               _c_int, _c_int, _c_p]),
+    "qk_norm_rope_append": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_f, _c_f,
+                                     _c_int, _c_int, _c_int, _c_int, _c_p, _c_int, _c_int,
+                                     _c_int, _c_int, _c_p, _c_p, _c_p, _c_p]),
     "paged_decode_attn": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_int, _c_int, _c_int, _c_int,
                                    _c_p, _c_p, _c_int, _c_f, _c_int, _c_int, _c_int, _c_int,
                                    _c_int, _c_p, _c_sz, _c_p, _c_p, _c_p]),
@@ -303,6 +306,21 @@ def qk_norm_rope(q, k, gamma_q, gamma_k, pos, theta: float, eps: float = 1e-6,
     _check(load_library().qk_norm_rope(
         _ptr(q), _ptr(k), _ptr(gamma_q), _ptr(gamma_k), _ptr(pos), float(theta), float(eps),
         B, Hq, Hkv, D, _stream(stream)), "qk_norm_rope")
+
+
+def qk_norm_rope_append(q, k, v, gamma_q, gamma_k, batch_idx, input_pos, theta: float,
+                        eps, dev_table, n_slots, max_pages_per_seq, page_size, n_pages,
+                        k_cache, v_cache, err_word=None, stream=None) -> None:
+    _bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v"), _bf16(gamma_q, "gamma_q")
+    _bf16(gamma_k, "gamma_k"), _bf16(k_cache, "k_cache"), _bf16(v_cache, "v_cache")
+    _i32(batch_idx, "batch_idx"), _i32(input_pos, "input_pos"), _i32(dev_table, "dev_table")
+    B, Hq, D = q.shape
+    Hkv = k.shape[1]
+    _check(load_library().qk_norm_rope_append(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(gamma_q), _ptr(gamma_k), _ptr(batch_idx),
+        _ptr(input_pos), float(theta), float(eps), B, Hq, Hkv, D, _ptr(dev_table), n_slots,
+        max_pages_per_seq, page_size, n_pages, _ptr(k_cache), _ptr(v_cache), _ptr(err_word),
+        _stream(stream)), "qk_norm_rope_append")
 
 
 def paged_decode_attn_splits(B, Hkv, D, max_pages_per_seq, page_size, window=0) -> int:

@@ -348,7 +348,8 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
     const long long tlim = tbl < (1LL << 20) ? tbl : (1LL << 20);
     for (long long i = 32LL * gt; i < tlim; i += 32LL * gs) prefetch_l2(p.table + i);
   }
-  pkv_grid_dependency_sync();
+  pkv_wait_prior_grid();
+  pkv_allow_next_grid();
   for (int b = tid; b < p.B; b += kThreads) {
     const RowInfo r = row_info(p, b, err, blockIdx.x == 0);
     rows[b] = make_int2(r.n_tiles > 0 ? r.slot : -1, r.L);
@@ -775,7 +776,8 @@ __global__ void combine_kernel(const float *__restrict__ o_part,
                                const float *__restrict__ lse_part,
                                const int *__restrict__ parts_in, const Problem p, int D,
                                __nv_bfloat16 *__restrict__ out) {
-  pkv_grid_dependency_sync();
+  pkv_wait_prior_grid();
+  pkv_allow_next_grid();
   const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (r >= p.B * p.Hq) return;

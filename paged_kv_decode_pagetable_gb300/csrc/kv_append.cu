@@ -28,7 +28,8 @@ __global__ void kv_append_kernel(const uint4 *__restrict__ k,
                                  int n_pages, uint4 *__restrict__ k_cache,
                                  uint4 *__restrict__ v_cache, int Hkv,
                                  int chunks_per_head, int32_t *err) {
-  pkv_grid_dependency_sync();
+  pkv_wait_prior_grid();
+  pkv_allow_next_grid();
   // linear index over [2 (k|v)][B][Hkv][chunks_per_head]
   long long per_tensor = 1LL * B * Hkv * chunks_per_head;
   long long i = blockIdx.x * 1LL * blockDim.x + threadIdx.x;

@@ -51,12 +51,20 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 
 #ifdef __CUDACC__
 // Waits until the previous kernel of the stream has completed and its
-// memory is visible (a no-op for a plain launch), then lets the next kernel
-// of the stream be scheduled. Called by every thread before any global
-// memory access; the next kernel can only start once all CTAs of this one
-// have passed this point, so it never takes resources they still need.
-__device__ __forceinline__ void pkv_grid_dependency_sync() {
+// memory is visible (a no-op for a plain launch). Every kernel calls it
+// before its first global memory access.
+__device__ __forceinline__ void pkv_wait_prior_grid() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+// Lets the next kernel of the stream be scheduled before this one ends. It
+// takes effect once every CTA of this grid has issued it (or exited), so the
+// next kernel never waits for resources held by CTAs that have not started.
+// Kernels that do not call it release their dependents as their CTAs exit.
+// The small kernels whose CTAs leave room for the persistent attention CTAs
+// (kv_append, qk_norm_rope, combine) and the attention kernel itself call it
+// early; the fused prologue does not, because its CTAs fill the register
+// file and would delay the attention CTAs it released.
+__device__ __forceinline__ void pkv_allow_next_grid() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 #endif

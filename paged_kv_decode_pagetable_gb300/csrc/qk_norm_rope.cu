@@ -11,6 +11,10 @@
 // One warp per (row, head); lane l owns the rotation pairs (i, i + D/2) for
 // i = l, l + 32, ...  so each lane rotates with no exchange and the only
 // cross-lane step is the sum of squares. fp32 math, one rounding to bf16.
+// qk_norm_rope_append fuses the decode K/V scatter of "unsloth: compare
+// main...transformers-continuous-batching-qwen3" · flex_paged_attention.py ·
+// PageTable.assign into the same pass (write-then-attend order of the
+// attention forward).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -20,28 +24,14 @@ namespace {
 
 constexpr int kMaxPairsPerLane = 16;  // D <= 1024
 
-__global__ void qk_norm_rope_kernel(__nv_bfloat16 *__restrict__ q,
-                                    __nv_bfloat16 *__restrict__ k,
-                                    const __nv_bfloat16 *__restrict__ gq,
-                                    const __nv_bfloat16 *__restrict__ gk,
-                                    const int32_t *__restrict__ pos,
-                                    float log2_theta, float eps, int B, int Hq,
-                                    int Hkv, int D) {
-  pkv_grid_dependency_sync();
-  const int warps_per_block = blockDim.x >> 5;
-  const long long w = blockIdx.x * 1LL * warps_per_block + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  const int H = Hq + Hkv;
-  if (w >= 1LL * B * H) return;
-  const int b = static_cast<int>(w / H);
-  const int h = static_cast<int>(w % H);
-  const bool is_q = h < Hq;
-  __nv_bfloat16 *x = is_q ? q + (1LL * b * Hq + h) * D
-                          : k + (1LL * b * Hkv + (h - Hq)) * D;
-  const __nv_bfloat16 *g = is_q ? gq : gk;
+// Norm + RoPE of one head vector x[0..D) held by a warp: lane l owns pairs
+// (i, i + D/2), i = l + 32j. Returns the rotated values in lo[] / hi[].
+__device__ __forceinline__ void norm_rope_warp(const __nv_bfloat16 *__restrict__ x,
+                                               const __nv_bfloat16 *__restrict__ g, float p,
+                                               float log2_theta, float eps, int D, int lane,
+                                               float (&lo)[kMaxPairsPerLane],
+                                               float (&hi)[kMaxPairsPerLane]) {
   const int half = D >> 1;
-
-  float lo[kMaxPairsPerLane], hi[kMaxPairsPerLane];
   float ss = 0.f;
 #pragma unroll
   for (int j = 0; j < kMaxPairsPerLane; ++j) {
@@ -59,7 +49,6 @@ __global__ void qk_norm_rope_kernel(__nv_bfloat16 *__restrict__ q,
     for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
     inv_rms = rsqrtf(ss / static_cast<float>(D) + eps);
   }
-  const float p = static_cast<float>(pos[b]);
 #pragma unroll
   for (int j = 0; j < kMaxPairsPerLane; ++j) {
     int i = lane + 32 * j;
@@ -71,10 +60,120 @@ __global__ void qk_norm_rope_kernel(__nv_bfloat16 *__restrict__ q,
       }
       // theta^(-2i/D) = 2^(-(2i/D) log2 theta)
       float inv_freq = exp2f(-(2.0f * i / static_cast<float>(D)) * log2_theta);
-      float s, c;
-      sincosf(p * inv_freq, &s, &c);
-      x[i] = __float2bfloat16_rn(r1 * c - r2 * s);
-      x[i + half] = __float2bfloat16_rn(r2 * c + r1 * s);
+      float sn, cs;
+      sincosf(p * inv_freq, &sn, &cs);
+      lo[j] = r1 * cs - r2 * sn;
+      hi[j] = r2 * cs + r1 * sn;
+    }
+  }
+}
+
+__global__ void qk_norm_rope_kernel(__nv_bfloat16 *__restrict__ q,
+                                    __nv_bfloat16 *__restrict__ k,
+                                    const __nv_bfloat16 *__restrict__ gq,
+                                    const __nv_bfloat16 *__restrict__ gk,
+                                    const int32_t *__restrict__ pos,
+                                    float log2_theta, float eps, int B, int Hq,
+                                    int Hkv, int D) {
+  pkv_wait_prior_grid();
+  pkv_allow_next_grid();
+  const int warps_per_block = blockDim.x >> 5;
+  const long long w = blockIdx.x * 1LL * warps_per_block + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  const int H = Hq + Hkv;
+  if (w >= 1LL * B * H) return;
+  const int b = static_cast<int>(w / H);
+  const int h = static_cast<int>(w % H);
+  const bool is_q = h < Hq;
+  __nv_bfloat16 *x = is_q ? q + (1LL * b * Hq + h) * D
+                          : k + (1LL * b * Hkv + (h - Hq)) * D;
+  const int half = D >> 1;
+  float lo[kMaxPairsPerLane], hi[kMaxPairsPerLane];
+  norm_rope_warp(x, is_q ? gq : gk, static_cast<float>(pos[b]), log2_theta, eps, D, lane, lo, hi);
+#pragma unroll
+  for (int j = 0; j < kMaxPairsPerLane; ++j) {
+    int i = lane + 32 * j;
+    if (i < half) {
+      x[i] = __float2bfloat16_rn(lo[j]);
+      x[i + half] = __float2bfloat16_rn(hi[j]);
+    }
+  }
+}
+
+// qk_norm_rope followed by kv_append in one pass: query heads are rotated in
+// place; a kv head's rotated k is written back to k and, with v, straight to
+// its cache row (the scatter address of kv_append, same checks and error
+// bits). The table entry is the only dependent load and it overlaps the
+// norm/rotary arithmetic.
+__global__ void qk_norm_rope_append_kernel(
+    __nv_bfloat16 *__restrict__ q, __nv_bfloat16 *__restrict__ k,
+    const __nv_bfloat16 *__restrict__ v, const __nv_bfloat16 *__restrict__ gq,
+    const __nv_bfloat16 *__restrict__ gk, const int32_t *__restrict__ batch_idx,
+    const int32_t *__restrict__ pos, float log2_theta, float eps, int B, int Hq, int Hkv,
+    int D, const int32_t *__restrict__ table, int n_slots, int max_pages, int page_size,
+    int n_pages, __nv_bfloat16 *__restrict__ k_cache, __nv_bfloat16 *__restrict__ v_cache,
+    int32_t *__restrict__ err) {
+  pkv_wait_prior_grid();
+  const int warps_per_block = blockDim.x >> 5;
+  const long long w = blockIdx.x * 1LL * warps_per_block + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  const int H = Hq + Hkv;
+  if (w >= 1LL * B * H) return;
+  const int b = static_cast<int>(w / H);
+  const int h = static_cast<int>(w % H);
+  const bool is_q = h < Hq;
+  const int half = D >> 1;
+  const int pb = pos[b];
+  if (is_q) {
+    __nv_bfloat16 *x = q + (1LL * b * Hq + h) * D;
+    float lo[kMaxPairsPerLane], hi[kMaxPairsPerLane];
+    norm_rope_warp(x, gq, static_cast<float>(pb), log2_theta, eps, D, lane, lo, hi);
+#pragma unroll
+    for (int j = 0; j < kMaxPairsPerLane; ++j) {
+      int i = lane + 32 * j;
+      if (i < half) {
+        x[i] = __float2bfloat16_rn(lo[j]);
+        x[i + half] = __float2bfloat16_rn(hi[j]);
+      }
+    }
+    return;
+  }
+  const int hk = h - Hq;
+  // scatter address (issued before the arithmetic so the table load overlaps it)
+  const int slot = batch_idx ? batch_idx[b] : b;
+  int bits = 0, page = -1;
+  if (slot < 0 || slot >= n_slots) {
+    bits = PKV_ERR_SLOT;
+  } else if (pb < 0 || pb / page_size >= max_pages) {
+    bits = PKV_ERR_POS;
+  } else {
+    page = table[static_cast<long long>(slot) * max_pages + pb / page_size];
+  }
+  __nv_bfloat16 *x = k + (1LL * b * Hkv + hk) * D;
+  const __nv_bfloat16 *vx = v + (1LL * b * Hkv + hk) * D;
+  float lo[kMaxPairsPerLane], hi[kMaxPairsPerLane];
+  norm_rope_warp(x, gk, static_cast<float>(pb), log2_theta, eps, D, lane, lo, hi);
+  if (!bits) {
+    if (page < 0) bits = PKV_ERR_PAGE_NEG;
+    else if (page >= n_pages) bits = PKV_ERR_PAGE_RANGE;
+  }
+  if (bits && hk == 0 && lane == 0 && err) atomicOr(err, bits);
+  const long long row = 1LL * page * page_size + pb % page_size;
+  __nv_bfloat16 *kc = k_cache + ((1LL * hk * n_pages * page_size) + row) * D;
+  __nv_bfloat16 *vc = v_cache + ((1LL * hk * n_pages * page_size) + row) * D;
+#pragma unroll
+  for (int j = 0; j < kMaxPairsPerLane; ++j) {
+    int i = lane + 32 * j;
+    if (i < half) {
+      const __nv_bfloat16 a = __float2bfloat16_rn(lo[j]), c = __float2bfloat16_rn(hi[j]);
+      x[i] = a;
+      x[i + half] = c;
+      if (!bits) {
+        kc[i] = a;
+        kc[i + half] = c;
+        vc[i] = vx[i];
+        vc[i + half] = vx[i + half];
+      }
     }
   }
 }
@@ -103,5 +202,39 @@ extern "C" int qk_norm_rope(pkv_bf16 *q, pkv_bf16 *k, const pkv_bf16 *gamma_q,
       reinterpret_cast<__nv_bfloat16 *>(k), reinterpret_cast<const __nv_bfloat16 *>(gamma_q),
       reinterpret_cast<const __nv_bfloat16 *>(gamma_k), pos, log2f(theta), eps, B, Hq, Hkv,
       D));
+  return pkv::ok();
+}
+
+extern "C" int qk_norm_rope_append(pkv_bf16 *q, pkv_bf16 *k, const pkv_bf16 *v,
+                                   const pkv_bf16 *gamma_q, const pkv_bf16 *gamma_k,
+                                   const int32_t *batch_idx, const int32_t *input_pos,
+                                   float theta, float eps, int B, int Hq, int Hkv, int D,
+                                   const int32_t *dev_table, int n_slots,
+                                   int max_pages_per_seq, int page_size, int n_pages,
+                                   pkv_bf16 *k_cache, pkv_bf16 *v_cache, int32_t *err_word,
+                                   void *stream) {
+  if (B < 0 || Hq < 0 || Hkv < 1 || D < 2 || D % 2 || D > 64 * kMaxPairsPerLane)
+    return pkv::fail(PKV_E_BAD_ARG, "qk_norm_rope_append: bad shape (Hkv >= 1, D even, <= 1024)");
+  if (page_size < 1 || n_pages < 1 || n_slots < 1 || max_pages_per_seq < 1)
+    return pkv::fail(PKV_E_BAD_ARG, "qk_norm_rope_append: bad table geometry");
+  if (!(theta > 0.f)) return pkv::fail(PKV_E_BAD_ARG, "qk_norm_rope_append: theta must be > 0");
+  if (!(eps >= 0.f)) return pkv::fail(PKV_E_BAD_ARG, "qk_norm_rope_append: eps must be >= 0");
+  if ((gamma_q == nullptr) != (gamma_k == nullptr))
+    return pkv::fail(PKV_E_BAD_ARG, "qk_norm_rope_append: give both gains or neither");
+  if (B == 0) return pkv::ok();
+  if (!input_pos || (Hq && !q) || !k || !v || !dev_table || !k_cache || !v_cache)
+    return pkv::fail(PKV_E_BAD_ARG, "qk_norm_rope_append: NULL tensor");
+  const long long warps = 1LL * B * (Hq + Hkv);
+  const int threads = 256, wpb = threads / 32;
+  long long blocks = (warps + wpb - 1) / wpb;
+  PKV_CUDA_CHECK(pkv::launch_pdl(
+      qk_norm_rope_append_kernel, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0,
+      static_cast<cudaStream_t>(stream), reinterpret_cast<__nv_bfloat16 *>(q),
+      reinterpret_cast<__nv_bfloat16 *>(k), reinterpret_cast<const __nv_bfloat16 *>(v),
+      reinterpret_cast<const __nv_bfloat16 *>(gamma_q),
+      reinterpret_cast<const __nv_bfloat16 *>(gamma_k), batch_idx, input_pos, log2f(theta),
+      eps, B, Hq, Hkv, D, dev_table, n_slots, max_pages_per_seq, page_size, n_pages,
+      reinterpret_cast<__nv_bfloat16 *>(k_cache), reinterpret_cast<__nv_bfloat16 *>(v_cache),
+      err_word));
   return pkv::ok();
 }

@@ -299,3 +299,45 @@ def test_graph_replay_is_bit_identical_to_eager(dev):
         assert torch.equal(bufs["out"].view(torch.int16), eager.view(torch.int16))
         assert torch.equal(bufs["kc"].view(torch.int16), eager_kc.view(torch.int16))
     assert pkv.pkv_read_error_word(err) == 0
+
+
+# ------------------------------------------------------ fused prologue
+@pytest.mark.parametrize("B,Hq,Hkv,D,ps,norm", [(8, 32, 8, 128, 64, True), (16, 24, 8, 128, 64, False),
+                                                (5, 8, 1, 256, 16, True), (3, 8, 1, 512, 64, True),
+                                                (4, 6, 3, 64, 8, True)])
+def test_fused_prologue_equals_norm_rope_then_append(dev, B, Hq, Hkv, D, ps, norm):
+    rng = np.random.default_rng(300 + B + D)
+    P, max_pages = 4 * B + 3, 4
+    table = np.full((B + 2, max_pages), -1, np.int32)
+    table[0] = 0
+    table[1:B + 1] = rng.permutation(np.arange(1, P))[:4 * B].reshape(B, 4)
+    bidx = rng.permutation(np.arange(1, B + 1)).astype(np.int32)
+    pos = rng.integers(0, 4 * ps, size=B).astype(np.int32)
+    if B > 3:   # a bad slot, a position past the row and an unreserved block
+        bidx[0], pos[1] = B + 5, 4 * ps + 3
+        table[bidx[2], pos[2] // ps] = -1
+    q = wl.randn_bf16(rng, (B, Hq, D))
+    k = wl.randn_bf16(rng, (B, Hkv, D))
+    v = wl.randn_bf16(rng, (B, Hkv, D))
+    gq, gk = wl.gamma_bf16(rng, D), wl.gamma_bf16(rng, D)
+    kc0 = wl.randn_bf16(rng, (Hkv, P * ps, D))
+    vc0 = wl.randn_bf16(rng, (Hkv, P * ps, D))
+    d = lambda a: torch.from_numpy(a).to(dev)
+    outs = []
+    for fused in (False, True):
+        dq, dk, dv = q.to(dev), k.to(dev), v.to(dev)
+        kc, vc = kc0.to(dev), vc0.to(dev)
+        err = torch.zeros(1, dtype=torch.int32, device=dev)
+        g1, g2 = (gq.to(dev), gk.to(dev)) if norm else (None, None)
+        if fused:
+            pkv.qk_norm_rope_append(dq, dk, dv, g1, g2, d(bidx), d(pos), 1e6, 1e-6, d(table),
+                                    B + 2, max_pages, ps, P, kc, vc, err)
+        else:
+            pkv.qk_norm_rope(dq, dk, g1, g2, d(pos), 1e6, 1e-6)
+            pkv.kv_append(dk, dv, d(bidx), d(pos), d(table), B + 2, max_pages, ps, P, kc, vc, err)
+        outs.append([bits(t) for t in (dq, dk, kc, vc)] + [pkv.pkv_read_error_word(err)])
+    for a, b in zip(outs[0][:4], outs[1][:4]):
+        assert np.array_equal(a, b)
+    assert outs[0][4] == outs[1][4]
+    if B > 3:
+        assert outs[1][4] == (pkv.PKV_ERR_SLOT | pkv.PKV_ERR_POS | pkv.PKV_ERR_PAGE_NEG)
