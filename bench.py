@@ -60,15 +60,54 @@ def parse_args():
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--layers", type=int, default=0,
                     help="layer caches to cycle (0: enough for 4x L2)")
+    ap.add_argument("--workload", default="rollout", choices=sorted(WORKLOAD_CHOICES),
+                    help="rollout (the headline line) or one of the static decode layers")
     return ap.parse_args()
 
 
 # ----------------------------------------------------------------- helpers --
-def attn_bytes(seq_lens: np.ndarray, B, Hq, Hkv, D, ps) -> int:
+def attn_bytes(seq_lens: np.ndarray, B, Hq, Hkv, D, ps, window: int = 0) -> int:
     """Algorithmic bytes of one paged_decode_attn call: K and V of every key
-    read once, q read, out written, one table entry per page."""
-    n = seq_lens.astype(np.int64)
-    return int(Hkv * n.sum() * D * 2 * 2 + B * Hq * D * 2 * 2 + (-(-n // ps)).sum() * 4)
+    the row attends to read once, q read, out written, one table entry per
+    page touched."""
+    L = seq_lens.astype(np.int64)
+    n = np.minimum(L, window) if window > 0 else L
+    lo = L - n
+    pages = np.where(n > 0, (L + ps - 1) // ps - lo // ps, 0)
+    return int(Hkv * n.sum() * D * 2 * 2 + B * Hq * D * 2 * 2 + pages.sum() * 4)
+
+
+# name -> (workload, layer index, description)
+WORKLOAD_CHOICES = {
+    "rollout": ("rollout", 0, None),
+    "qwen3": ("qwen3", 0, "Qwen3-4B-shaped decode layer: B=8, 32/8 heads, D=128, page 64, "
+                          "L0 ~ U[64,1024], one token appended per step, q/k norm, theta 1e6"),
+    "llama": ("llama", 0, "Llama-3.2-3B-shaped decode layer: B=16, 24/8 heads, D=128, page 64, "
+                          "L ~ U[512,1024], theta 5e5, no q/k norm"),
+    "gemma-sliding": ("gemma", 0, "Gemma-4-E2B sliding layer: B=64, 8/1 heads, D=256, window 512, "
+                                  "page 64, L ~ U[256,2048], theta 1e4, q/k norm"),
+    "gemma-full": ("gemma", 1, "Gemma-4-E2B full layer: B=64, 8/1 heads, D=512, page 64, "
+                               "L ~ U[256,2048], theta 1e6, q/k norm"),
+}
+
+
+def static_metadata(w, total_steps):
+    """Per-step tables and row metadata for a fixed batch whose rows each
+    append one token per step (host-only PageTable)."""
+    import paged_kv_decode_pagetable_gb300 as pkv
+    pt = pkv.PageTable(w.max_batch_size, w.page_size, w.n_pages, w.max_pages_per_seq)
+    L0 = wl.static_lengths(w)
+    slots = [pt.assign(int(L) + 1) for L in L0]
+    tables, bidx, pos, lens = [], [], [], []
+    for t in range(total_steps):
+        p = (L0 + t).astype(np.int32)
+        for s_, L in zip(slots, p):
+            pt.reserve(s_, int(L) + 1)
+        tables.append(pt.host_table().numpy())
+        bidx.append(np.array(slots, np.int32))
+        pos.append(p)
+        lens.append(p + 1)
+    return (np.stack(tables), np.stack(bidx), np.stack(pos), np.stack(lens))
 
 
 def measured_peaks():
@@ -211,12 +250,12 @@ class PagePool:
         self.vc = rng.standard_normal((w.n_kv_heads, pages * w.page_size, D)).astype(np.float32)
 
 
-def oracle_sample(w, lens_rows, rng, seconds, pool, min_rows=1):
+def oracle_sample(w, lens_rows, rng, seconds, pool, D=128, window=0, min_rows=1):
     """Times the oracle's attention for rows with the given lengths (cycled),
     their pages drawn from `pool`, until `seconds` of CPU time have been spent
     inside the oracle; returns (bytes, seconds, rows)."""
     import oracle
-    D, Hq, Hkv, ps = 128, w.n_q_heads, w.n_kv_heads, w.page_size
+    Hq, Hkv, ps = w.n_q_heads, w.n_kv_heads, w.page_size
     pool_pages, kc, vc = pool.pages, pool.kc, pool.vc
     total_bytes, elapsed, rows = 0, 0.0, 0
     i = 0
@@ -228,9 +267,9 @@ def oracle_sample(w, lens_rows, rng, seconds, pool, min_rows=1):
         table[1] = rng.integers(0, pool_pages, size=nb)
         q = rng.standard_normal((1, Hq, D))
         t0 = time.perf_counter()
-        oracle.decode_attention(q, kc, vc, table, [1], [L], 0, D ** -0.5, ps)
+        oracle.decode_attention(q, kc, vc, table, [1], [L], window, D ** -0.5, ps)
         elapsed += time.perf_counter() - t0
-        total_bytes += attn_bytes(np.array([L]), 1, Hq, Hkv, D, ps)
+        total_bytes += attn_bytes(np.array([L]), 1, Hq, Hkv, D, ps, window)
         rows += 1
     return total_bytes, elapsed, rows
 
@@ -284,14 +323,23 @@ def run_ours(args, world, rank, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     pkv.load_library()
-    w = wl.ROLLOUT
-    spec = engine.LayerSpec(w.layers[0].head_dim, w.layers[0].theta, 0, True, True)
+    wname, li, desc = WORKLOAD_CHOICES[args.workload]
+    w = wl.WORKLOADS[wname]
+    lay = w.layers[li]
+    spec = engine.LayerSpec(lay.head_dim, lay.theta, lay.window, lay.qk_norm, True)
     B, Hq, Hkv, D, ps = w.batch, w.n_q_heads, w.n_kv_heads, spec.head_dim, w.page_size
     W, K = args.warmup, args.steps
     total = W + K
-
-    tables, bidx, pos, lens = rollout_metadata(w, total)
-    step_bytes = np.array([attn_bytes(lens[t], B, Hq, Hkv, D, ps) for t in range(total)])
+    if wname == "rollout":
+        tables, bidx, pos, lens = rollout_metadata(w, total)
+    else:
+        # a fixed batch appends one token per step until the table rows are
+        # full, then the same steps repeat (re-appending the same positions)
+        period = min(total, w.max_seq - int(wl.static_lengths(w).max()))
+        idx = np.arange(total) % period
+        tables, bidx, pos, lens = (a[idx] for a in static_metadata(w, period))
+    step_bytes = np.array([attn_bytes(lens[t], B, Hq, Hkv, D, ps, spec.window)
+                           for t in range(total)])
     d_tables = torch.from_numpy(tables).to(dev)
     d_bidx = torch.from_numpy(bidx).to(dev)
     d_pos = torch.from_numpy(pos).to(dev)
@@ -312,7 +360,8 @@ def run_ours(args, world, rank, local):
     gk = (1 + 0.1 * torch.randn(D, generator=g, device=dev)).to(torch.bfloat16)
     out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
-    ws = engine.AttnWorkspace(B, Hq, Hkv, D, w.max_pages_per_seq, ps, 0, dev, args.num_splits)
+    ws = engine.AttnWorkspace(B, Hq, Hkv, D, w.max_pages_per_seq, ps, spec.window, dev,
+                              args.num_splits)
 
     class Geom:
         n_slots, max_pages_per_seq, page_size, n_pages = (w.n_slots, w.max_pages_per_seq, ps,
@@ -327,8 +376,8 @@ def run_ours(args, world, rank, local):
     def attn_only(t):
         kc, vc = caches[t % n_layers]
         pkv.paged_decode_attn(q, kc, vc, d_tables[t], w.n_slots, w.max_pages_per_seq, ps,
-                              w.n_pages, d_bidx[t], d_lens[t], 0, D ** -0.5, ws.splits, ws.buf,
-                              out, err)
+                              w.n_pages, d_bidx[t], d_lens[t], spec.window, D ** -0.5, ws.splits,
+                              ws.buf, out, err)
 
     # warm-up: W eager steps (first use of every kernel), then capture
     for t in range(W):
@@ -386,7 +435,8 @@ def run_ours(args, world, rank, local):
     cpu = None
     if rank == 0 and world == 1:
         rng = np.random.default_rng(w.seed(7))
-        b, s, n = oracle_sample(w, lens[W], rng, args.cpu_seconds, PagePool(w, rng))
+        b, s, n = oracle_sample(w, lens[W], rng, args.cpu_seconds, PagePool(w, rng, D), D,
+                                spec.window)
         cpu = {"value": b / s / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
                "sample": f"{n} rows with the lengths of timed step 0's batch (cycled), float64 "
                          f"NumPy on 1 host thread, {s:.1f} s"}
@@ -396,7 +446,8 @@ def run_ours(args, world, rank, local):
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
             "warmup": W, "ms_per_step": t_max / K, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": WORKLOAD_DESC, "global_batch": B * world, "seq_len": "100-1024",
+            "config": {"workload": desc or WORKLOAD_DESC, "global_batch": B * world,
+                       "seq_len": f"{int(lens[W:].min())}-{int(lens[W:].max())}",
                        "num_splits": ws.splits or "auto (length-balanced parts)",
                        "max_parts_per_row": ws.max_parts, "layer_caches_cycled": n_layers,
                        "l2_policy": f"inputs larger than L2: {n_layers} layer caches of "
@@ -406,8 +457,8 @@ def run_ours(args, world, rank, local):
                        "parallelism": f"replicas x{world}"},
             "roofline": {"bound": "hbm", "achieved": attn_gbs, "peak": peak, "unit": "GB/s",
                          "frac": attn_gbs / peak, "peak_kind": peak_kind,
-                         "kernel": "decode_attn_kernel<128> + combine_kernel",
-                         "traffic": profile_traffic("rollout_decode_attn_128",
+                         "kernel": f"decode_attn_kernel<{D}> + combine_kernel",
+                         "traffic": profile_traffic(f"{args.workload}_decode_attn_{D}",
                                                     float(step_bytes[W:].mean()))},
             "cpu_baseline": cpu,
             "e2e": e2e,
@@ -419,17 +470,23 @@ def run_ours(args, world, rank, local):
 
 def run_e2e(args, w, spec, engine, pkv, caches, n_layers, tables, bidx, pos, lens, step_bytes,
             gq, gk, ws, dev, world):
+    """The metric through the public API with host buffers: every step copies
+    its q, k, v, page table and row metadata from pinned host memory to the
+    device, runs the layer step, and copies the output back to pinned host
+    memory. As in the pages' engine (capture_decode_cudagraph / replay), the
+    steps are replayed from a CUDA graph captured over the API calls; the
+    same steps issued eagerly from Python are reported as eager_value."""
     B, Hq, Hkv, D = w.batch, w.n_q_heads, w.n_kv_heads, spec.head_dim
     n = min(args.e2e_steps, args.steps)
     W = args.warmup
-    ring = 4
+    ring = 8
     gen = torch.Generator().manual_seed(w.seed(3))
     host_q = [torch.randn((B, Hq, D), generator=gen).to(torch.bfloat16).pin_memory() for _ in range(ring)]
     host_k = [torch.randn((B, Hkv, D), generator=gen).to(torch.bfloat16).pin_memory() for _ in range(ring)]
     host_v = [torch.randn((B, Hkv, D), generator=gen).to(torch.bfloat16).pin_memory() for _ in range(ring)]
     h_tables = torch.from_numpy(tables).pin_memory()
     h_meta = torch.from_numpy(np.stack([bidx, pos, lens], axis=1)).pin_memory()   # [T][3][B]
-    h_out = torch.empty((B, Hq, D), dtype=torch.bfloat16).pin_memory()
+    h_out = [torch.empty((B, Hq, D), dtype=torch.bfloat16).pin_memory() for _ in range(ring)]
     q = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=dev)
     k = torch.empty((B, Hkv, D), dtype=torch.bfloat16, device=dev)
     v = torch.empty((B, Hkv, D), dtype=torch.bfloat16, device=dev)
@@ -452,25 +509,37 @@ def run_e2e(args, w, spec, engine, pkv, caches, n_layers, tables, bidx, pos, len
         kc, vc = caches[t % n_layers]
         engine.decode_layer_step(spec, Geom, kc, vc, q, k, v, d_meta[0], d_meta[1], d_meta[2],
                                  out, ws, gq, gk, w.eps, table=d_table)
-        h_out.copy_(out, non_blocking=True)
+        h_out[j].copy_(out, non_blocking=True)
 
     for t in range(min(W, 8)):
         one(t)
     torch.cuda.synchronize()
-    barrier(world)
     stream = torch.cuda.current_stream()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for t in range(W, W + n):
-        one(t)
-    e1.record(stream)
+
+    def timed(fn):
+        barrier(world)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return reduce_max(e0.elapsed_time(e1), world)
+
+    ms_eager = timed(lambda: [one(t) for t in range(W, W + n)])
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for t in range(W, W + n):
+            one(t)
+    g.replay()
     torch.cuda.synchronize()
-    ms = reduce_max(e0.elapsed_time(e1), world)
+    ms = timed(g.replay)
     byts = reduce_sum(float(step_bytes[W:W + n].sum()), world)
     h2d = (B * Hq * D + 2 * B * Hkv * D) * 2 + tables[0].nbytes + 3 * B * 4
     return {"value": byts / (ms * 1e-3) / 1e9, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
-            "d2h_bytes_per_step": int(B * Hq * D * 2), "steps": n,
-            "ms_per_step": ms / n}
+            "d2h_bytes_per_step": int(B * Hq * D * 2), "steps": n, "ms_per_step": ms / n,
+            "mode": "CUDA graph of the API calls, host copies inside every step",
+            "eager_value": byts / (ms_eager * 1e-3) / 1e9, "eager_ms_per_step": ms_eager / n}
 
 
 def main():
