@@ -5,7 +5,10 @@ Workload: the continuous-batching rollout with Qwen3-4B head shapes — 64
 slots, 32 q / 8 kv heads, head_dim 128, page 64, max_seq 1024, prompts
 U[100, 400], each sequence stopping at a seeded length and its slot and
 pages reused at once (fragmented placement). A step is one layer's decode
-step: q/k RMSNorm + RoPE, the K/V append, split-KV attention and combine.
+step: q/k RMSNorm + RoPE, the K/V append, split-KV attention and combine —
+by default the fused paged_decode_step kernel plus the combine (--chain:
+three separate kernels). --workload picks one of the static decode layers
+instead (qwen3 B=8, llama B=16, gemma sliding D=256 / full D=512).
 
 value      algorithmic KV-read bytes of the attention (K+V of every key,
            q in, out, table entries) / device time of the whole step, GB/s;
@@ -58,6 +61,9 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--num-splits", type=int, default=0)
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--chain", action="store_true",
+                    help="layer step as three kernels (qk_norm_rope, kv_append, attention) "
+                         "instead of the fused paged_decode_step")
     ap.add_argument("--layers", type=int, default=0,
                     help="layer caches to cycle (0: enough for 4x L2)")
     ap.add_argument("--workload", default="rollout", choices=sorted(WORKLOAD_CHOICES),
@@ -371,7 +377,8 @@ def run_ours(args, world, rank, local):
     def step(t):
         kc, vc = caches[t % n_layers]
         engine.decode_layer_step(spec, Geom, kc, vc, q, k, v, d_bidx[t], d_pos[t], d_lens[t], out,
-                                 ws, gq, gk, w.eps, err=err, table=d_tables[t])
+                                 ws, gq, gk, w.eps, err=err, table=d_tables[t],
+                                 fused=not args.chain)
 
     def attn_only(t):
         kc, vc = caches[t % n_layers]
@@ -425,7 +432,7 @@ def run_ours(args, world, rank, local):
     attn_gbs = timed_bytes / (t_attn_ms * 1e-3) / 1e9
     peaks, peak_kind = measured_peaks()
     peak = float(peaks.get("hbm_gbs", 6800.0))
-    launches_per_step = 3 + (1 if ws.max_parts > 1 else 0)
+    launches_per_step = (3 if args.chain else 1) + (1 if ws.max_parts > 1 else 0)
 
     # ---- end to end through the public API: pinned host in, output back ----
     e2e = run_e2e(args, w, spec, engine, pkv, caches, n_layers, tables, bidx, pos, lens,
@@ -454,6 +461,8 @@ def run_ours(args, world, rank, local):
                                     f"{caches[0][0].numel() * 4 / 2**20:.0f} MiB cycled; "
                                     f"{kv_step / 2**20:.0f} MiB of K/V read per step",
                        "us_per_step": t_max / K * 1e3, "attn_us_per_call": t_attn_ms / K * 1e3,
+                       "layer_step": ("qk_norm_rope + kv_append + paged_decode_attn"
+                                      if args.chain else "paged_decode_step (fused)"),
                        "parallelism": f"replicas x{world}"},
             "roofline": {"bound": "hbm", "achieved": attn_gbs, "peak": peak, "unit": "GB/s",
                          "frac": attn_gbs / peak, "peak_kind": peak_kind,
@@ -508,7 +517,7 @@ def run_e2e(args, w, spec, engine, pkv, caches, n_layers, tables, bidx, pos, len
         d_meta.copy_(h_meta[t], non_blocking=True)
         kc, vc = caches[t % n_layers]
         engine.decode_layer_step(spec, Geom, kc, vc, q, k, v, d_meta[0], d_meta[1], d_meta[2],
-                                 out, ws, gq, gk, w.eps, table=d_table)
+                                 out, ws, gq, gk, w.eps, table=d_table, fused=not args.chain)
         h_out[j].copy_(out, non_blocking=True)
 
     for t in range(min(W, 8)):

@@ -186,7 +186,7 @@ int qk_norm_rope_append(pkv_bf16 *q, pkv_bf16 *k, const pkv_bf16 *v,
  * not overlap on the GPU.
  * q: bf16 [B][Hq][D], out: bf16 [B][Hq][D], caches and table as above.
  * Requires D in {64, 128, 256, 512}, 1 <= Hq/Hkv <= 8, Hq % Hkv == 0,
- * page_size a power of two >= 8, B <= 2048, and 16-byte aligned q, out,
+ * page_size a power of two >= 8, B <= 512, and 16-byte aligned q, out,
  * caches.
  * Table entries that are negative or >= n_pages inside a row's key range
  * set PKV_ERR_PAGE_* (that row's output is then unspecified); L beyond
@@ -207,6 +207,35 @@ int paged_decode_attn_splits(int B, int Hkv, int D, int max_pages_per_seq,
                              int page_size, int window, int *num_splits);
 /* workspace bytes for up to num_splits parts per row (0 when num_splits <= 1) */
 size_t paged_decode_attn_workspace(int B, int Hq, int D, int num_splits);
+
+/* ---------------------------------------------------------------------
+ * paged_decode_step — one decode layer step in one pass: the write-then-
+ * attend order of [P1]'s attention forward (q/k norm, rotary, the paged
+ * write of [P3] PageTable.assign, then flex_attention over the pages).
+ * Results equal the sequence
+ *   qk_norm_rope(q', k', gamma_q, gamma_k, input_pos, theta, eps, ...)
+ *   kv_append(k', v, batch_idx, input_pos, ...)
+ *   paged_decode_attn(q', ..., seq_lens = input_pos + 1, ...)
+ * on copies q', k' of q and k: the caches receive the same bytes, out the
+ * same bits, err_word the same bits. q, k and v are inputs only (not
+ * rotated in place). The rotated query never leaves the SM; the rotated key
+ * is written to its cache row by the CTA that reads the row's last key tile,
+ * which also uses it directly, so no second pass over the cache is needed.
+ * Rows must name distinct slots (two rows appending into one slot would
+ * each see an unspecified subset of the other's new token). Arguments as in
+ * the three calls; requires gains both given or both NULL (no norm),
+ * theta > 0, eps >= 0, 16-byte aligned k and v. The workspace is sized as for
+ * paged_decode_attn.
+ * ------------------------------------------------------------------- */
+int paged_decode_step(const pkv_bf16 *q, const pkv_bf16 *k, const pkv_bf16 *v,
+                      const pkv_bf16 *gamma_q, const pkv_bf16 *gamma_k,
+                      const int32_t *batch_idx, const int32_t *input_pos,
+                      float theta, float eps, const int32_t *dev_table,
+                      int n_slots, int max_pages_per_seq, int page_size,
+                      int n_pages, pkv_bf16 *k_cache, pkv_bf16 *v_cache,
+                      int window, float scale, int B, int Hq, int Hkv, int D,
+                      int num_splits, void *workspace, size_t workspace_bytes,
+                      pkv_bf16 *out, int32_t *err_word, void *stream);
 
 /* ---------------------------------------------------------------------
  * paged_decode_attn_noalloc — paged_decode_attn without a caller workspace.

@@ -91,6 +91,10 @@ _SIGS = {
     "paged_decode_attn_splits": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
                                           ctypes.POINTER(_c_int)]),
     "paged_decode_attn_workspace": (_c_sz, [_c_int, _c_int, _c_int, _c_int]),
+    "paged_decode_step": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_f, _c_f, _c_p,
+                                   _c_int, _c_int, _c_int, _c_int, _c_p, _c_p, _c_int, _c_f,
+                                   _c_int, _c_int, _c_int, _c_int, _c_int, _c_p, _c_sz, _c_p,
+                                   _c_p, _c_p]),
     "pkv_read_error_word": (_c_int, [_c_p, _c_p, _c_ip]),
     "pkv_last_error": (ctypes.c_char_p, []),
 }
@@ -348,6 +352,26 @@ def paged_decode_attn(q, k_cache, v_cache, dev_table, n_slots, max_pages_per_seq
         page_size, n_pages, _ptr(batch_idx), _ptr(seq_lens), int(window), float(scale), B, Hq,
         Hkv, D, int(num_splits), _ptr(workspace), ws_bytes, _ptr(out), _ptr(err_word),
         _stream(stream)), "paged_decode_attn")
+
+
+def paged_decode_step(q, k, v, gamma_q, gamma_k, batch_idx, input_pos, theta, eps, dev_table,
+                      n_slots, max_pages_per_seq, page_size, n_pages, k_cache, v_cache, window,
+                      scale, num_splits, workspace, out, err_word=None, stream=None) -> None:
+    """qk_norm_rope + kv_append + paged_decode_attn (seq_lens = input_pos + 1)
+    in one pass; q, k and v are read only."""
+    _bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v"), _bf16(gamma_q, "gamma_q")
+    _bf16(gamma_k, "gamma_k"), _bf16(k_cache, "k_cache"), _bf16(v_cache, "v_cache")
+    _bf16(out, "out")
+    _i32(dev_table, "dev_table"), _i32(batch_idx, "batch_idx"), _i32(input_pos, "input_pos")
+    B, Hq, D = q.shape
+    Hkv = k_cache.shape[0]
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load_library().paged_decode_step(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(gamma_q), _ptr(gamma_k), _ptr(batch_idx),
+        _ptr(input_pos), float(theta), float(eps), _ptr(dev_table), n_slots, max_pages_per_seq,
+        page_size, n_pages, _ptr(k_cache), _ptr(v_cache), int(window), float(scale), B, Hq, Hkv,
+        D, int(num_splits), _ptr(workspace), ws_bytes, _ptr(out), _ptr(err_word),
+        _stream(stream)), "paged_decode_step")
 
 
 def paged_decode_attn_noalloc(q, k_cache, v_cache, dev_table, n_slots, max_pages_per_seq,

@@ -39,6 +39,7 @@
 #include <cmath>
 #include <mutex>
 
+#include "norm_rope.cuh"
 #include "pkv_internal.h"
 
 namespace {
@@ -59,9 +60,12 @@ struct Cfg {
   static constexpr int STAGE_BYTES = kT * D * 2;
   static constexpr int Q_ROW = D * 2 + 16;          // padded: conflict-free B-fragment loads
   static constexpr int Q_BYTES = kMaxG * Q_ROW;
+  // one Q stage: the G query rows, then (fused step) the raw k and v rows of
+  // the token the unit appends
+  static constexpr int Q_STAGE = Q_BYTES + 4 * D;
   static constexpr int OFF_V = NS * STAGE_BYTES;
   static constexpr int OFF_Q = 2 * NS * STAGE_BYTES;
-  static constexpr int OFF_P = OFF_Q + 2 * Q_BYTES;
+  static constexpr int OFF_P = OFF_Q + 2 * Q_STAGE;
   static constexpr int OFF_RED = OFF_P + kT * 16;                // 2 x [4][8] f32
   static constexpr int OFF_BAR = OFF_RED + 2 * kCWarps * kMaxG * 4;
   static constexpr int N_BARS = 4 * NS + 4;
@@ -69,7 +73,13 @@ struct Cfg {
   static constexpr int OFF_MISC = OFF_MASK + 2 * NS * 4;          // abort flag
   static constexpr int OFF_ROWS = OFF_MISC + 16;                  // int2 [kMaxRows]
   static constexpr int OFF_PRE = OFF_ROWS + kMaxRows * 8;         // int [kMaxRows + 1]
-  static constexpr int SMEM = OFF_PRE + (kMaxRows + 1) * 4 + 1024;  // + alignment
+  // fused step only: rotation factors of the unit's row (f32 cos[D/2],
+  // sin[D/2]), the norm gains (bf16 [D] each) and per row the cache row of
+  // its appended token (-1: not written, page error; -2: position error)
+  static constexpr int OFF_FAC = (OFF_PRE + (kMaxRows + 1) * 4 + 15) & ~15;
+  static constexpr int OFF_GAM = OFF_FAC + 4 * D;
+  static constexpr int OFF_APP = OFF_GAM + 4 * D;
+  static constexpr int SMEM = OFF_APP + kMaxRows * 4 + 1024;  // + alignment
   static constexpr int CTAS_PER_SM = D <= 128 ? 2 : 1;
 };
 
@@ -171,13 +181,14 @@ __device__ __forceinline__ uint32_t swz(int r, int chunk) {
 // ------------------------------------------------------- row geometry ----
 struct Problem {
   const int32_t *table, *batch_idx, *seq_lens;
+  int len_bias;       // L = seq_lens[b] + len_bias (1 when seq_lens holds input_pos)
   int n_slots, max_pages, log2_ps, n_pages, window, B, Hq, Hkv, G;
   int fixed_splits;   // > 0: each row cut into at most this many parts; 0: balanced
   int max_parts;      // partial slots per (row, head) in the workspace
 };
 
 struct RowInfo {
-  int slot, L, lo, t_first, n_tiles;
+  int slot, L, lo, t_first, n_tiles, raw;   // raw: seq_lens[b] as read
 };
 
 // Row b's slot, clamped length and key-tile range, read from global memory;
@@ -186,7 +197,8 @@ __device__ __forceinline__ RowInfo row_info(const Problem &p, int b, int32_t *er
                                             bool report) {
   RowInfo r;
   r.slot = p.batch_idx ? p.batch_idx[b] : b;
-  r.L = p.seq_lens[b];
+  r.raw = p.seq_lens[b];
+  r.L = r.raw < 0x7fffffff ? r.raw + p.len_bias : r.raw;
   bool empty = false;
   if (r.slot < 0 || r.slot >= p.n_slots) {
     if (report && err) atomicOr(err, PKV_ERR_SLOT);
@@ -219,6 +231,67 @@ __device__ __forceinline__ int fixed_parts(int n_tiles, int S) {
   if (n_tiles <= 0) return 0;
   const int ch = (n_tiles + S - 1) / S;
   return (n_tiles + ch - 1) / ch;
+}
+
+// Inputs of the fused decode step (qk_norm_rope + kv_append + attention);
+// unused by the plain attention kernel.
+struct StepArgs {
+  const __nv_bfloat16 *k_new, *v_new;     // [B][Hkv][D], not modified
+  const __nv_bfloat16 *gamma_q, *gamma_k; // [D] each, or both NULL (no norm)
+  float log2_theta, eps;
+  __nv_bfloat16 *k_cache, *v_cache;       // the caches the tensor maps read
+};
+
+// Cache row of token `pos` of `slot` with kv_append's checks in its order
+// (slot, position, negative page, page range); -1 and the error bit if the
+// token cannot be written.
+__device__ __forceinline__ long long append_row(const Problem &p, int slot, int pos,
+                                                int &bits) {
+  bits = 0;
+  if (slot < 0 || slot >= p.n_slots) {
+    bits = PKV_ERR_SLOT;
+    return -1;
+  }
+  if (pos < 0 || (pos >> p.log2_ps) >= p.max_pages) {
+    bits = PKV_ERR_POS;
+    return -1;
+  }
+  const int page = __ldg(p.table + static_cast<size_t>(slot) * p.max_pages + (pos >> p.log2_ps));
+  if (page < 0) {
+    bits = PKV_ERR_PAGE_NEG;
+    return -1;
+  }
+  if (page >= p.n_pages) {
+    bits = PKV_ERR_PAGE_RANGE;
+    return -1;
+  }
+  return (static_cast<long long>(page) << p.log2_ps) + (pos & ((1 << p.log2_ps) - 1));
+}
+
+// Norm + RoPE of the new k of (row b, kv head g) by one warp, then the
+// kv_append write of k and v at cache row `row` (>= 0). Used for rows that
+// have no keys to attend to (padding rows), whose append no unit performs.
+template <int D>
+__device__ __forceinline__ void step_append_head(const Problem &p, const StepArgs &sa, int b,
+                                                 int g, float fpos, long long row, int lane) {
+  constexpr int PAIRS = (D / 2 + 31) / 32;
+  constexpr int half = D / 2;
+  const size_t src = (static_cast<size_t>(b) * p.Hkv + g) * D;
+  float lo[PAIRS], hi[PAIRS];
+  pkv_norm_rope_lane<PAIRS>(sa.k_new + src, sa.gamma_k, fpos, sa.log2_theta, sa.eps, D, lane,
+                            lo, hi);
+  const size_t dst = (static_cast<size_t>(g) * p.n_pages * (1 << p.log2_ps) + row) * D;
+#pragma unroll
+  for (int j = 0; j < PAIRS; ++j) {
+    const int i = lane + 32 * j;
+    if (i < half) {
+      sa.k_cache[dst + i] = __float2bfloat16_rn(lo[j]);
+      sa.k_cache[dst + i + half] = __float2bfloat16_rn(hi[j]);
+    }
+  }
+  const uint4 *vs = reinterpret_cast<const uint4 *>(sa.v_new + src);
+  for (int c = lane; c < D / 8; c += 32)
+    reinterpret_cast<uint4 *>(sa.v_cache + dst)[c] = __ldg(vs + c);
 }
 
 // largest b in [0, B) with scale * pre[b] <= x (pre non-decreasing, pre[0] = 0);
@@ -289,14 +362,15 @@ __device__ __forceinline__ bool next_unit(const Problem &p, const int2 *rows, co
 }
 
 // ------------------------------------------------------------- kernel ----
-template <int D>
+template <int D, bool STEP>
 __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
     decode_attn_kernel(const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV,
                        const __nv_bfloat16 *__restrict__ q, const Problem p,
                        float scale_log2, float *__restrict__ o_part,
                        float *__restrict__ lse_part, int *__restrict__ parts_out,
-                       __nv_bfloat16 *__restrict__ out, int32_t *__restrict__ err) {
+                       __nv_bfloat16 *__restrict__ out, int32_t *__restrict__ err,
+                       const StepArgs sa) {
   using Cf = Cfg<D>;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -317,6 +391,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
   volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + Cf::OFF_MISC);
   int2 *rows = reinterpret_cast<int2 *>(sm + Cf::OFF_ROWS);
   int *pre = reinterpret_cast<int *>(sm + Cf::OFF_PRE);
+  int *app = reinterpret_cast<int *>(sm + Cf::OFF_APP);
 
   // ---- set-up: barriers, row cache, per-row tile or part prefix sums ----
   if (tid == 0) {
@@ -354,6 +429,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
     const RowInfo r = row_info(p, b, err, blockIdx.x == 0);
     rows[b] = make_int2(r.n_tiles > 0 ? r.slot : -1, r.L);
     pre[b + 1] = p.fixed_splits > 0 ? fixed_parts(r.n_tiles, p.fixed_splits) : r.n_tiles;
+    if constexpr (STEP) app[b] = r.raw;
   }
   __syncthreads();
   if (warp == 0) {  // inclusive scan of pre[1..B] in chunks of 32
@@ -399,12 +475,50 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
     }
   }
 
-  // rows with no key: zero output (rows spread over the CTAs)
+  if constexpr (STEP) {
+    // consumers: the norm gains, and per row with keys the cache row its new
+    // token goes to (kv_append's checks; CTA 0 reports the error bits). The
+    // table loads overlap the wait for the first tiles.
+    if (warp < kCWarps) {
+      if (sa.gamma_q) {
+        __nv_bfloat16 *gs = reinterpret_cast<__nv_bfloat16 *>(sm + Cf::OFF_GAM);
+        for (int i = tid; i < D; i += kCThreads) {
+          gs[i] = sa.gamma_q[i];
+          gs[D + i] = sa.gamma_k[i];
+        }
+      }
+      for (int b = tid; b < p.B; b += kCThreads) {
+        const int2 c = rows[b];
+        if (c.x <= 0) continue;   // no keys: appended by the zero-row pass below
+        int bits;
+        const long long row = append_row(p, c.x, app[b], bits);
+        if (bits && blockIdx.x == 0 && err) atomicOr(err, bits);
+        app[b] = row >= 0 ? static_cast<int>(row) : (bits == PKV_ERR_POS ? -2 : -1);
+      }
+      consumer_sync();
+    }
+  }
+
+  // rows with no key: zero output (rows spread over the CTAs); in the fused
+  // step their new token is still appended as kv_append would (padding rows
+  // write into the reserved page of slot 0)
   if (warp < kCWarps) {
     for (int b = blockIdx.x; b < p.B; b += gridDim.x) {
       if (pre[b + 1] != pre[b]) continue;
       __nv_bfloat16 *o = out + static_cast<size_t>(b) * p.Hq * D;
       for (int i = tid; i < p.Hq * D; i += kCThreads) o[i] = __float2bfloat16_rn(0.f);
+      if constexpr (STEP) {
+        const int slot = p.batch_idx ? __ldg(p.batch_idx + b) : b;
+        const int pos = __ldg(p.seq_lens + b);
+        int bits;
+        const long long row = append_row(p, slot, pos, bits);
+        if (bits) {
+          if (tid == 0 && err) atomicOr(err, bits);
+        } else {
+          for (int g = warp; g < p.Hkv; g += kCWarps)
+            step_append_head<D>(p, sa, b, g, static_cast<float>(pos), row, lane);
+        }
+      }
     }
   }
 
@@ -458,17 +572,31 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
       // query rows of the GQA group, one bulk copy per head into padded rows
       {
         const int qs = it_q & 1;
+        // fused step: the unit that holds the row's last tile also gets the
+        // raw k and v rows of the token it appends
+        const bool kv_rows = STEP && w.k1 == rows[w.b].y;
         if (lane == 0) {
           ok = mbar_wait(emptyQ + 8 * qs, ((it_q >> 1) & 1) ^ 1, abort_flag);
-          if (ok) mbar_expect_tx(fullQ + 8 * qs, static_cast<uint32_t>(p.G * D * 2));
+          if (ok)
+            mbar_expect_tx(fullQ + 8 * qs,
+                           static_cast<uint32_t>((p.G + (kv_rows ? 2 : 0)) * D * 2));
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
+        const uint32_t qdst = sQ + qs * Cf::Q_STAGE;
         if (lane < p.G)
-          bulk_load(sQ + qs * Cf::Q_BYTES + lane * Cf::Q_ROW,
+          bulk_load(qdst + lane * Cf::Q_ROW,
                     q + ((static_cast<size_t>(w.b) * p.Hq + static_cast<size_t>(w.g) * p.G +
                           lane) * D),
                     static_cast<uint32_t>(D * 2), fullQ + 8 * qs);
+        if constexpr (STEP) {
+          if (kv_rows && (lane == 30 || lane == 31)) {
+            const size_t src = (static_cast<size_t>(w.b) * p.Hkv + w.g) * D;
+            bulk_load(qdst + Cf::Q_BYTES + (lane - 30) * D * 2,
+                      lane == 30 ? sa.k_new + src : sa.v_new + src,
+                      static_cast<uint32_t>(D * 2), fullQ + 8 * qs);
+          }
+        }
         ++it_q;
       }
       for (int base = 0; base < n_boxes && ok; base += 32) {
@@ -572,22 +700,90 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
 
   while (next_unit(p, rows, pre, units, w)) {
     uint32_t qb[KS][2];
+    const int qs = it_q & 1;
+    const uint8_t *qstage = sm + Cf::OFF_Q + qs * Cf::Q_STAGE;
+    int patch = -1;   // fused step: row of the appended token in the unit's last tile
     {
-      const int qs = it_q & 1;
       if (!mbar_wait(fullQ + 8 * qs, (it_q >> 1) & 1, abort_flag)) {
         failed = true;
         *abort_flag = 1;
       }
+      if constexpr (STEP) {
+        // Rotate the raw query rows in place with the row's rotation factors
+        // (computed once, one pair per thread). The unit that holds the row's
+        // last tile also rotates the new k in place, writes k and v to their
+        // cache row (the kv_append of the chain) and later patches both into
+        // that tile, whose TMA copy may predate the write.
+        constexpr int PAIRS = (D / 2 + 31) / 32;
+        const int L_b = rows[w.b].y;
+        const int app_b = app[w.b];
+        const int pos_b = app_b == -2 ? __ldg(p.seq_lens + w.b) : L_b - 1;
+        const float fpos = static_cast<float>(pos_b);
+        float *fac = reinterpret_cast<float *>(sm + Cf::OFF_FAC);
+        for (int i = tid; i < D / 2; i += kCThreads) {
+          float cs, sn;
+          pkv_rope_factor(i, D, fpos, sa.log2_theta, cs, sn);
+          fac[i] = cs;
+          fac[D / 2 + i] = sn;
+        }
+        consumer_sync();
+        const __nv_bfloat16 *gq =
+            sa.gamma_q ? reinterpret_cast<const __nv_bfloat16 *>(sm + Cf::OFF_GAM) : nullptr;
+        auto table_factor = [&](int i, float &cs, float &sn) {
+          cs = fac[i];
+          sn = fac[D / 2 + i];
+        };
+        auto rotate_row = [&](__nv_bfloat16 *x, const __nv_bfloat16 *g, float (&lo)[PAIRS],
+                              float (&hi)[PAIRS]) {
+          pkv_norm_rope_core<PAIRS>(x, g, sa.eps, D, lane, table_factor, lo, hi);
+#pragma unroll
+          for (int j = 0; j < PAIRS; ++j) {
+            const int i = lane + 32 * j;
+            if (i < D / 2) {
+              x[i] = __float2bfloat16_rn(lo[j]);
+              x[i + D / 2] = __float2bfloat16_rn(hi[j]);
+            }
+          }
+        };
+        for (int h = warp; h < p.G; h += kCWarps) {
+          float lo[PAIRS], hi[PAIRS];
+          rotate_row(reinterpret_cast<__nv_bfloat16 *>(sm + Cf::OFF_Q + qs * Cf::Q_STAGE +
+                                                       h * Cf::Q_ROW),
+                     gq, lo, hi);
+        }
+        const bool append = w.k1 == L_b && app_b >= 0;
+        if (append && warp == p.G % kCWarps) {
+          __nv_bfloat16 *kx =
+              reinterpret_cast<__nv_bfloat16 *>(sm + Cf::OFF_Q + qs * Cf::Q_STAGE + Cf::Q_BYTES);
+          float lo[PAIRS], hi[PAIRS];
+          rotate_row(kx, gq ? gq + D : nullptr, lo, hi);
+          __syncwarp();
+          const size_t dst = (static_cast<size_t>(w.g) * p.n_pages * (1 << p.log2_ps) +
+                              static_cast<size_t>(app_b)) * D;
+          const uint4 *ks = reinterpret_cast<const uint4 *>(kx);
+          const uint4 *vs = reinterpret_cast<const uint4 *>(kx + D);
+          for (int c = lane; c < D / 8; c += 32) {
+            reinterpret_cast<uint4 *>(sa.k_cache + dst)[c] = ks[c];
+            reinterpret_cast<uint4 *>(sa.v_cache + dst)[c] = vs[c];
+          }
+        }
+        fence_proxy_async();
+        consumer_sync();
+        if (append) patch = pos_b & (kT - 1);
+      }
       const bool hv = gid < p.G;
-      const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
-          sm + Cf::OFF_Q + qs * Cf::Q_BYTES + (hv ? gid : 0) * Cf::Q_ROW);
+      const uint32_t *qrow =
+          reinterpret_cast<const uint32_t *>(qstage + (hv ? gid : 0) * Cf::Q_ROW);
 #pragma unroll
       for (int ks = 0; ks < KS; ++ks) {
         qb[ks][0] = hv ? qrow[(16 * ks + 2 * tig) >> 1] : 0u;
         qb[ks][1] = hv ? qrow[(16 * ks + 8 + 2 * tig) >> 1] : 0u;
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(emptyQ + 8 * qs);
+      // the fused step keeps the stage (its k / v rows) until the unit ends
+      if (!STEP) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(emptyQ + 8 * qs);
+      }
       ++it_q;
     }
     float o[MT][4];
@@ -604,6 +800,14 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
       }
       const uint32_t km = kmask[st];
       const uint32_t kbase = sK + st * Cf::STAGE_BYTES;
+      const bool patch_here = STEP && patch >= 0 && t == w.tb - 1;
+      if (patch_here && warp == (patch >> 4)) {  // this warp's 16 keys hold the new token
+        const uint4 *src = reinterpret_cast<const uint4 *>(qstage + Cf::Q_BYTES);
+        for (int c = lane; c < D / 8; c += 32)
+          *reinterpret_cast<uint4 *>(sm + st * Cf::STAGE_BYTES + swz(patch, c)) = src[c];
+        fence_proxy_async();
+        __syncwarp();
+      }
 
       // ---- S^T[16 keys x 8 heads], keys 16*warp .. +15 of the tile ----
       float sacc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -683,6 +887,12 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
         }
         fence_proxy_async();
       }
+      if (patch_here && tid < D / 8) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(qstage + Cf::Q_BYTES + D * 2);
+        *reinterpret_cast<uint4 *>(sm + Cf::OFF_V + st * Cf::STAGE_BYTES + swz(patch, tid)) =
+            src[tid];
+        fence_proxy_async();
+      }
       consumer_sync();  // (2) P, sums and V visible
       float ts0 = 0.f, ts1 = 0.f;
 #pragma unroll
@@ -724,6 +934,10 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(emptyV + 8 * st);
+    }
+    if constexpr (STEP) {   // the unit's Q stage (and its k / v rows) is free
+      __syncwarp();
+      if (lane == 0) mbar_arrive(emptyQ + 8 * qs);
     }
 
     if (failed) continue;
@@ -856,7 +1070,7 @@ int make_cache_map(CUtensorMap *tm, const void *base, long long rows, int D,
   return PKV_OK;
 }
 
-template <int D>
+template <int D, bool STEP>
 int set_smem_attr() {
   static std::mutex mu;
   static bool done[64] = {false};
@@ -865,7 +1079,7 @@ int set_smem_attr() {
   if (dev < 0 || dev >= 64) return pkv::fail(PKV_E_CUDA, "device id out of range");
   std::lock_guard<std::mutex> lock(mu);
   if (!done[dev]) {
-    PKV_CUDA_CHECK(cudaFuncSetAttribute(decode_attn_kernel<D>,
+    PKV_CUDA_CHECK(cudaFuncSetAttribute(decode_attn_kernel<D, STEP>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         Cfg<D>::SMEM));
     done[dev] = true;
@@ -873,20 +1087,21 @@ int set_smem_attr() {
   return PKV_OK;
 }
 
-template <int D>
+template <int D, bool STEP>
 int launch_attn(const CUtensorMap &tmK, const CUtensorMap &tmV, const pkv_bf16 *q,
                 const Problem &p, float scale_log2, float *o_part, float *lse_part,
-                int *parts, pkv_bf16 *out, int32_t *err, cudaStream_t stream) {
-  int st = set_smem_attr<D>();
+                int *parts, pkv_bf16 *out, int32_t *err, const StepArgs &sa,
+                cudaStream_t stream) {
+  int st = set_smem_attr<D, STEP>();
   if (st != PKV_OK) return st;
   const int sms = pkv::sm_count();
   if (sms <= 0) return pkv::fail(PKV_E_CUDA, "paged_decode_attn: no SM count");
   const int grid = sms * Cfg<D>::CTAS_PER_SM;
-  PKV_CUDA_CHECK(pkv::launch_pdl(decode_attn_kernel<D>, dim3(grid), dim3(kThreads),
+  PKV_CUDA_CHECK(pkv::launch_pdl(decode_attn_kernel<D, STEP>, dim3(grid), dim3(kThreads),
                                  Cfg<D>::SMEM, stream, tmK, tmV,
                                  reinterpret_cast<const __nv_bfloat16 *>(q), p, scale_log2,
                                  o_part, lse_part, parts,
-                                 reinterpret_cast<__nv_bfloat16 *>(out), err));
+                                 reinterpret_cast<__nv_bfloat16 *>(out), err, sa));
   return PKV_OK;
 }
 
@@ -925,49 +1140,66 @@ int paged_decode_attn_splits(int B, int Hkv, int D, int max_pages_per_seq,
   return pkv::ok();
 }
 
-int paged_decode_attn(const pkv_bf16 *q, const pkv_bf16 *k_cache,
-                      const pkv_bf16 *v_cache, const int32_t *dev_table,
-                      int n_slots, int max_pages_per_seq, int page_size,
-                      int n_pages, const int32_t *batch_idx,
-                      const int32_t *seq_lens, int window, float scale, int B,
-                      int Hq, int Hkv, int D, int num_splits, void *workspace,
-                      size_t workspace_bytes, pkv_bf16 *out, int32_t *err_word,
-                      void *stream) {
+}  // extern "C"
+
+namespace {
+
+// Argument checks, tensor maps, problem set-up and the launches shared by
+// paged_decode_attn (sa == nullptr; seq_lens = lengths) and the fused
+// paged_decode_step (seq_lens = input positions, lengths = positions + 1).
+int decode_common(const char *fn, const pkv_bf16 *q, const pkv_bf16 *k_cache,
+                  const pkv_bf16 *v_cache, const int32_t *dev_table, int n_slots,
+                  int max_pages_per_seq, int page_size, int n_pages,
+                  const int32_t *batch_idx, const int32_t *seq_lens, int window, float scale,
+                  int B, int Hq, int Hkv, int D, int num_splits, void *workspace,
+                  size_t workspace_bytes, pkv_bf16 *out, int32_t *err_word,
+                  const StepArgs *sa, void *stream) {
   if (D != 64 && D != 128 && D != 256 && D != 512)
-    return pkv::fail(PKV_E_BAD_ARG, "paged_decode_attn: D must be 64, 128, 256 or 512");
+    return pkv::fail(PKV_E_BAD_ARG, "%s: D must be 64, 128, 256 or 512", fn);
   if (Hkv < 1 || Hq < Hkv || Hq % Hkv || Hq / Hkv > kMaxG)
-    return pkv::fail(PKV_E_BAD_ARG, "paged_decode_attn: need Hq %% Hkv == 0 and Hq/Hkv <= %d", kMaxG);
+    return pkv::fail(PKV_E_BAD_ARG, "%s: need Hq %% Hkv == 0 and Hq/Hkv <= %d", fn, kMaxG);
   if (!pkv::is_pow2(page_size) || page_size < 8)
-    return pkv::fail(PKV_E_BAD_ARG, "paged_decode_attn: page_size must be a power of two >= 8");
+    return pkv::fail(PKV_E_BAD_ARG, "%s: page_size must be a power of two >= 8", fn);
   if (B < 0 || n_slots < 1 || max_pages_per_seq < 1 || n_pages < 1 || num_splits < 0)
-    return pkv::fail(PKV_E_BAD_ARG, "paged_decode_attn: bad size argument");
+    return pkv::fail(PKV_E_BAD_ARG, "%s: bad size argument", fn);
   if (B > kMaxRows)
-    return pkv::fail(PKV_E_BAD_ARG, "paged_decode_attn: B must be <= %d", kMaxRows);
+    return pkv::fail(PKV_E_BAD_ARG, "%s: B must be <= %d", fn, kMaxRows);
   if (static_cast<long long>(max_pages_per_seq) * page_size > (1LL << 30))
-    return pkv::fail(PKV_E_BAD_ARG, "paged_decode_attn: table row too long");
+    return pkv::fail(PKV_E_BAD_ARG, "%s: table row too long", fn);
   const long long rows = 1LL * Hkv * n_pages * page_size;
   if (rows >= (1LL << 31))
-    return pkv::fail(PKV_E_BAD_ARG, "paged_decode_attn: cache has too many rows");
+    return pkv::fail(PKV_E_BAD_ARG, "%s: cache has too many rows", fn);
   if (!(scale > 0.f) || !std::isfinite(scale))
-    return pkv::fail(PKV_E_BAD_ARG, "paged_decode_attn: scale must be finite and > 0");
+    return pkv::fail(PKV_E_BAD_ARG, "%s: scale must be finite and > 0", fn);
+  if (sa) {
+    if (!(sa->log2_theta > -INFINITY) || !std::isfinite(sa->log2_theta))
+      return pkv::fail(PKV_E_BAD_ARG, "%s: theta must be finite and > 0", fn);
+    if (!(sa->eps >= 0.f))
+      return pkv::fail(PKV_E_BAD_ARG, "%s: eps must be >= 0", fn);
+    if ((sa->gamma_q == nullptr) != (sa->gamma_k == nullptr))
+      return pkv::fail(PKV_E_BAD_ARG, "%s: give both gains or neither", fn);
+  }
   if (B == 0) return pkv::ok();
   if (!q || !k_cache || !v_cache || !dev_table || !seq_lens || !out)
-    return pkv::fail(PKV_E_BAD_ARG, "paged_decode_attn: NULL tensor");
+    return pkv::fail(PKV_E_BAD_ARG, "%s: NULL tensor", fn);
+  if (sa && (!sa->k_new || !sa->v_new))
+    return pkv::fail(PKV_E_BAD_ARG, "%s: NULL tensor", fn);
   if (!pkv::aligned16(q) || !pkv::aligned16(out) || !pkv::aligned16(k_cache) ||
-      !pkv::aligned16(v_cache))
-    return pkv::fail(PKV_E_BAD_ARG, "paged_decode_attn: tensors must be 16-byte aligned");
+      !pkv::aligned16(v_cache) ||
+      (sa && (!pkv::aligned16(sa->k_new) || !pkv::aligned16(sa->v_new))))
+    return pkv::fail(PKV_E_BAD_ARG, "%s: tensors must be 16-byte aligned", fn);
   {
     const long long row_tiles = (1LL * max_pages_per_seq * page_size + kT - 1) / kT + 1;
     if (1LL * B * Hkv * row_tiles >= (1LL << 31))
-      return pkv::fail(PKV_E_BAD_ARG, "paged_decode_attn: B * Hkv * tiles per row too large");
+      return pkv::fail(PKV_E_BAD_ARG, "%s: B * Hkv * tiles per row too large", fn);
   }
   const int max_parts = max_parts_for(max_pages_per_seq, page_size, window, num_splits);
   const size_t need = paged_decode_attn_workspace(B, Hq, D, max_parts);
   if (need > 0) {
     if (!workspace || workspace_bytes < need)
-      return pkv::fail(PKV_E_BAD_ARG, "paged_decode_attn: workspace needs %zu bytes", need);
+      return pkv::fail(PKV_E_BAD_ARG, "%s: workspace needs %zu bytes", fn, need);
     if (!pkv::aligned16(workspace))
-      return pkv::fail(PKV_E_BAD_ARG, "paged_decode_attn: workspace must be 16-byte aligned");
+      return pkv::fail(PKV_E_BAD_ARG, "%s: workspace must be 16-byte aligned", fn);
   }
   int *parts = nullptr;
   float *o_part = nullptr, *lse_part = nullptr;
@@ -988,6 +1220,7 @@ int paged_decode_attn(const pkv_bf16 *q, const pkv_bf16 *k_cache,
   p.table = dev_table;
   p.batch_idx = batch_idx;
   p.seq_lens = seq_lens;
+  p.len_bias = sa ? 1 : 0;
   p.n_slots = n_slots;
   p.max_pages = max_pages_per_seq;
   p.log2_ps = log2_ps;
@@ -1002,20 +1235,20 @@ int paged_decode_attn(const pkv_bf16 *q, const pkv_bf16 *k_cache,
   p.max_parts = max_parts;
   const float scale_log2 = scale * 1.4426950408889634f;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const StepArgs none = {};
+  const StepArgs &a = sa ? *sa : none;
+#define PKV_LAUNCH(DD)                                                                        \
+  st = sa ? launch_attn<DD, true>(tmK, tmV, q, p, scale_log2, o_part, lse_part, parts, out,   \
+                                  err_word, a, s)                                             \
+          : launch_attn<DD, false>(tmK, tmV, q, p, scale_log2, o_part, lse_part, parts, out,  \
+                                   err_word, a, s)
   switch (D) {
-    case 64:
-      st = launch_attn<64>(tmK, tmV, q, p, scale_log2, o_part, lse_part, parts, out, err_word, s);
-      break;
-    case 128:
-      st = launch_attn<128>(tmK, tmV, q, p, scale_log2, o_part, lse_part, parts, out, err_word, s);
-      break;
-    case 256:
-      st = launch_attn<256>(tmK, tmV, q, p, scale_log2, o_part, lse_part, parts, out, err_word, s);
-      break;
-    default:
-      st = launch_attn<512>(tmK, tmV, q, p, scale_log2, o_part, lse_part, parts, out, err_word, s);
-      break;
+    case 64: PKV_LAUNCH(64); break;
+    case 128: PKV_LAUNCH(128); break;
+    case 256: PKV_LAUNCH(256); break;
+    default: PKV_LAUNCH(512); break;
   }
+#undef PKV_LAUNCH
   if (st != PKV_OK) return st;
   if (max_parts > 1) {
     const int rows_bh = B * Hq;
@@ -1028,6 +1261,49 @@ int paged_decode_attn(const pkv_bf16 *q, const pkv_bf16 *k_cache,
                                    reinterpret_cast<__nv_bfloat16 *>(out)));
   }
   return pkv::ok();
+}
+
+}  // namespace
+
+extern "C" {
+
+int paged_decode_attn(const pkv_bf16 *q, const pkv_bf16 *k_cache,
+                      const pkv_bf16 *v_cache, const int32_t *dev_table,
+                      int n_slots, int max_pages_per_seq, int page_size,
+                      int n_pages, const int32_t *batch_idx,
+                      const int32_t *seq_lens, int window, float scale, int B,
+                      int Hq, int Hkv, int D, int num_splits, void *workspace,
+                      size_t workspace_bytes, pkv_bf16 *out, int32_t *err_word,
+                      void *stream) {
+  return decode_common("paged_decode_attn", q, k_cache, v_cache, dev_table, n_slots,
+                       max_pages_per_seq, page_size, n_pages, batch_idx, seq_lens, window,
+                       scale, B, Hq, Hkv, D, num_splits, workspace, workspace_bytes, out,
+                       err_word, nullptr, stream);
+}
+
+int paged_decode_step(const pkv_bf16 *q, const pkv_bf16 *k, const pkv_bf16 *v,
+                      const pkv_bf16 *gamma_q, const pkv_bf16 *gamma_k,
+                      const int32_t *batch_idx, const int32_t *input_pos, float theta,
+                      float eps, const int32_t *dev_table, int n_slots,
+                      int max_pages_per_seq, int page_size, int n_pages, pkv_bf16 *k_cache,
+                      pkv_bf16 *v_cache, int window, float scale, int B, int Hq, int Hkv,
+                      int D, int num_splits, void *workspace, size_t workspace_bytes,
+                      pkv_bf16 *out, int32_t *err_word, void *stream) {
+  if (!(theta > 0.f) || !std::isfinite(theta))
+    return pkv::fail(PKV_E_BAD_ARG, "paged_decode_step: theta must be finite and > 0");
+  StepArgs sa;
+  sa.k_new = reinterpret_cast<const __nv_bfloat16 *>(k);
+  sa.v_new = reinterpret_cast<const __nv_bfloat16 *>(v);
+  sa.gamma_q = reinterpret_cast<const __nv_bfloat16 *>(gamma_q);
+  sa.gamma_k = reinterpret_cast<const __nv_bfloat16 *>(gamma_k);
+  sa.log2_theta = log2f(theta);
+  sa.eps = eps;
+  sa.k_cache = reinterpret_cast<__nv_bfloat16 *>(k_cache);
+  sa.v_cache = reinterpret_cast<__nv_bfloat16 *>(v_cache);
+  return decode_common("paged_decode_step", q, k_cache, v_cache, dev_table, n_slots,
+                       max_pages_per_seq, page_size, n_pages, batch_idx, input_pos, window,
+                       scale, B, Hq, Hkv, D, num_splits, workspace, workspace_bytes, out,
+                       err_word, &sa, stream);
 }
 
 }  // extern "C"

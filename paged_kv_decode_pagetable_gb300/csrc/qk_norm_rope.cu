@@ -1,16 +1,7 @@
 // qk_norm_rope: per-head RMSNorm followed by rotate-half RoPE, in place.
 //
-// Order and convention from "unsloth: compare main...flex-moe-qwen3" ·
-// unsloth/inference/flex_gemma4_moe.py · attention forward (q_norm / k_norm
-// on the head axis, then rotary) and Rotary helpers (rotate_half =
-// cat(-x2, x1); x*cos + rotate_half(x)*sin):
-//   r = x * rsqrt(mean(x^2) + eps) * gamma
-//   y_i = r_i cos(phi_i) - r_{i+D/2} sin(phi_i)
-//   y_{i+D/2} = r_{i+D/2} cos(phi_i) + r_i sin(phi_i),  phi_i = pos*theta^(-2i/D)
-//
-// One warp per (row, head); lane l owns the rotation pairs (i, i + D/2) for
-// i = l, l + 32, ...  so each lane rotates with no exchange and the only
-// cross-lane step is the sum of squares. fp32 math, one rounding to bf16.
+// The arithmetic (fp32, one rounding to bf16) is pkv_norm_rope_lane in
+// norm_rope.cuh, shared with the fused decode step. One warp per (row, head).
 // qk_norm_rope_append fuses the decode K/V scatter of "unsloth: compare
 // main...transformers-continuous-batching-qwen3" · flex_paged_attention.py ·
 // PageTable.assign into the same pass (write-then-attend order of the
@@ -18,54 +9,19 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include "norm_rope.cuh"
 #include "pkv_internal.h"
 
 namespace {
 
 constexpr int kMaxPairsPerLane = 16;  // D <= 1024
 
-// Norm + RoPE of one head vector x[0..D) held by a warp: lane l owns pairs
-// (i, i + D/2), i = l + 32j. Returns the rotated values in lo[] / hi[].
 __device__ __forceinline__ void norm_rope_warp(const __nv_bfloat16 *__restrict__ x,
                                                const __nv_bfloat16 *__restrict__ g, float p,
                                                float log2_theta, float eps, int D, int lane,
                                                float (&lo)[kMaxPairsPerLane],
                                                float (&hi)[kMaxPairsPerLane]) {
-  const int half = D >> 1;
-  float ss = 0.f;
-#pragma unroll
-  for (int j = 0; j < kMaxPairsPerLane; ++j) {
-    int i = lane + 32 * j;
-    if (i < half) {
-      lo[j] = __bfloat162float(x[i]);
-      hi[j] = __bfloat162float(x[i + half]);
-      ss = fmaf(lo[j], lo[j], ss);
-      ss = fmaf(hi[j], hi[j], ss);
-    }
-  }
-  float inv_rms = 1.f;
-  if (g) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    inv_rms = rsqrtf(ss / static_cast<float>(D) + eps);
-  }
-#pragma unroll
-  for (int j = 0; j < kMaxPairsPerLane; ++j) {
-    int i = lane + 32 * j;
-    if (i < half) {
-      float r1 = lo[j], r2 = hi[j];
-      if (g) {
-        r1 = r1 * inv_rms * __bfloat162float(g[i]);
-        r2 = r2 * inv_rms * __bfloat162float(g[i + half]);
-      }
-      // theta^(-2i/D) = 2^(-(2i/D) log2 theta)
-      float inv_freq = exp2f(-(2.0f * i / static_cast<float>(D)) * log2_theta);
-      float sn, cs;
-      sincosf(p * inv_freq, &sn, &cs);
-      lo[j] = r1 * cs - r2 * sn;
-      hi[j] = r2 * cs + r1 * sn;
-    }
-  }
+  pkv_norm_rope_lane<kMaxPairsPerLane>(x, g, p, log2_theta, eps, D, lane, lo, hi);
 }
 
 __global__ void qk_norm_rope_kernel(__nv_bfloat16 *__restrict__ q,

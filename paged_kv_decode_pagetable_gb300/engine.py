@@ -3,9 +3,11 @@
 The step follows the write-then-attend order of "unsloth: compare
 main...flex-moe-qwen3" · flex_gemma4_moe.py · attention forward: per-head
 q/k RMSNorm, RoPE, the paged write of the new K/V, then attention over keys
-0..pos. All three run as CUDA kernels of libpkv on the caller's stream with
-fixed shapes, so a step can be captured in a CUDA graph (the pages capture
-the decode step per batch bucket, capture_decode_cudagraph).
+0..pos. By default the whole step is one fused libpkv kernel (plus the split
+combine); the three separate kernels remain available. Everything runs on
+the caller's stream with fixed shapes, so a step can be captured in a CUDA
+graph (the pages capture the decode step per batch bucket,
+capture_decode_cudagraph).
 
 The driver applies a schedule of finished / admitted requests to the
 PageTable the way the pages' generate loop does (free on finish, assign a
@@ -20,7 +22,7 @@ import numpy as np
 import torch
 
 from . import (PageTable, kv_append, paged_decode_attn, paged_decode_attn_splits,
-               paged_decode_attn_workspace, qk_norm_rope)
+               paged_decode_attn_workspace, paged_decode_step, qk_norm_rope)
 
 
 @dataclasses.dataclass(frozen=True)
@@ -62,25 +64,33 @@ class AttnWorkspace:
 def decode_layer_step(spec: LayerSpec, pt: PageTable, k_cache, v_cache, q, k, v, batch_idx,
                       input_pos, seq_lens, out, ws: AttnWorkspace, gamma_q=None, gamma_k=None,
                       eps: float = 1e-6, scale: float | None = None, err=None, stream=None,
-                      table=None):
-    """qk_norm_rope -> kv_append -> paged_decode_attn for one layer.
+                      table=None, fused: bool = True):
+    """One layer's decode step: q/k norm + RoPE, K/V append, attention.
+
+    fused (default, rotary layers): one paged_decode_step call; q, k and v
+    are read only and seq_lens must equal input_pos + 1 (the kernel derives
+    it). Otherwise the chain qk_norm_rope -> kv_append -> paged_decode_attn,
+    which rotates q and k in place; both give the same bits.
 
     `pt` supplies the table geometry (n_slots, max_pages_per_seq, page_size,
     n_pages) and, unless `table` is given, the device table itself."""
     table = pt.dev_table if table is None else table
-    # Two small kernels rather than the fused qk_norm_rope_append: kv_append's
-    # few CTAs can share the SMs with the early-launched persistent attention
-    # CTAs, which the fused kernel's CTAs cannot (measured: 38.5 vs 42-43 us
-    # per layer step on the rollout workload).
+    scale = scale if scale is not None else spec.head_dim ** -0.5
+    gq = gamma_q if spec.qk_norm else None
+    gk = gamma_k if spec.qk_norm else None
+    if fused and spec.rope:
+        paged_decode_step(q, k, v, gq, gk, batch_idx, input_pos, spec.theta, eps, table,
+                          pt.n_slots, pt.max_pages_per_seq, pt.page_size, pt.n_pages, k_cache,
+                          v_cache, spec.window, scale, ws.splits, ws.buf, out, err,
+                          stream=stream)
+        return
     if spec.rope:
-        qk_norm_rope(q, k, gamma_q if spec.qk_norm else None, gamma_k if spec.qk_norm else None,
-                     input_pos, spec.theta, eps, stream=stream)
+        qk_norm_rope(q, k, gq, gk, input_pos, spec.theta, eps, stream=stream)
     kv_append(k, v, batch_idx, input_pos, table, pt.n_slots, pt.max_pages_per_seq,
               pt.page_size, pt.n_pages, k_cache, v_cache, err, stream=stream)
     paged_decode_attn(q, k_cache, v_cache, table, pt.n_slots, pt.max_pages_per_seq,
-                      pt.page_size, pt.n_pages, batch_idx, seq_lens, spec.window,
-                      scale if scale is not None else spec.head_dim ** -0.5, ws.splits,
-                      ws.buf, out, err, stream=stream)
+                      pt.page_size, pt.n_pages, batch_idx, seq_lens, spec.window, scale,
+                      ws.splits, ws.buf, out, err, stream=stream)
 
 
 @dataclasses.dataclass

@@ -1,9 +1,12 @@
 """End-to-end GPU parity on the five workloads (C ABI, real allocator).
 
-Each step runs qk_norm_rope -> kv_append -> paged_decode_attn as the
-product does and is compared with the oracle:
+Each step runs the layer step as the product does (the fused
+paged_decode_step, or the chain qk_norm_rope -> kv_append ->
+paged_decode_attn) and is compared with the oracle:
   * the device page table equals the oracle allocator's table (bit-exact);
-  * q/k after norm+RoPE are within one bf16 rounding of the oracle;
+  * q/k after norm+RoPE are within one bf16 rounding of the oracle (for
+    the fused step, which leaves q and k unrotated, the rotation is
+    recomputed with qk_norm_rope, whose bits the fused kernel reproduces);
   * the appended cache rows equal the GPU's roped k / raw v (bit-exact);
   * attention equals the oracle fed the GPU's own bf16 q and cache
     (max abs <= 1e-2, mean abs <= 1e-3); on the last step of each workload
@@ -82,13 +85,25 @@ def _check_step(w, spec, pt, model, kc, vc, q_raw, k_raw, v_raw, q_gpu, k_gpu, o
         assert_attn_close(f64(out), ref2)
 
 
+def _rotated(spec, q, k, gq, gk, pos, eps, dev, fused):
+    """The rotated q and k the step attended with: the in-place result of the
+    chain, or (fused step) qk_norm_rope applied to copies of the inputs."""
+    if not (fused and spec.rope):
+        return q, k
+    qr, kr = q.clone(), k.clone()
+    g = (lambda t: None if t is None or not spec.qk_norm else t.to(dev))
+    pkv.qk_norm_rope(qr, kr, g(gq), g(gk), pos, spec.theta, eps)
+    return qr, kr
+
+
 def _specs(w):
     rope = w.name != "tiny"
     return [engine.LayerSpec(l.head_dim, l.theta, l.window, l.qk_norm, rope) for l in w.layers]
 
 
+@pytest.mark.parametrize("fused", [True, False])
 @pytest.mark.parametrize("name,steps", [("qwen3", 64), ("llama", 4), ("gemma", 2)])
-def test_static_workload(dev, name, steps):
+def test_static_workload(dev, name, steps, fused):
     w = wl.WORKLOADS[name]
     rng = np.random.default_rng(w.seed())
     pt = pkv.PageTable(w.max_batch_size, w.page_size, w.n_pages, w.max_pages_per_seq, device=dev)
@@ -130,10 +145,12 @@ def test_static_workload(dev, name, steps):
             kc, vc = caches[li]
             engine.decode_layer_step(spec, pt, kc, vc, q, k, v, d_bidx, d_pos, d_lens, out,
                                      wss[li], None if gq is None else gq.to(dev),
-                                     None if gk is None else gk.to(dev), w.eps, err=err)
+                                     None if gk is None else gk.to(dev), w.eps, err=err,
+                                     fused=fused)
             torch.cuda.synchronize()
             if t in check_at:
-                _check_step(w, spec, pt, model, kc, vc, q_raw, k_raw, v_raw, q, k, out, meta,
+                qr, kr = _rotated(spec, q, k, gq, gk, d_pos, w.eps, dev, fused)
+                _check_step(w, spec, pt, model, kc, vc, q_raw, k_raw, v_raw, qr, kr, out, meta,
                             gq, gk, check_chain=(t == steps - 1))
         length = [L + 1 for L in length]
     assert pkv.pkv_read_error_word(err) == 0
@@ -182,7 +199,8 @@ def test_tiny_workload_permuted_pages(dev):
         assert_attn_close(f64(out), ref)
 
 
-def test_rollout_continuous_batching(dev):
+@pytest.mark.parametrize("fused", [True, False])
+def test_rollout_continuous_batching(dev, fused):
     """64 slots, 512 steps; finished sequences free their slot and pages and
     new prompts take them at once, so placement fragments."""
     w = wl.ROLLOUT
@@ -223,14 +241,15 @@ def test_rollout_continuous_batching(dev):
         k_raw = wl.randn_bf16(rng, (w.batch, w.n_kv_heads, D))
         v_raw = wl.randn_bf16(rng, (w.batch, w.n_kv_heads, D))
         q, k, v = q_raw.to(dev), k_raw.to(dev), v_raw.to(dev)
+        d_pos = torch.from_numpy(meta.input_pos).to(dev)
         engine.decode_layer_step(spec, pt, kc, vc, q, k, v,
-                                 torch.from_numpy(meta.batch_idx).to(dev),
-                                 torch.from_numpy(meta.input_pos).to(dev),
+                                 torch.from_numpy(meta.batch_idx).to(dev), d_pos,
                                  torch.from_numpy(meta.seq_lens).to(dev), out, ws, dgq, dgk,
-                                 w.eps, err=err)
+                                 w.eps, err=err, fused=fused)
         if t in check_at:
             torch.cuda.synchronize()
-            _check_step(w, spec, pt, model, kc, vc, q_raw, k_raw, v_raw, q, k, out, meta,
+            qr, kr = _rotated(spec, q, k, gq, gk, d_pos, w.eps, dev, fused)
+            _check_step(w, spec, pt, model, kc, vc, q_raw, k_raw, v_raw, qr, kr, out, meta,
                         gq, gk, check_chain=(t == w.steps - 1))
         elif t % 16 == 0:
             assert np.array_equal(pt.dev_table.cpu().numpy(), model.table), t
