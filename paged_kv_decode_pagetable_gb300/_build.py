@@ -40,7 +40,7 @@ def _stale(obj: str, deps: list[str]) -> bool:
 def build(verbose: bool = False, force: bool = False) -> str:
     nvcc = _nvcc()
     os.makedirs(BUILD, exist_ok=True)
-    headers = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".h")]
+    headers = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".h", ".cuh"))]
     headers.append(os.path.join(ROOT, "include", "pkv.h"))
     jobs = []
     objs = []
