@@ -51,6 +51,11 @@ constexpr int kThreads = kCThreads + 32;   // + producer warp
 constexpr int kMaxG = 8;             // query heads per kv head (MMA N)
 constexpr int kMaxRows = 512;        // rows per call (row cache kept in smem)
 constexpr int kSpinLimit = 1 << 22;
+// Balanced split cost model, in quarter tiles: a key tile costs kTileCost and
+// starting a (row, kv head) costs kUnitCost more (its query load, table
+// lookups and epilogue measured at about three quarters of a tile's time).
+constexpr int kTileCost = 4;
+constexpr int kUnitCost = 3;
 
 template <int D>
 struct Cfg {
@@ -71,17 +76,21 @@ struct Cfg {
   static constexpr int N_BARS = 4 * NS + 4;
   static constexpr int OFF_MASK = OFF_BAR + N_BARS * 8;           // 2 x NS u32
   static constexpr int OFF_MISC = OFF_MASK + 2 * NS * 4;          // abort flag
-  static constexpr int OFF_ROWS = OFF_MISC + 16;                  // int2 [kMaxRows]
+  static constexpr int OFF_DESC = OFF_MISC + 16;                  // Unit [2] (48 B each)
+  static constexpr int OFF_ROWS = OFF_DESC + 2 * 48;              // int2 [kMaxRows]
   static constexpr int OFF_PRE = OFF_ROWS + kMaxRows * 8;         // int [kMaxRows + 1]
+  static constexpr int OFF_PRC = OFF_PRE + (kMaxRows + 1) * 4;    // int [kMaxRows + 1]
   // fused step only: rotation factors of the unit's row (f32 cos[D/2],
-  // sin[D/2]), the norm gains (bf16 [D] each) and per row the cache row of
-  // its appended token (-1: not written, page error; -2: position error)
-  static constexpr int OFF_FAC = (OFF_PRE + (kMaxRows + 1) * 4 + 15) & ~15;
+  // sin[D/2]) and the norm gains (bf16 [D] each)
+  static constexpr int OFF_FAC = (OFF_PRC + (kMaxRows + 1) * 4 + 15) & ~15;
   static constexpr int OFF_GAM = OFF_FAC + 4 * D;
-  static constexpr int OFF_APP = OFF_GAM + 4 * D;
-  static constexpr int SMEM = OFF_APP + kMaxRows * 4 + 1024;  // + alignment
+  static constexpr int SMEM = OFF_GAM + 4 * D + 1024;  // + alignment
   static constexpr int CTAS_PER_SM = D <= 128 ? 2 : 1;
 };
+// shared memory per SM on sm_103a: 228 KB, of which 1 KB is reserved per CTA
+static_assert(Cfg<64>::CTAS_PER_SM * (Cfg<64>::SMEM + 1024) <= 228 * 1024, "D=64 residency");
+static_assert(Cfg<128>::CTAS_PER_SM * (Cfg<128>::SMEM + 1024) <= 228 * 1024, "D=128 residency");
+static_assert(Cfg<256>::SMEM <= 227 * 1024 && Cfg<512>::SMEM <= 227 * 1024, "smem per CTA");
 
 // ---------------------------------------------------------------- PTX ----
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -143,6 +152,19 @@ __device__ __forceinline__ void fence_proxy_async() {
 __device__ __forceinline__ void consumer_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(kCThreads) : "memory");
 }
+// consumer_sync that also returns the OR of `v` over the consumer threads
+__device__ __forceinline__ bool consumer_sync_or(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 q, %1, 0;\n\t"
+      "bar.red.or.pred p, 1, %2, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(v)), "n"(kCThreads)
+      : "memory");
+  return r != 0;
+}
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1,
                                         uint32_t &r2, uint32_t &r3) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
@@ -188,8 +210,12 @@ struct Problem {
 };
 
 struct RowInfo {
-  int slot, L, lo, t_first, n_tiles, raw;   // raw: seq_lens[b] as read
+  int slot, L, lo, t_first, n_tiles;
+  bool clamped;   // L was cut to the table's capacity (position error)
 };
+
+// The row cache keeps {slot or -1, L}; bit 31 of L marks a clamped length.
+constexpr int kClampBit = static_cast<int>(0x80000000u);
 
 // Row b's slot, clamped length and key-tile range, read from global memory;
 // errors are reported by the caller-selected thread.
@@ -197,8 +223,9 @@ __device__ __forceinline__ RowInfo row_info(const Problem &p, int b, int32_t *er
                                             bool report) {
   RowInfo r;
   r.slot = p.batch_idx ? p.batch_idx[b] : b;
-  r.raw = p.seq_lens[b];
-  r.L = r.raw < 0x7fffffff ? r.raw + p.len_bias : r.raw;
+  const int raw = p.seq_lens[b];
+  r.L = raw < 0x7fffffff ? raw + p.len_bias : raw;
+  r.clamped = false;
   bool empty = false;
   if (r.slot < 0 || r.slot >= p.n_slots) {
     if (report && err) atomicOr(err, PKV_ERR_SLOT);
@@ -207,6 +234,7 @@ __device__ __forceinline__ RowInfo row_info(const Problem &p, int b, int32_t *er
   const int Lmax = p.max_pages << p.log2_ps;
   if (r.L > Lmax || r.L < 0) {
     if (report && err) atomicOr(err, PKV_ERR_POS);
+    r.clamped = r.L > Lmax;
     r.L = r.L < 0 ? 0 : Lmax;
   }
   if (r.slot == 0 || r.L <= 0) empty = true;
@@ -220,7 +248,7 @@ __device__ __forceinline__ RowInfo row_info(const Problem &p, int b, int32_t *er
 __device__ __forceinline__ RowInfo row_cached(const Problem &p, int2 c) {
   RowInfo r;
   r.slot = c.x;
-  r.L = c.y;
+  r.L = c.y & ~kClampBit;
   r.lo = p.window > 0 ? max(0, r.L - p.window) : 0;
   r.t_first = r.lo / kT;
   r.n_tiles = (r.slot <= 0 || r.L <= 0) ? 0 : (r.L + kT - 1) / kT - r.t_first;
@@ -305,23 +333,52 @@ __device__ __forceinline__ int find_row(const int *pre, int B, int scale, int x)
   return lo;
 }
 
-// A run of key tiles of one (row, kv head) processed by one CTA.
+// A run of key tiles of one (row, kv head) processed by one CTA. The
+// producer computes each unit once and hands it to the consumers in shared
+// memory with the unit's query rows (b < 0: no more units).
 struct Unit {
   int b, g, slot, ta, tb, k0, k1, part, parts;
+  // fused step, unit holding the row's last tile: cache row of the appended
+  // token (kv_append's address), -1 if its page entry is invalid, -2 if its
+  // position is past the table (both errors are reported by the attention's
+  // own checks of the same row); -1 for every other unit
+  int app;
 };
+static_assert(sizeof(Unit) <= 48, "unit descriptor slot");
 
 // Walks this CTA's units. Balanced mode: the (row, kv head, tile) sequence
-// is flattened and every CTA owns the same number of consecutive tiles
-// (q = ceil(total / CTAs)); a (row, head) that straddles CTAs is finished
-// by the combine kernel. Fixed mode: units are (row, part, head) with each
-// row cut into at most S equal parts, dealt out in equal counts.
+// is flattened and laid on a cost line where each tile costs kTileCost and
+// each (row, head) kUnitCost more before its first tile; every CTA owns the
+// tiles whose cost position falls in its equal share [c*qc, (c+1)*qc), a
+// contiguous run of the flattened sequence. A (row, head) that straddles
+// CTAs is finished by the combine kernel. Fixed mode: units are (row, part,
+// head) with each row cut into at most S equal parts, dealt out in equal
+// counts.
 struct UnitIter {
   int pos, end;   // balanced: flattened tile index; fixed: unit index
-  int q;          // balanced: tiles per CTA
+  int qc;         // balanced: cost per CTA
 };
 
+// Cost position of the first tile of (row b, head g): prc is the prefix of
+// per-row head costs (kTileCost * tiles + kUnitCost for rows with tiles).
+__device__ __forceinline__ int head_cost_start(const Problem &p, const int *prc, int b, int g) {
+  return p.Hkv * prc[b] + g * (prc[b + 1] - prc[b]) + kUnitCost;
+}
+
+// Flattened index of the first tile whose cost position is >= x.
+__device__ __forceinline__ int first_tile_at(const Problem &p, const int *pre, const int *prc,
+                                             int x) {
+  if (x >= p.Hkv * prc[p.B]) return p.Hkv * pre[p.B];
+  const int b = find_row(prc, p.B, p.Hkv, x);
+  const int W = prc[b + 1] - prc[b], T = pre[b + 1] - pre[b];
+  const int within = x - p.Hkv * prc[b];
+  const int g = within / W, r = within - g * W;
+  const int j = r <= kUnitCost ? 0 : (r - kUnitCost + kTileCost - 1) / kTileCost;
+  return p.Hkv * pre[b] + g * T + j;
+}
+
 __device__ __forceinline__ bool next_unit(const Problem &p, const int2 *rows, const int *pre,
-                                          UnitIter &it, Unit &w) {
+                                          const int *prc, UnitIter &it, Unit &w) {
   if (it.pos >= it.end) return false;
   if (p.fixed_splits == 0) {
     const int b = find_row(pre, p.B, p.Hkv, it.pos);
@@ -331,14 +388,14 @@ __device__ __forceinline__ bool next_unit(const Problem &p, const int2 *rows, co
     w.g = within / tiles;
     const int t0 = within - w.g * tiles;
     const int n = min(tiles - t0, it.end - it.pos);
-    const int s_rh = p.Hkv * pre[b] + w.g * tiles;
-    const int first_cta = s_rh / it.q, last_cta = (s_rh + tiles - 1) / it.q;
+    const int c0 = head_cost_start(p, prc, b, w.g);
+    const int first_cta = c0 / it.qc;
     w.b = b;
     w.slot = r.slot;
     w.ta = r.t_first + t0;
     w.tb = w.ta + n;
-    w.parts = last_cta - first_cta + 1;
-    w.part = it.pos / it.q - first_cta;
+    w.parts = (c0 + kTileCost * (tiles - 1)) / it.qc - first_cta + 1;
+    w.part = (c0 + kTileCost * t0) / it.qc - first_cta;
     w.k0 = max(r.lo, w.ta * kT);
     w.k1 = min(r.L, w.tb * kT);
     it.pos += n;
@@ -391,7 +448,8 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
   volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + Cf::OFF_MISC);
   int2 *rows = reinterpret_cast<int2 *>(sm + Cf::OFF_ROWS);
   int *pre = reinterpret_cast<int *>(sm + Cf::OFF_PRE);
-  int *app = reinterpret_cast<int *>(sm + Cf::OFF_APP);
+  int *prc = reinterpret_cast<int *>(sm + Cf::OFF_PRC);
+  Unit *udesc = reinterpret_cast<Unit *>(sm + Cf::OFF_DESC);
 
   // ---- set-up: barriers, row cache, per-row tile or part prefix sums ----
   if (tid == 0) {
@@ -427,25 +485,26 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
   pkv_allow_next_grid();
   for (int b = tid; b < p.B; b += kThreads) {
     const RowInfo r = row_info(p, b, err, blockIdx.x == 0);
-    rows[b] = make_int2(r.n_tiles > 0 ? r.slot : -1, r.L);
+    rows[b] = make_int2(r.n_tiles > 0 ? r.slot : -1, r.L | (r.clamped ? kClampBit : 0));
     pre[b + 1] = p.fixed_splits > 0 ? fixed_parts(r.n_tiles, p.fixed_splits) : r.n_tiles;
-    if constexpr (STEP) app[b] = r.raw;
+    prc[b + 1] = r.n_tiles > 0 ? kTileCost * r.n_tiles + kUnitCost : 0;
   }
   __syncthreads();
-  if (warp == 0) {  // inclusive scan of pre[1..B] in chunks of 32
+  if (warp < 2) {  // inclusive scans of pre[1..B] (warp 0) and prc[1..B] (warp 1)
+    int *arr = warp == 0 ? pre : prc;
     int carry = 0;
     for (int base = 0; base < p.B; base += 32) {
       const int i = base + lane;
-      int v = i < p.B ? pre[i + 1] : 0;
+      int v = i < p.B ? arr[i + 1] : 0;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int t = __shfl_up_sync(0xffffffffu, v, o);
         if (lane >= o) v += t;
       }
-      if (i < p.B) pre[i + 1] = v + carry;
+      if (i < p.B) arr[i + 1] = v + carry;
       carry += __shfl_sync(0xffffffffu, v, 31);
     }
-    if (lane == 0) pre[0] = 0;
+    if (lane == 0) arr[0] = 0;
   }
   __syncthreads();
   UnitIter it0;
@@ -453,11 +512,15 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
     const int total = p.Hkv * pre[p.B];
     if (p.fixed_splits == 0) {
       const int grid = static_cast<int>(gridDim.x);
-      it0.q = total > 0 ? (total + grid - 1) / grid : 1;
-      it0.pos = static_cast<int>(min(static_cast<long long>(total), 1LL * it0.q * blockIdx.x));
-      it0.end = min(total, it0.pos + it0.q);
+      const int cost = p.Hkv * prc[p.B];
+      // at least one tile per share, so that every CTA between the first and
+      // the last owner of a (row, head) owns one of its tiles
+      it0.qc = max(kTileCost, (cost + grid - 1) / grid);
+      const long long c0 = 1LL * it0.qc * blockIdx.x, c1 = c0 + it0.qc;
+      it0.pos = first_tile_at(p, pre, prc, static_cast<int>(c0 < cost ? c0 : cost));
+      it0.end = first_tile_at(p, pre, prc, static_cast<int>(c1 < cost ? c1 : cost));
     } else {
-      it0.q = 1;
+      it0.qc = 1;
       it0.pos = static_cast<int>(1LL * total * blockIdx.x / gridDim.x);
       it0.end = static_cast<int>(1LL * total * (blockIdx.x + 1) / gridDim.x);
     }
@@ -467,8 +530,8 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
         const int n = pre[b + 1] - pre[b];
         int parts = n;
         if (p.fixed_splits == 0 && n > 0) {
-          const int s_rh = p.Hkv * pre[b] + g * n;
-          parts = (s_rh + n - 1) / it0.q - s_rh / it0.q + 1;
+          const int c0 = head_cost_start(p, prc, b, g);
+          parts = (c0 + kTileCost * (n - 1)) / it0.qc - c0 / it0.qc + 1;
         }
         parts_out[rh] = parts;
       }
@@ -476,26 +539,13 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
   }
 
   if constexpr (STEP) {
-    // consumers: the norm gains, and per row with keys the cache row its new
-    // token goes to (kv_append's checks; CTA 0 reports the error bits). The
-    // table loads overlap the wait for the first tiles.
-    if (warp < kCWarps) {
-      if (sa.gamma_q) {
-        __nv_bfloat16 *gs = reinterpret_cast<__nv_bfloat16 *>(sm + Cf::OFF_GAM);
-        for (int i = tid; i < D; i += kCThreads) {
-          gs[i] = sa.gamma_q[i];
-          gs[D + i] = sa.gamma_k[i];
-        }
+    // consumers: the norm gains (read after the first unit's barrier)
+    if (warp < kCWarps && sa.gamma_q) {
+      __nv_bfloat16 *gs = reinterpret_cast<__nv_bfloat16 *>(sm + Cf::OFF_GAM);
+      for (int i = tid; i < D; i += kCThreads) {
+        gs[i] = sa.gamma_q[i];
+        gs[D + i] = sa.gamma_k[i];
       }
-      for (int b = tid; b < p.B; b += kCThreads) {
-        const int2 c = rows[b];
-        if (c.x <= 0) continue;   // no keys: appended by the zero-row pass below
-        int bits;
-        const long long row = append_row(p, c.x, app[b], bits);
-        if (bits && blockIdx.x == 0 && err) atomicOr(err, bits);
-        app[b] = row >= 0 ? static_cast<int>(row) : (bits == PKV_ERR_POS ? -2 : -1);
-      }
-      consumer_sync();
     }
   }
 
@@ -563,7 +613,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
     Unit w, wn;
     int it_k = 0, it_v = 0, it_q = 0;
     bool ok = true;
-    bool have = next_unit(p, rows, pre, it, w);
+    bool have = next_unit(p, rows, pre, prc, it, w);
     int page_first = have ? box_page(w, lane) : -1;
     while (ok && have) {
       bool have_next = false, looked_ahead = false;
@@ -574,12 +624,27 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
         const int qs = it_q & 1;
         // fused step: the unit that holds the row's last tile also gets the
         // raw k and v rows of the token it appends
-        const bool kv_rows = STEP && w.k1 == rows[w.b].y;
+        const int c_b = rows[w.b].y;
+        const bool kv_rows = STEP && w.k1 == (c_b & ~kClampBit);
         if (lane == 0) {
           ok = mbar_wait(emptyQ + 8 * qs, ((it_q >> 1) & 1) ^ 1, abort_flag);
-          if (ok)
+          if (ok) {
+            w.app = -1;
+            if (kv_rows) {
+              if (c_b < 0) {
+                w.app = -2;
+              } else {
+                const int pos = (c_b & ~kClampBit) - 1;
+                const int page = __ldg(p.table + static_cast<size_t>(w.slot) * p.max_pages +
+                                       (pos >> p.log2_ps));
+                if (page >= 0 && page < p.n_pages)
+                  w.app = (page << p.log2_ps) + (pos & (ps - 1));
+              }
+            }
+            udesc[qs] = w;   // published to the consumers by the arrive below
             mbar_expect_tx(fullQ + 8 * qs,
                            static_cast<uint32_t>((p.G + (kv_rows ? 2 : 0)) * D * 2));
+          }
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
@@ -648,13 +713,13 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
           ok = __shfl_sync(0xffffffffu, ok, 0);
           if (!looked_ahead) {  // next unit's table lookups, once this one is moving
             looked_ahead = true;
-            have_next = next_unit(p, rows, pre, it, wn);
+            have_next = next_unit(p, rows, pre, prc, it, wn);
             page_next = have_next ? box_page(wn, lane) : -1;
           }
         }
       }
       if (!looked_ahead) {
-        have_next = next_unit(p, rows, pre, it, wn);
+        have_next = next_unit(p, rows, pre, prc, it, wn);
         page_next = have_next ? box_page(wn, lane) : -1;
       }
       w = wn;
@@ -662,6 +727,15 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
       have = have_next;
     }
     if (lane != 0) return;
+    if (ok) {   // end-of-work descriptor in the next Q stage
+      const int qs = it_q & 1;
+      ok = mbar_wait(emptyQ + 8 * qs, ((it_q >> 1) & 1) ^ 1, abort_flag);
+      if (ok) {
+        udesc[qs].b = -1;
+        mbar_arrive(fullQ + 8 * qs);
+        ++it_q;
+      }
+    }
     if (!ok) {
       *abort_flag = 1;
       if (err) atomicOr(err, PKV_ERR_TIMEOUT);
@@ -695,19 +769,26 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
   constexpr int MT = D / 64;  // 16-row m-tiles of this warp's D/4 slice
   int it = 0, it_q = 0;
   bool failed = false;
-  UnitIter units = it0;
-  Unit w;
 
-  while (next_unit(p, rows, pre, units, w)) {
+  while (true) {
     uint32_t qb[KS][2];
     const int qs = it_q & 1;
     const uint8_t *qstage = sm + Cf::OFF_Q + qs * Cf::Q_STAGE;
     int patch = -1;   // fused step: row of the appended token in the unit's last tile
-    {
-      if (!mbar_wait(fullQ + 8 * qs, (it_q >> 1) & 1, abort_flag)) {
+    // the unit comes from the producer with its query rows; all consumer
+    // threads leave the loop together (end of work, or a wait that gave up)
+    const bool q_ok = mbar_wait(fullQ + 8 * qs, (it_q >> 1) & 1, abort_flag);
+    Unit w;
+    w.b = -1;
+    if (q_ok) w = udesc[qs];
+    if (consumer_sync_or(!q_ok || w.b < 0)) {
+      if (!q_ok) {
         failed = true;
         *abort_flag = 1;
       }
+      break;
+    }
+    {
       if constexpr (STEP) {
         // Rotate the raw query rows in place with the row's rotation factors
         // (computed once, one pair per thread). The unit that holds the row's
@@ -715,9 +796,10 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
         // cache row (the kv_append of the chain) and later patches both into
         // that tile, whose TMA copy may predate the write.
         constexpr int PAIRS = (D / 2 + 31) / 32;
-        const int L_b = rows[w.b].y;
-        const int app_b = app[w.b];
-        const int pos_b = app_b == -2 ? __ldg(p.seq_lens + w.b) : L_b - 1;
+        const int c_b = rows[w.b].y;
+        const int L_b = c_b & ~kClampBit;
+        const int app_b = w.app;
+        const int pos_b = c_b < 0 ? __ldg(p.seq_lens + w.b) : L_b - 1;
         const float fpos = static_cast<float>(pos_b);
         float *fac = reinterpret_cast<float *>(sm + Cf::OFF_FAC);
         for (int i = tid; i < D / 2; i += kCThreads) {
@@ -1190,7 +1272,7 @@ int decode_common(const char *fn, const pkv_bf16 *q, const pkv_bf16 *k_cache,
     return pkv::fail(PKV_E_BAD_ARG, "%s: tensors must be 16-byte aligned", fn);
   {
     const long long row_tiles = (1LL * max_pages_per_seq * page_size + kT - 1) / kT + 1;
-    if (1LL * B * Hkv * row_tiles >= (1LL << 31))
+    if (1LL * B * Hkv * (kTileCost * row_tiles + kUnitCost) >= (1LL << 31))
       return pkv::fail(PKV_E_BAD_ARG, "%s: B * Hkv * tiles per row too large", fn);
   }
   const int max_parts = max_parts_for(max_pages_per_seq, page_size, window, num_splits);
