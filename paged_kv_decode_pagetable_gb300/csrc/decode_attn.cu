@@ -1065,13 +1065,16 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
 
 // Merge the parts of one (row, head) with weights 2^(lse_c - max), skipping
 // parts without keys (lse = -inf). (Row, head) pairs handled by one CTA were
-// written by the attention kernel itself. One warp per (row, head); the part
-// count and the log-sum-exps are loaded together, then each lane merges four
-// consecutive output columns.
+// written by the attention kernel itself. One warp per (row, head); lane l
+// merges output columns 4l + 128c. The part count, the log-sum-exps and the
+// first two partials are loaded together, so the common two-part merge needs
+// one round trip to L2 after the attention kernel completes.
+template <int D>
 __global__ void combine_kernel(const float *__restrict__ o_part,
                                const float *__restrict__ lse_part,
-                               const int *__restrict__ parts_in, const Problem p, int D,
+                               const int *__restrict__ parts_in, const Problem p,
                                __nv_bfloat16 *__restrict__ out) {
+  constexpr int CH = (D + 127) / 128;   // float4 column chunks per lane
   pkv_wait_prior_grid();
   pkv_allow_next_grid();
   const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -1079,24 +1082,37 @@ __global__ void combine_kernel(const float *__restrict__ o_part,
   if (r >= p.B * p.Hq) return;
   const int b = r / p.Hq, g = (r - b * p.Hq) / p.G;
   const float *lse = lse_part + static_cast<size_t>(r) * p.max_parts;
+  const float *op = o_part + static_cast<size_t>(r) * p.max_parts * D;
   const int parts = __ldcg(parts_in + b * p.Hkv + g);
   float my_lse = lane < p.max_parts ? __ldcg(lse + lane) : -INFINITY;
+  float4 v0[CH], v1[CH];   // parts 0 and 1 (max_parts >= 2 whenever this kernel runs)
+#pragma unroll
+  for (int c = 0; c < CH; ++c) {
+    const int d = 4 * lane + 128 * c;
+    if (d < D) {
+      v0[c] = __ldcg(reinterpret_cast<const float4 *>(op + d));
+      v1[c] = __ldcg(reinterpret_cast<const float4 *>(op + D + d));
+    }
+  }
   if (parts <= 1) return;
   if (lane >= parts) my_lse = -INFINITY;
   float m = my_lse;
   for (int s = 32 + lane; s < parts; s += 32) m = fmaxf(m, __ldcg(lse + s));
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-  const float *op = o_part + static_cast<size_t>(r) * p.max_parts * D;
   __nv_bfloat16 *orow = out + static_cast<size_t>(r) * D;
-  for (int d = 4 * lane; d < D; d += 128) {
+#pragma unroll
+  for (int c = 0; c < CH; ++c) {
+    const int d = 4 * lane + 128 * c;
+    if (d >= D) continue;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     float wsum = 0.f;
     if (m != -INFINITY) {
-#pragma unroll 4
       for (int s = 0; s < parts; ++s) {
         const float l = s < 32 ? __shfl_sync(0xffffffffu, my_lse, s) : __ldcg(lse + s);
-        const float4 v = __ldcg(reinterpret_cast<const float4 *>(op + static_cast<size_t>(s) * D + d));
+        const float4 v = s == 0   ? v0[c]
+                         : s == 1 ? v1[c]
+                                  : __ldcg(reinterpret_cast<const float4 *>(op + static_cast<size_t>(s) * D + d));
         const float wgt = l == -INFINITY ? 0.f : exp2f(l - m);
         wsum += wgt;
         acc.x = fmaf(wgt, v.x, acc.x);
@@ -1335,11 +1351,14 @@ int decode_common(const char *fn, const pkv_bf16 *q, const pkv_bf16 *k_cache,
   if (max_parts > 1) {
     const int rows_bh = B * Hq;
     const int wpb = 4;
-    PKV_CUDA_CHECK(pkv::launch_pdl(combine_kernel, dim3((rows_bh + wpb - 1) / wpb),
-                                   dim3(wpb * 32), 0, s,
+    auto *kern = D == 64    ? combine_kernel<64>
+                 : D == 128 ? combine_kernel<128>
+                 : D == 256 ? combine_kernel<256>
+                            : combine_kernel<512>;
+    PKV_CUDA_CHECK(pkv::launch_pdl(kern, dim3((rows_bh + wpb - 1) / wpb), dim3(wpb * 32), 0, s,
                                    static_cast<const float *>(o_part),
                                    static_cast<const float *>(lse_part),
-                                   static_cast<const int *>(parts), p, D,
+                                   static_cast<const int *>(parts), p,
                                    reinterpret_cast<__nv_bfloat16 *>(out)));
   }
   return pkv::ok();
