@@ -322,15 +322,26 @@ __device__ __forceinline__ void step_append_head(const Problem &p, const StepArg
     reinterpret_cast<uint4 *>(sa.v_cache + dst)[c] = __ldg(vs + c);
 }
 
-// largest b in [0, B) with scale * pre[b] <= x (pre non-decreasing, pre[0] = 0);
-// the host guarantees Hkv * (tiles of all rows) < 2^31
-__device__ __forceinline__ int find_row(const int *pre, int B, int scale, int x) {
-  int lo = 0, hi = B;
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (scale * pre[mid] <= x) lo = mid; else hi = mid;
+// Largest b in [0, B) with scale * arr[b] <= x, for a non-decreasing arr
+// with arr[0] = 0 <= x, found by the whole (converged) warp: each lane tests
+// one row of every 32 and the ballots are counted. The host guarantees
+// Hkv * (tiles of all rows) and the matching costs stay below 2^31.
+__device__ __forceinline__ int find_row_warp(const int *arr, int B, int scale, int x, int lane) {
+  int count = 0;
+  for (int base = 0; base < B; base += 32) {
+    const int b = base + lane;
+    const unsigned le = __ballot_sync(0xffffffffu, b < B && scale * arr[b] <= x);
+    count += __popc(le);
+    if (le != 0xffffffffu) break;   // monotone: no later row qualifies
   }
-  return lo;
+  return count - 1;
+}
+
+// floor(x / d) for 0 <= x < n * d with a small n (a kv-head index), by ballot
+// when n <= 32; the warp must be converged and the arguments uniform.
+__device__ __forceinline__ int small_quotient_warp(int x, int d, int n, int lane) {
+  if (n > 32) return x / d;
+  return __popc(__ballot_sync(0xffffffffu, lane < n && lane * d <= x)) - 1;
 }
 
 // A run of key tiles of one (row, kv head) processed by one CTA. The
@@ -365,27 +376,28 @@ __device__ __forceinline__ int head_cost_start(const Problem &p, const int *prc,
   return p.Hkv * prc[b] + g * (prc[b + 1] - prc[b]) + kUnitCost;
 }
 
-// Flattened index of the first tile whose cost position is >= x.
+// Flattened index of the first tile whose cost position is >= x (warp-wide).
 __device__ __forceinline__ int first_tile_at(const Problem &p, const int *pre, const int *prc,
-                                             int x) {
+                                             int x, int lane) {
   if (x >= p.Hkv * prc[p.B]) return p.Hkv * pre[p.B];
-  const int b = find_row(prc, p.B, p.Hkv, x);
+  const int b = find_row_warp(prc, p.B, p.Hkv, x, lane);
   const int W = prc[b + 1] - prc[b], T = pre[b + 1] - pre[b];
   const int within = x - p.Hkv * prc[b];
-  const int g = within / W, r = within - g * W;
+  const int g = small_quotient_warp(within, W, p.Hkv, lane), r = within - g * W;
   const int j = r <= kUnitCost ? 0 : (r - kUnitCost + kTileCost - 1) / kTileCost;
   return p.Hkv * pre[b] + g * T + j;
 }
 
+// Called by the converged producer warp with uniform arguments.
 __device__ __forceinline__ bool next_unit(const Problem &p, const int2 *rows, const int *pre,
-                                          const int *prc, UnitIter &it, Unit &w) {
+                                          const int *prc, UnitIter &it, Unit &w, int lane) {
   if (it.pos >= it.end) return false;
   if (p.fixed_splits == 0) {
-    const int b = find_row(pre, p.B, p.Hkv, it.pos);
+    const int b = find_row_warp(pre, p.B, p.Hkv, it.pos, lane);
     const RowInfo r = row_cached(p, rows[b]);
     const int tiles = pre[b + 1] - pre[b];
     const int within = it.pos - p.Hkv * pre[b];
-    w.g = within / tiles;
+    w.g = small_quotient_warp(within, tiles, p.Hkv, lane);
     const int t0 = within - w.g * tiles;
     const int n = min(tiles - t0, it.end - it.pos);
     const int c0 = head_cost_start(p, prc, b, w.g);
@@ -402,7 +414,7 @@ __device__ __forceinline__ bool next_unit(const Problem &p, const int2 *rows, co
   } else {
     const int rc = it.pos / p.Hkv;
     w.g = it.pos - rc * p.Hkv;
-    const int b = find_row(pre, p.B, 1, rc);
+    const int b = find_row_warp(pre, p.B, 1, rc, lane);
     const RowInfo r = row_cached(p, rows[b]);
     const int ch = (r.n_tiles + p.fixed_splits - 1) / p.fixed_splits;
     w.b = b;
@@ -493,6 +505,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
   if (warp < 2) {  // inclusive scans of pre[1..B] (warp 0) and prc[1..B] (warp 1)
     int *arr = warp == 0 ? pre : prc;
     int carry = 0;
+#pragma unroll 1
     for (int base = 0; base < p.B; base += 32) {
       const int i = base + lane;
       int v = i < p.B ? arr[i + 1] : 0;
@@ -505,6 +518,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
       carry += __shfl_sync(0xffffffffu, v, 31);
     }
     if (lane == 0) arr[0] = 0;
+    __syncwarp();
   }
   __syncthreads();
   UnitIter it0;
@@ -516,9 +530,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
       // at least one tile per share, so that every CTA between the first and
       // the last owner of a (row, head) owns one of its tiles
       it0.qc = max(kTileCost, (cost + grid - 1) / grid);
-      const long long c0 = 1LL * it0.qc * blockIdx.x, c1 = c0 + it0.qc;
-      it0.pos = first_tile_at(p, pre, prc, static_cast<int>(c0 < cost ? c0 : cost));
-      it0.end = first_tile_at(p, pre, prc, static_cast<int>(c1 < cost ? c1 : cost));
+      it0.pos = it0.end = 0;   // the producer warp finds its range (first_tile_at)
     } else {
       it0.qc = 1;
       it0.pos = static_cast<int>(1LL * total * blockIdx.x / gridDim.x);
@@ -613,7 +625,13 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
     Unit w, wn;
     int it_k = 0, it_v = 0, it_q = 0;
     bool ok = true;
-    bool have = next_unit(p, rows, pre, prc, it, w);
+    if (p.fixed_splits == 0) {
+      const int cost = p.Hkv * prc[p.B];
+      const long long c0 = 1LL * it.qc * blockIdx.x, c1 = c0 + it.qc;
+      it.pos = first_tile_at(p, pre, prc, static_cast<int>(c0 < cost ? c0 : cost), lane);
+      it.end = first_tile_at(p, pre, prc, static_cast<int>(c1 < cost ? c1 : cost), lane);
+    }
+    bool have = next_unit(p, rows, pre, prc, it, w, lane);
     int page_first = have ? box_page(w, lane) : -1;
     while (ok && have) {
       bool have_next = false, looked_ahead = false;
@@ -713,13 +731,13 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
           ok = __shfl_sync(0xffffffffu, ok, 0);
           if (!looked_ahead) {  // next unit's table lookups, once this one is moving
             looked_ahead = true;
-            have_next = next_unit(p, rows, pre, prc, it, wn);
+            have_next = next_unit(p, rows, pre, prc, it, wn, lane);
             page_next = have_next ? box_page(wn, lane) : -1;
           }
         }
       }
       if (!looked_ahead) {
-        have_next = next_unit(p, rows, pre, prc, it, wn);
+        have_next = next_unit(p, rows, pre, prc, it, wn, lane);
         page_next = have_next ? box_page(wn, lane) : -1;
       }
       w = wn;
