@@ -53,9 +53,11 @@ constexpr int kMaxRows = 512;        // rows per call (row cache kept in smem)
 constexpr int kSpinLimit = 1 << 22;
 // Balanced split cost model, in quarter tiles: a key tile costs kTileCost and
 // starting a (row, kv head) costs kUnitCost more (its query load, table
-// lookups and epilogue measured at about three quarters of a tile's time).
+// lookups, epilogue and the tail of its partly used last tile). The value
+// is the best of a sweep over 1..16 on the rollout, Llama and Gemma layers
+// (6: rollout attention 29.24 -> 28.98 us against 3).
 constexpr int kTileCost = 4;
-constexpr int kUnitCost = 3;
+constexpr int kUnitCost = 6;
 
 template <int D>
 struct Cfg {
