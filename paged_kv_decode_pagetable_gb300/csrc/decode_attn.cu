@@ -368,8 +368,9 @@ static_assert(sizeof(Unit) <= 48, "unit descriptor slot");
 // head) with each row cut into at most S equal parts, dealt out in equal
 // counts.
 struct UnitIter {
-  int pos, end;   // balanced: flattened tile index; fixed: unit index
-  int qc;         // balanced: cost per CTA
+  int pos, end;     // balanced: flattened tile index; fixed: unit index
+  int qc;           // balanced: cost per CTA
+  int hb, hg, ht;   // balanced: (row, head, tile) of pos when already known; hb < 0 if not
 };
 
 // Cost position of the first tile of (row b, head g): prc is the prefix of
@@ -378,16 +379,42 @@ __device__ __forceinline__ int head_cost_start(const Problem &p, const int *prc,
   return p.Hkv * prc[b] + g * (prc[b + 1] - prc[b]) + kUnitCost;
 }
 
-// Flattened index of the first tile whose cost position is >= x (warp-wide).
-__device__ __forceinline__ int first_tile_at(const Problem &p, const int *pre, const int *prc,
-                                             int x, int lane) {
-  if (x >= p.Hkv * prc[p.B]) return p.Hkv * pre[p.B];
-  const int b = find_row_warp(prc, p.B, p.Hkv, x, lane);
-  const int W = prc[b + 1] - prc[b], T = pre[b + 1] - pre[b];
-  const int within = x - p.Hkv * prc[b];
-  const int g = small_quotient_warp(within, W, p.Hkv, lane), r = within - g * W;
-  const int j = r <= kUnitCost ? 0 : (r - kUnitCost + kTileCost - 1) / kTileCost;
-  return p.Hkv * pre[b] + g * T + j;
+// The CTA's range: flattened indices of the first tiles whose cost positions
+// are >= x0 and >= x1 (x0 <= x1), found in one warp-wide pass over the rows;
+// the (row, head, tile) of the first bound is kept for the first unit.
+__device__ __forceinline__ void locate_range(const Problem &p, const int *pre, const int *prc,
+                                             int x0, int x1, int lane, UnitIter &it) {
+  int n0 = 0, n1 = 0;   // rows whose cost start is <= x0, <= x1
+  for (int base = 0; base < p.B; base += 32) {
+    const int b = base + lane;
+    const int v = b < p.B ? p.Hkv * prc[b] : 0x7fffffff;
+    const unsigned m0 = __ballot_sync(0xffffffffu, v <= x0);
+    const unsigned m1 = __ballot_sync(0xffffffffu, v <= x1);
+    n0 += __popc(m0);
+    n1 += __popc(m1);
+    if (m1 != 0xffffffffu) break;   // monotone, and m0 is a subset of m1
+  }
+  const int total_cost = p.Hkv * prc[p.B];
+  it.hb = -1;
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const int x = k ? x1 : x0;
+    int flat = p.Hkv * pre[p.B];
+    if (x < total_cost) {
+      const int b = (k ? n1 : n0) - 1;
+      const int W = prc[b + 1] - prc[b], T = pre[b + 1] - pre[b];
+      const int within = x - p.Hkv * prc[b];
+      const int g = small_quotient_warp(within, W, p.Hkv, lane), r = within - g * W;
+      const int j = r <= kUnitCost ? 0 : (r - kUnitCost + kTileCost - 1) / kTileCost;
+      flat = p.Hkv * pre[b] + g * T + j;
+      if (k == 0 && j < T) {
+        it.hb = b;
+        it.hg = g;
+        it.ht = j;
+      }
+    }
+    if (k) it.end = flat; else it.pos = flat;
+  }
 }
 
 // Called by the converged producer warp with uniform arguments.
@@ -395,12 +422,21 @@ __device__ __forceinline__ bool next_unit(const Problem &p, const int2 *rows, co
                                           const int *prc, UnitIter &it, Unit &w, int lane) {
   if (it.pos >= it.end) return false;
   if (p.fixed_splits == 0) {
-    const int b = find_row_warp(pre, p.B, p.Hkv, it.pos, lane);
+    int b, t0;
+    if (it.hb >= 0) {   // located with the CTA's range
+      b = it.hb;
+      w.g = it.hg;
+      t0 = it.ht;
+      it.hb = -1;
+    } else {
+      b = find_row_warp(pre, p.B, p.Hkv, it.pos, lane);
+      const int within = it.pos - p.Hkv * pre[b];
+      const int T = pre[b + 1] - pre[b];
+      w.g = small_quotient_warp(within, T, p.Hkv, lane);
+      t0 = within - w.g * T;
+    }
     const RowInfo r = row_cached(p, rows[b]);
     const int tiles = pre[b + 1] - pre[b];
-    const int within = it.pos - p.Hkv * pre[b];
-    w.g = small_quotient_warp(within, tiles, p.Hkv, lane);
-    const int t0 = within - w.g * tiles;
     const int n = min(tiles - t0, it.end - it.pos);
     const int c0 = head_cost_start(p, prc, b, w.g);
     const int first_cta = c0 / it.qc;
@@ -409,7 +445,7 @@ __device__ __forceinline__ bool next_unit(const Problem &p, const int2 *rows, co
     w.ta = r.t_first + t0;
     w.tb = w.ta + n;
     w.parts = (c0 + kTileCost * (tiles - 1)) / it.qc - first_cta + 1;
-    w.part = (c0 + kTileCost * t0) / it.qc - first_cta;
+    w.part = static_cast<int>(blockIdx.x) - first_cta;   // this CTA owns the unit's tiles
     w.k0 = max(r.lo, w.ta * kT);
     w.k1 = min(r.L, w.tb * kT);
     it.pos += n;
@@ -532,9 +568,11 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
       // at least one tile per share, so that every CTA between the first and
       // the last owner of a (row, head) owns one of its tiles
       it0.qc = max(kTileCost, (cost + grid - 1) / grid);
-      it0.pos = it0.end = 0;   // the producer warp finds its range (first_tile_at)
+      it0.pos = it0.end = 0;   // the producer warp finds its range (locate_range)
+      it0.hb = -1;
     } else {
       it0.qc = 1;
+      it0.hb = -1;
       it0.pos = static_cast<int>(1LL * total * blockIdx.x / gridDim.x);
       it0.end = static_cast<int>(1LL * total * (blockIdx.x + 1) / gridDim.x);
     }
@@ -630,8 +668,8 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
     if (p.fixed_splits == 0) {
       const int cost = p.Hkv * prc[p.B];
       const long long c0 = 1LL * it.qc * blockIdx.x, c1 = c0 + it.qc;
-      it.pos = first_tile_at(p, pre, prc, static_cast<int>(c0 < cost ? c0 : cost), lane);
-      it.end = first_tile_at(p, pre, prc, static_cast<int>(c1 < cost ? c1 : cost), lane);
+      locate_range(p, pre, prc, static_cast<int>(c0 < cost ? c0 : cost),
+                   static_cast<int>(c1 < cost ? c1 : cost), lane, it);
     }
     bool have = next_unit(p, rows, pre, prc, it, w, lane);
     int page_first = have ? box_page(w, lane) : -1;
