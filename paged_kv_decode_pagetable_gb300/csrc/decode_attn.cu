@@ -138,6 +138,14 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *tm,
       "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(bar)
       : "memory");
 }
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *tm,
+                                            int x, int y, int z, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
+}
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes,
                                           uint32_t bar) {
   asm volatile(
@@ -473,6 +481,8 @@ template <int D, bool STEP>
 __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
     decode_attn_kernel(const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV,
+                       const __grid_constant__ CUtensorMap tmK3,
+                       const __grid_constant__ CUtensorMap tmV3,
                        const __nv_bfloat16 *__restrict__ q, const Problem p,
                        float scale_log2, float *__restrict__ o_part,
                        float *__restrict__ lse_part, int *__restrict__ parts_out,
@@ -742,6 +752,19 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
           if (lane == 0) {
             const uint32_t bytes =
                 static_cast<uint32_t>(__popc(mask)) * Cf::CHUNKS * box_rows * 128;
+            // One box per tile (pages of >= 64 keys): a tile whose keys end
+            // (or start) inside it is loaded as the 64 rows ending at its
+            // last key (starting at its first key); rows outside the page are
+            // zero-filled by the copy and never read from memory. Shared
+            // memory row r then holds key t*64 + r + off.
+            int off = 0;
+            if (boxes == 1 && Cf::NS > 1) {   // (a one-stage ring gains nothing: D=512)
+              const int t = w.ta + base + tt;
+              const int lo_r = max(w.k0 - t * kT, 0), hi_r = min(w.k1 - t * kT, kT);
+              if (hi_r < kT && (lo_r == 0 || hi_r <= kT - lo_r)) off = hi_r - kT;
+              else if (lo_r > 0) off = lo_r;
+            }
+            const uint32_t mword = mask | (static_cast<uint32_t>(off & 0xff) << 8);
             for (int kv = 0; kv < 2 && ok; ++kv) {
               const int itx = kv ? it_v : it_k;
               const int st = itx % Cf::NS;
@@ -750,20 +773,30 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
                 ok = false;
                 break;
               }
-              (kv ? vmask : kmask)[st] = mask;
+              (kv ? vmask : kmask)[st] = mword;
               const uint32_t full = (kv ? fullV : fullK) + 8 * st;
               mbar_expect_tx(full, bytes);
               const uint32_t dst0 = (kv ? sV : sK) + st * Cf::STAGE_BYTES;
               const CUtensorMap *tm = kv ? &tmV : &tmK;
+              if (boxes == 1 && off != 0) {   // 3-D map {column, row in page, page}
+                const CUtensorMap *tm3 = kv ? &tmV3 : &tmK3;
+                if (r0 >= 0) {
 #pragma unroll
-              for (int i = 0; i < kT / 8; ++i) {
-                const int rv = i == 0 ? r0 : i == 1 ? r1 : i == 2 ? r2 : i == 3 ? r3
-                             : i == 4 ? r4 : i == 5 ? r5 : i == 6 ? r6 : r7;
-                if (rv < 0) continue;
+                  for (int cc = 0; cc < Cf::CHUNKS; ++cc)
+                    tma_load_3d(dst0 + cc * Cf::CHUNK_BYTES, tm3, cc * 64,
+                                (r0 & (ps - 1)) + off, r0 >> p.log2_ps, full);
+                }
+              } else {            // 2-D map {column, cache row}
 #pragma unroll
-                for (int cc = 0; cc < Cf::CHUNKS; ++cc)
-                  tma_load_2d(dst0 + cc * Cf::CHUNK_BYTES + i * box_rows * 128, tm, cc * 64,
-                              rv, full);
+                for (int i = 0; i < kT / 8; ++i) {
+                  const int rv = i == 0 ? r0 : i == 1 ? r1 : i == 2 ? r2 : i == 3 ? r3
+                               : i == 4 ? r4 : i == 5 ? r5 : i == 6 ? r6 : r7;
+                  if (rv < 0) continue;
+#pragma unroll
+                  for (int cc = 0; cc < Cf::CHUNKS; ++cc)
+                    tma_load_2d(dst0 + cc * Cf::CHUNK_BYTES + i * box_rows * 128, tm, cc * 64,
+                                rv, full);
+                }
               }
               if (kv) ++it_v; else ++it_k;
             }
@@ -939,12 +972,15 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
         *abort_flag = 1;
       }
       const uint32_t km = kmask[st];
+      const int off = static_cast<int8_t>((km >> 8) & 0xffu);   // smem row r holds key t*kT + r + off
+      const int tlo = max(w.k0, t * kT), thi = min(w.k1, t * kT + kT);
       const uint32_t kbase = sK + st * Cf::STAGE_BYTES;
       const bool patch_here = STEP && patch >= 0 && t == w.tb - 1;
-      if (patch_here && warp == (patch >> 4)) {  // this warp's 16 keys hold the new token
+      const int prow = patch - off;   // shared-memory row of the appended token
+      if (patch_here && warp == (prow >> 4)) {  // this warp's 16 keys hold the new token
         const uint4 *src = reinterpret_cast<const uint4 *>(qstage + Cf::Q_BYTES);
         for (int c = lane; c < D / 8; c += 32)
-          *reinterpret_cast<uint4 *>(sm + st * Cf::STAGE_BYTES + swz(patch, c)) = src[c];
+          *reinterpret_cast<uint4 *>(sm + st * Cf::STAGE_BYTES + swz(prow, c)) = src[c];
         fence_proxy_async();
         __syncwarp();
       }
@@ -962,9 +998,9 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
         }
       }
       const int kr_lo = 16 * warp + gid, kr_hi = kr_lo + 8;
-      const int key_lo = t * kT + kr_lo, key_hi = t * kT + kr_hi;
-      const bool v_lo = key_lo >= w.k0 && key_lo < w.k1 && ((km >> (kr_lo / box_rows)) & 1u);
-      const bool v_hi = key_hi >= w.k0 && key_hi < w.k1 && ((km >> (kr_hi / box_rows)) & 1u);
+      const int key_lo = t * kT + kr_lo + off, key_hi = t * kT + kr_hi + off;
+      const bool v_lo = key_lo >= tlo && key_lo < thi && ((km >> (kr_lo / box_rows)) & 1u);
+      const bool v_hi = key_hi >= tlo && key_hi < thi && ((km >> (kr_hi / box_rows)) & 1u);
       const float s00 = (v_lo && hv0) ? sacc[0] * scale_log2 : -INFINITY;
       const float s01 = (v_lo && hv1) ? sacc[1] * scale_log2 : -INFINITY;
       const float s10 = (v_hi && hv0) ? sacc[2] * scale_log2 : -INFINITY;
@@ -1012,15 +1048,16 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
         failed = true;
         *abort_flag = 1;
       }
-      const uint32_t vm = vmask[st];
+      const uint32_t vm = vmask[st];   // same row offset as the K tile
       const uint32_t vbase = sV + st * Cf::STAGE_BYTES;
-      const bool full_tile = t * kT >= w.k0 && t * kT + kT <= w.k1 && vm == all_boxes;
+      const bool full_tile = off == 0 && t * kT >= w.k0 && t * kT + kT <= w.k1 &&
+                             (vm & 0xffu) == all_boxes;
       if (!full_tile) {
         const uint4 z = make_uint4(0u, 0u, 0u, 0u);
         for (int i = tid; i < kT * (D / 8); i += kCThreads) {
           const int r = i / (D / 8), c = i % (D / 8);
-          const int key = t * kT + r;
-          const bool valid = key >= w.k0 && key < w.k1 && ((vm >> (r / box_rows)) & 1u);
+          const int key = t * kT + r + off;
+          const bool valid = key >= tlo && key < thi && ((vm >> (r / box_rows)) & 1u);
           if (!valid)
             *reinterpret_cast<uint4 *>(sm + Cf::OFF_V + st * Cf::STAGE_BYTES +
                                        (c >> 3) * (kT * 128) + r * 128 + (c & 7) * 16) = z;
@@ -1029,7 +1066,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
       }
       if (patch_here && tid < D / 8) {
         const uint4 *src = reinterpret_cast<const uint4 *>(qstage + Cf::Q_BYTES + D * 2);
-        *reinterpret_cast<uint4 *>(sm + Cf::OFF_V + st * Cf::STAGE_BYTES + swz(patch, tid)) =
+        *reinterpret_cast<uint4 *>(sm + Cf::OFF_V + st * Cf::STAGE_BYTES + swz(prow, tid)) =
             src[tid];
         fence_proxy_async();
       }
@@ -1208,19 +1245,27 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 2-D map over a cache viewed as [rows][D] bf16 with [box_rows][64] boxes.
+// Map over a cache of `rows` rows of D bf16 in pages of page_size rows, with
+// [box_rows][64] boxes: a 2-D map {column, row}, or (paged) a 3-D map
+// {column, row in page, page}, so that a box starting before or ending after
+// its page reads zeros there instead of the neighbouring page (out-of-range
+// elements are filled, not loaded). Full tiles use the 2-D map; the partly
+// used tiles at a row's ends use the 3-D one.
 int make_cache_map(CUtensorMap *tm, const void *base, long long rows, int D,
-                   int box_rows) {
+                   int box_rows, int page_size, bool paged) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return pkv::fail(PKV_E_CUDA, "cuTensorMapEncodeTiled unavailable");
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(D) * 2};
-  cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(box_rows)};
-  cuuint32_t estr[2] = {1u, 1u};
-  CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base),
-                  dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D),
+                        static_cast<cuuint64_t>(paged ? page_size : rows),
+                        static_cast<cuuint64_t>(paged ? rows / page_size : 1)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2,
+                           static_cast<cuuint64_t>(D) * 2 * page_size};
+  cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(box_rows), 1u};
+  cuuint32_t estr[3] = {1u, 1u, 1u};
+  CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, paged ? 3 : 2,
+                  const_cast<void *>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS)
     return pkv::fail(PKV_E_CUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
   return PKV_OK;
@@ -1244,7 +1289,8 @@ int set_smem_attr() {
 }
 
 template <int D, bool STEP>
-int launch_attn(const CUtensorMap &tmK, const CUtensorMap &tmV, const pkv_bf16 *q,
+int launch_attn(const CUtensorMap &tmK, const CUtensorMap &tmV, const CUtensorMap &tmK3,
+                const CUtensorMap &tmV3, const pkv_bf16 *q,
                 const Problem &p, float scale_log2, float *o_part, float *lse_part,
                 int *parts, pkv_bf16 *out, int32_t *err, const StepArgs &sa,
                 cudaStream_t stream) {
@@ -1254,7 +1300,7 @@ int launch_attn(const CUtensorMap &tmK, const CUtensorMap &tmV, const pkv_bf16 *
   if (sms <= 0) return pkv::fail(PKV_E_CUDA, "paged_decode_attn: no SM count");
   const int grid = sms * Cfg<D>::CTAS_PER_SM;
   PKV_CUDA_CHECK(pkv::launch_pdl(decode_attn_kernel<D, STEP>, dim3(grid), dim3(kThreads),
-                                 Cfg<D>::SMEM, stream, tmK, tmV,
+                                 Cfg<D>::SMEM, stream, tmK, tmV, tmK3, tmV3,
                                  reinterpret_cast<const __nv_bfloat16 *>(q), p, scale_log2,
                                  o_part, lse_part, parts,
                                  reinterpret_cast<__nv_bfloat16 *>(out), err, sa));
@@ -1365,11 +1411,20 @@ int decode_common(const char *fn, const pkv_bf16 *q, const pkv_bf16 *k_cache,
     lse_part = o_part + static_cast<size_t>(B) * Hq * max_parts * D;
   }
   const int box_rows = page_size < kT ? page_size : kT;
-  CUtensorMap tmK, tmV;
-  int st = make_cache_map(&tmK, k_cache, rows, D, box_rows);
+  CUtensorMap tmK, tmV, tmK3, tmV3;
+  int st = make_cache_map(&tmK, k_cache, rows, D, box_rows, page_size, false);
   if (st != PKV_OK) return st;
-  st = make_cache_map(&tmV, v_cache, rows, D, box_rows);
+  st = make_cache_map(&tmV, v_cache, rows, D, box_rows, page_size, false);
   if (st != PKV_OK) return st;
+  if (box_rows == kT) {
+    st = make_cache_map(&tmK3, k_cache, rows, D, box_rows, page_size, true);
+    if (st != PKV_OK) return st;
+    st = make_cache_map(&tmV3, v_cache, rows, D, box_rows, page_size, true);
+    if (st != PKV_OK) return st;
+  } else {
+    tmK3 = tmK;
+    tmV3 = tmV;
+  }
   int log2_ps = 0;
   while ((1 << log2_ps) < page_size) ++log2_ps;
   Problem p;
@@ -1394,9 +1449,9 @@ int decode_common(const char *fn, const pkv_bf16 *q, const pkv_bf16 *k_cache,
   const StepArgs none = {};
   const StepArgs &a = sa ? *sa : none;
 #define PKV_LAUNCH(DD)                                                                        \
-  st = sa ? launch_attn<DD, true>(tmK, tmV, q, p, scale_log2, o_part, lse_part, parts, out,   \
+  st = sa ? launch_attn<DD, true>(tmK, tmV, tmK3, tmV3, q, p, scale_log2, o_part, lse_part, parts, out,   \
                                   err_word, a, s)                                             \
-          : launch_attn<DD, false>(tmK, tmV, q, p, scale_log2, o_part, lse_part, parts, out,  \
+          : launch_attn<DD, false>(tmK, tmV, tmK3, tmV3, q, p, scale_log2, o_part, lse_part, parts, out,  \
                                    err_word, a, s)
   switch (D) {
     case 64: PKV_LAUNCH(64); break;
