@@ -22,13 +22,13 @@ from .pagetable import (PageTableModel, NoSlot, NoPages, BadSlot, BadArg,
                         PageTableError)
 from .paged_kv import (physical_row, kv_append, gather_pages,
                        ERR_POS, ERR_PAGE_RANGE, ERR_PAGE_NEG, ERR_SLOT)
-from .norm_rope import rms_norm, rope, qk_norm_rope, inv_freq
+from .norm_rope import rms_norm, rope, qk_norm_rope, inv_freq, v_norm
 from .attention import decode_attention, decode_attention_row
 
 __all__ = [
     "PageTableModel", "NoSlot", "NoPages", "BadSlot", "BadArg", "PageTableError",
     "physical_row", "kv_append", "gather_pages",
     "ERR_POS", "ERR_PAGE_RANGE", "ERR_PAGE_NEG", "ERR_SLOT",
-    "rms_norm", "rope", "qk_norm_rope", "inv_freq",
+    "rms_norm", "rope", "qk_norm_rope", "inv_freq", "v_norm",
     "decode_attention", "decode_attention_row",
 ]

@@ -86,3 +86,54 @@ def test_norm_then_rope_order_and_pos_zero():
     # without the norm branch only the rotation is applied
     q2, k2 = oracle.qk_norm_rope(q, k, None, None, [3, 9], 1e4, 1e-6, norm=False)
     assert np.allclose(q2, oracle.rope(q, [3, 9], 1e4), atol=0)
+
+
+# ------------------------------------------------ Gemma-4 variants
+def test_proportional_rope_hand_values_and_pass_through():
+    """Partial (proportional) RoPE: only the leading rotary_dims rotate, with the
+    full-dimension frequencies; the tail pairs see inv_freq 0 (cos 1, sin 0)."""
+    # D=8, theta=100, rotary_dims=4: inv_freq = [1, 100^(-2/8), 0, 0]
+    f = oracle.inv_freq(8, 100.0, 4)
+    assert np.allclose(f, [1.0, 100.0 ** -0.25, 0.0, 0.0], rtol=1e-15)
+    x = np.arange(1.0, 9.0)[None, :]           # x1 = [1,2,3,4], x2 = [5,6,7,8]
+    p = 0.5
+    y = oracle.rope(x, [p], 100.0, 4)[0]
+    a0, a1 = p * 1.0, p * 100.0 ** -0.25
+    want = [1 * math.cos(a0) - 5 * math.sin(a0), 2 * math.cos(a1) - 6 * math.sin(a1), 3.0, 4.0,
+            5 * math.cos(a0) + 1 * math.sin(a0), 6 * math.cos(a1) + 2 * math.sin(a1), 7.0, 8.0]
+    assert np.allclose(y, want, rtol=1e-13)
+    rng = np.random.default_rng(10)
+    x = rng.standard_normal((3, 2, 512))
+    pos = np.array([7.0, 300.0, 2047.0])
+    y = oracle.rope(x, pos, 1e6, 128)
+    # pairs 64..255 (dims 64..255 and 320..511) pass through exactly
+    assert np.array_equal(y[..., 64:256], x[..., 64:256])
+    assert np.array_equal(y[..., 320:], x[..., 320:])
+    # the rotated part equals the full rope's first 64 pairs (same frequencies)
+    full = oracle.rope(x, pos, 1e6)
+    assert np.allclose(y[..., :64], full[..., :64], atol=0)
+    assert np.allclose(y[..., 256:320], full[..., 256:320], atol=0)
+    # norm preserved, inverse rotation, and the two ends of the range
+    assert np.allclose(np.linalg.norm(y, axis=-1), np.linalg.norm(x, axis=-1), rtol=1e-12)
+    assert np.allclose(oracle.rope(y, -pos, 1e6, 128), x, atol=1e-12)
+    assert np.array_equal(oracle.rope(x, pos, 1e6, 0), x)
+    assert np.array_equal(oracle.rope(x, pos, 1e6, 512), full)
+
+
+def test_v_norm_is_rms_norm_without_gain():
+    # constant vector c -> c / sqrt(c^2 + eps); [3, 4] with eps 0 -> x / sqrt(12.5)
+    for c in (-2.0, 0.25):
+        assert np.allclose(oracle.v_norm(np.full((1, 1, 6), c), 1e-6),
+                           c / math.sqrt(c * c + 1e-6), rtol=1e-15)
+    assert np.allclose(oracle.v_norm(np.array([3.0, 4.0]), 0.0),
+                       [3 / math.sqrt(12.5), 4 / math.sqrt(12.5)], rtol=1e-15)
+    rng = np.random.default_rng(11)
+    v = rng.standard_normal((4, 2, 256))
+    y = oracle.v_norm(v, 0.0)
+    assert np.allclose(np.mean(y * y, -1), 1.0)                 # unit mean square
+    assert np.allclose(oracle.v_norm(-3.0 * v, 0.0), -y)         # scale-free, sign kept
+    # with K=V the value is the raw k normalised without a gain: it differs from the key
+    # (which also carries gamma_k and the rotation)
+    gk = 1 + 0.1 * rng.standard_normal(256)
+    _, k = oracle.qk_norm_rope(v, v, gk, gk, [5, 9, 11, 13], 1e6, 1e-6, rotary_dims=64)
+    assert not np.allclose(oracle.v_norm(v, 1e-6), k)
