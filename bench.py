@@ -91,9 +91,10 @@ WORKLOAD_CHOICES = {
     "llama": ("llama", 0, "Llama-3.2-3B-shaped decode layer: B=16, 24/8 heads, D=128, page 64, "
                           "L ~ U[512,1024], theta 5e5, no q/k norm"),
     "gemma-sliding": ("gemma", 0, "Gemma-4-E2B sliding layer: B=64, 8/1 heads, D=256, window 512, "
-                                  "page 64, L ~ U[256,2048], theta 1e4, q/k norm"),
+                                  "page 64, L ~ U[256,2048], theta 1e4, q/k norm, v norm"),
     "gemma-full": ("gemma", 1, "Gemma-4-E2B full layer: B=64, 8/1 heads, D=512, page 64, "
-                               "L ~ U[256,2048], theta 1e6, q/k norm"),
+                               "L ~ U[256,2048], theta 1e6 proportional RoPE on 128 dims, "
+                               "q/k norm, v norm, K=V"),
 }
 
 
@@ -332,7 +333,8 @@ def run_ours(args, world, rank, local):
     wname, li, desc = WORKLOAD_CHOICES[args.workload]
     w = wl.WORKLOADS[wname]
     lay = w.layers[li]
-    spec = engine.LayerSpec(lay.head_dim, lay.theta, lay.window, lay.qk_norm, True)
+    spec = engine.LayerSpec(lay.head_dim, lay.theta, lay.window, lay.qk_norm, True,
+                            lay.rotary_dims, lay.v_norm, lay.k_eq_v)
     B, Hq, Hkv, D, ps = w.batch, w.n_q_heads, w.n_kv_heads, spec.head_dim, w.page_size
     W, K = args.warmup, args.steps
     total = W + K

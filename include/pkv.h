@@ -142,6 +142,22 @@ int qk_norm_rope(pkv_bf16 *q, pkv_bf16 *k, const pkv_bf16 *gamma_q,
                  float eps, int B, int Hq, int Hkv, int D, void *stream);
 
 /* ---------------------------------------------------------------------
+ * qkv_norm_rope — qk_norm_rope with the Gemma-4 options of [P1] (two-tier
+ * RoPE, per-head Q/K/V RMSNorm, Rotary helpers docstring):
+ *   - rotary_dims (even, 0..D): only pairs i < rotary_dims/2 rotate, the
+ *     rest pass through, as a zero inverse frequency does ("proportional"
+ *     RoPE; rotary_dims = D is qk_norm_rope's full RoPE). Rotated pairs keep
+ *     the full-dimension frequency theta^(-2i/D).
+ *   - v (bf16 [B][Hkv][D], may be NULL): normalised in place without a gain,
+ *     v / sqrt(mean(v^2) + eps) (v_norm, with_scale=False).
+ * Other arguments as in qk_norm_rope; same arithmetic, one bf16 rounding.
+ * ------------------------------------------------------------------- */
+int qkv_norm_rope(pkv_bf16 *q, pkv_bf16 *k, pkv_bf16 *v, const pkv_bf16 *gamma_q,
+                  const pkv_bf16 *gamma_k, const int32_t *pos, float theta,
+                  float eps, int rotary_dims, int B, int Hq, int Hkv, int D,
+                  void *stream);
+
+/* ---------------------------------------------------------------------
  * qk_norm_rope_append — qk_norm_rope followed by kv_append in one kernel
  * (the write-then-attend prologue of [P1]'s attention forward: q/k norm,
  * rotary, then the paged write of [P3] PageTable.assign). Results are
@@ -236,6 +252,24 @@ int paged_decode_step(const pkv_bf16 *q, const pkv_bf16 *k, const pkv_bf16 *v,
                       int window, float scale, int B, int Hq, int Hkv, int D,
                       int num_splits, void *workspace, size_t workspace_bytes,
                       pkv_bf16 *out, int32_t *err_word, void *stream);
+/* paged_decode_step_ex — paged_decode_step with the Gemma-4 options of
+ * qkv_norm_rope ([P1] two-tier RoPE, v_norm, K=V alternative): rotary_dims
+ * as in qkv_norm_rope; v_norm != 0 normalises the appended value without a
+ * gain; k_eq_v != 0 takes the value from the raw k row (before k_norm and
+ * RoPE) instead of v, which may then be NULL. Equals qkv_norm_rope (on
+ * copies, with v' = copy of k when k_eq_v) -> kv_append -> paged_decode_attn
+ * bit for bit. paged_decode_step is this call with rotary_dims = D,
+ * v_norm = k_eq_v = 0. */
+int paged_decode_step_ex(const pkv_bf16 *q, const pkv_bf16 *k, const pkv_bf16 *v,
+                         const pkv_bf16 *gamma_q, const pkv_bf16 *gamma_k,
+                         const int32_t *batch_idx, const int32_t *input_pos,
+                         float theta, float eps, int rotary_dims, int v_norm,
+                         int k_eq_v, const int32_t *dev_table, int n_slots,
+                         int max_pages_per_seq, int page_size, int n_pages,
+                         pkv_bf16 *k_cache, pkv_bf16 *v_cache, int window,
+                         float scale, int B, int Hq, int Hkv, int D,
+                         int num_splits, void *workspace, size_t workspace_bytes,
+                         pkv_bf16 *out, int32_t *err_word, void *stream);
 
 /* ---------------------------------------------------------------------
  * paged_decode_attn_noalloc — paged_decode_attn without a caller workspace.

@@ -91,6 +91,12 @@ _SIGS = {
     "paged_decode_attn_splits": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
                                           ctypes.POINTER(_c_int)]),
     "paged_decode_attn_workspace": (_c_sz, [_c_int, _c_int, _c_int, _c_int]),
+    "qkv_norm_rope": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_f, _c_f, _c_int, _c_int,
+                               _c_int, _c_int, _c_int, _c_p]),
+    "paged_decode_step_ex": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_f, _c_f,
+                                      _c_int, _c_int, _c_int, _c_p, _c_int, _c_int, _c_int,
+                                      _c_int, _c_p, _c_p, _c_int, _c_f, _c_int, _c_int, _c_int,
+                                      _c_int, _c_int, _c_p, _c_sz, _c_p, _c_p, _c_p]),
     "paged_decode_step": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_f, _c_f, _c_p,
                                    _c_int, _c_int, _c_int, _c_int, _c_p, _c_p, _c_int, _c_f,
                                    _c_int, _c_int, _c_int, _c_int, _c_int, _c_p, _c_sz, _c_p,
@@ -312,6 +318,20 @@ def qk_norm_rope(q, k, gamma_q, gamma_k, pos, theta: float, eps: float = 1e-6,
         B, Hq, Hkv, D, _stream(stream)), "qk_norm_rope")
 
 
+def qkv_norm_rope(q, k, v, gamma_q, gamma_k, pos, theta: float, eps: float = 1e-6,
+                  rotary_dims: int | None = None, stream=None) -> None:
+    """qk_norm_rope with partial rotary (leading rotary_dims of D) and, when v
+    is given, v normalised in place without a gain."""
+    _bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v"), _bf16(gamma_q, "gamma_q")
+    _bf16(gamma_k, "gamma_k"), _i32(pos, "pos")
+    B, Hq, D = q.shape
+    Hkv = 0 if k is None else k.shape[1]
+    rd = D if rotary_dims is None else int(rotary_dims)
+    _check(load_library().qkv_norm_rope(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(gamma_q), _ptr(gamma_k), _ptr(pos), float(theta),
+        float(eps), rd, B, Hq, Hkv, D, _stream(stream)), "qkv_norm_rope")
+
+
 def qk_norm_rope_append(q, k, v, gamma_q, gamma_k, batch_idx, input_pos, theta: float,
                         eps, dev_table, n_slots, max_pages_per_seq, page_size, n_pages,
                         k_cache, v_cache, err_word=None, stream=None) -> None:
@@ -372,6 +392,29 @@ def paged_decode_step(q, k, v, gamma_q, gamma_k, batch_idx, input_pos, theta, ep
         page_size, n_pages, _ptr(k_cache), _ptr(v_cache), int(window), float(scale), B, Hq, Hkv,
         D, int(num_splits), _ptr(workspace), ws_bytes, _ptr(out), _ptr(err_word),
         _stream(stream)), "paged_decode_step")
+
+
+def paged_decode_step_ex(q, k, v, gamma_q, gamma_k, batch_idx, input_pos, theta, eps,
+                         rotary_dims, v_norm, k_eq_v, dev_table, n_slots, max_pages_per_seq,
+                         page_size, n_pages, k_cache, v_cache, window, scale, num_splits,
+                         workspace, out, err_word=None, stream=None) -> None:
+    """paged_decode_step with the Gemma-4 options: rotary on the leading
+    rotary_dims (None: all of D), gain-free value norm, value = raw k."""
+    _bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v"), _bf16(gamma_q, "gamma_q")
+    _bf16(gamma_k, "gamma_k"), _bf16(k_cache, "k_cache"), _bf16(v_cache, "v_cache")
+    _bf16(out, "out")
+    _i32(dev_table, "dev_table"), _i32(batch_idx, "batch_idx"), _i32(input_pos, "input_pos")
+    B, Hq, D = q.shape
+    Hkv = k_cache.shape[0]
+    rd = D if rotary_dims is None else int(rotary_dims)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load_library().paged_decode_step_ex(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(gamma_q), _ptr(gamma_k), _ptr(batch_idx),
+        _ptr(input_pos), float(theta), float(eps), rd, int(bool(v_norm)), int(bool(k_eq_v)),
+        _ptr(dev_table), n_slots, max_pages_per_seq, page_size, n_pages, _ptr(k_cache),
+        _ptr(v_cache), int(window), float(scale), B, Hq, Hkv, D, int(num_splits),
+        _ptr(workspace), ws_bytes, _ptr(out), _ptr(err_word), _stream(stream)),
+        "paged_decode_step_ex")
 
 
 def paged_decode_attn_noalloc(q, k_cache, v_cache, dev_table, n_slots, max_pages_per_seq,

@@ -278,6 +278,9 @@ struct StepArgs {
   const __nv_bfloat16 *gamma_q, *gamma_k; // [D] each, or both NULL (no norm)
   float log2_theta, eps;
   __nv_bfloat16 *k_cache, *v_cache;       // the caches the tensor maps read
+  int rot_pairs;   // rotated pairs (D/2 = full RoPE; fewer: Gemma-4 proportional RoPE)
+  int v_norm;      // value gets the gain-free RMSNorm (Gemma-4 v_norm)
+  int k_eq_v;      // value is the raw k row (Gemma-4 K=V), not v_new
 };
 
 // Cache row of token `pos` of `slot` with kv_append's checks in its order
@@ -306,9 +309,11 @@ __device__ __forceinline__ long long append_row(const Problem &p, int slot, int 
   return (static_cast<long long>(page) << p.log2_ps) + (pos & ((1 << p.log2_ps) - 1));
 }
 
-// Norm + RoPE of the new k of (row b, kv head g) by one warp, then the
-// kv_append write of k and v at cache row `row` (>= 0). Used for rows that
-// have no keys to attend to (padding rows), whose append no unit performs.
+// Norm + RoPE of the new k of (row b, kv head g) by one warp, the value
+// (v_new or, with K=V, the raw k row; gain-free RMSNorm when v_norm), then
+// the kv_append write of k and v at cache row `row` (>= 0). Used for rows
+// that have no keys to attend to (padding rows), whose append no unit
+// performs.
 template <int D>
 __device__ __forceinline__ void step_append_head(const Problem &p, const StepArgs &sa, int b,
                                                  int g, float fpos, long long row, int lane) {
@@ -316,8 +321,8 @@ __device__ __forceinline__ void step_append_head(const Problem &p, const StepArg
   constexpr int half = D / 2;
   const size_t src = (static_cast<size_t>(b) * p.Hkv + g) * D;
   float lo[PAIRS], hi[PAIRS];
-  pkv_norm_rope_lane<PAIRS>(sa.k_new + src, sa.gamma_k, fpos, sa.log2_theta, sa.eps, D, lane,
-                            lo, hi);
+  pkv_norm_rope_lane<PAIRS>(sa.k_new + src, sa.gamma_k, fpos, sa.log2_theta, sa.rot_pairs,
+                            sa.eps, D, lane, lo, hi);
   const size_t dst = (static_cast<size_t>(g) * p.n_pages * (1 << p.log2_ps) + row) * D;
 #pragma unroll
   for (int j = 0; j < PAIRS; ++j) {
@@ -327,9 +332,22 @@ __device__ __forceinline__ void step_append_head(const Problem &p, const StepArg
       sa.k_cache[dst + i + half] = __float2bfloat16_rn(hi[j]);
     }
   }
-  const uint4 *vs = reinterpret_cast<const uint4 *>(sa.v_new + src);
-  for (int c = lane; c < D / 8; c += 32)
-    reinterpret_cast<uint4 *>(sa.v_cache + dst)[c] = __ldg(vs + c);
+  const __nv_bfloat16 *vsrc = (sa.k_eq_v ? sa.k_new : sa.v_new) + src;
+  if (sa.v_norm) {
+    pkv_rms_norm_lane<PAIRS>(vsrc, sa.eps, D, lane, lo, hi);
+#pragma unroll
+    for (int j = 0; j < PAIRS; ++j) {
+      const int i = lane + 32 * j;
+      if (i < half) {
+        sa.v_cache[dst + i] = __float2bfloat16_rn(lo[j]);
+        sa.v_cache[dst + i + half] = __float2bfloat16_rn(hi[j]);
+      }
+    }
+  } else {
+    const uint4 *vs = reinterpret_cast<const uint4 *>(vsrc);
+    for (int c = lane; c < D / 8; c += 32)
+      reinterpret_cast<uint4 *>(sa.v_cache + dst)[c] = __ldg(vs + c);
+  }
 }
 
 // Largest b in [0, B) with scale * arr[b] <= x, for a non-decreasing arr
@@ -726,7 +744,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
           if (kv_rows && (lane == 30 || lane == 31)) {
             const size_t src = (static_cast<size_t>(w.b) * p.Hkv + w.g) * D;
             bulk_load(qdst + Cf::Q_BYTES + (lane - 30) * D * 2,
-                      lane == 30 ? sa.k_new + src : sa.v_new + src,
+                      lane == 30 || sa.k_eq_v ? sa.k_new + src : sa.v_new + src,
                       static_cast<uint32_t>(D * 2), fullQ + 8 * qs);
           }
         }
@@ -895,7 +913,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
         float *fac = reinterpret_cast<float *>(sm + Cf::OFF_FAC);
         for (int i = tid; i < D / 2; i += kCThreads) {
           float cs, sn;
-          pkv_rope_factor(i, D, fpos, sa.log2_theta, cs, sn);
+          pkv_rope_factor(i, D, fpos, sa.log2_theta, sa.rot_pairs, cs, sn);
           fac[i] = cs;
           fac[D / 2 + i] = sn;
         }
@@ -930,6 +948,18 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
               reinterpret_cast<__nv_bfloat16 *>(sm + Cf::OFF_Q + qs * Cf::Q_STAGE + Cf::Q_BYTES);
           float lo[PAIRS], hi[PAIRS];
           rotate_row(kx, gq ? gq + D : nullptr, lo, hi);
+          if (sa.v_norm) {   // the value row, in place: gain-free RMSNorm
+            __nv_bfloat16 *vx = kx + D;
+            pkv_rms_norm_lane<PAIRS>(vx, sa.eps, D, lane, lo, hi);
+#pragma unroll
+            for (int j = 0; j < PAIRS; ++j) {
+              const int i = lane + 32 * j;
+              if (i < D / 2) {
+                vx[i] = __float2bfloat16_rn(lo[j]);
+                vx[i + D / 2] = __float2bfloat16_rn(hi[j]);
+              }
+            }
+          }
           __syncwarp();
           const size_t dst = (static_cast<size_t>(w.g) * p.n_pages * (1 << p.log2_ps) +
                               static_cast<size_t>(app_b)) * D;
@@ -1495,6 +1525,37 @@ int paged_decode_attn(const pkv_bf16 *q, const pkv_bf16 *k_cache,
                        err_word, nullptr, stream);
 }
 
+int paged_decode_step_ex(const pkv_bf16 *q, const pkv_bf16 *k, const pkv_bf16 *v,
+                         const pkv_bf16 *gamma_q, const pkv_bf16 *gamma_k,
+                         const int32_t *batch_idx, const int32_t *input_pos, float theta,
+                         float eps, int rotary_dims, int v_norm, int k_eq_v,
+                         const int32_t *dev_table, int n_slots, int max_pages_per_seq,
+                         int page_size, int n_pages, pkv_bf16 *k_cache, pkv_bf16 *v_cache,
+                         int window, float scale, int B, int Hq, int Hkv, int D,
+                         int num_splits, void *workspace, size_t workspace_bytes,
+                         pkv_bf16 *out, int32_t *err_word, void *stream) {
+  if (!(theta > 0.f) || !std::isfinite(theta))
+    return pkv::fail(PKV_E_BAD_ARG, "paged_decode_step: theta must be finite and > 0");
+  if (rotary_dims < 0 || rotary_dims > D || rotary_dims % 2)
+    return pkv::fail(PKV_E_BAD_ARG, "paged_decode_step: rotary_dims must be even and in [0, D]");
+  StepArgs sa;
+  sa.k_new = reinterpret_cast<const __nv_bfloat16 *>(k);
+  sa.v_new = reinterpret_cast<const __nv_bfloat16 *>(k_eq_v ? k : v);
+  sa.gamma_q = reinterpret_cast<const __nv_bfloat16 *>(gamma_q);
+  sa.gamma_k = reinterpret_cast<const __nv_bfloat16 *>(gamma_k);
+  sa.log2_theta = log2f(theta);
+  sa.eps = eps;
+  sa.k_cache = reinterpret_cast<__nv_bfloat16 *>(k_cache);
+  sa.v_cache = reinterpret_cast<__nv_bfloat16 *>(v_cache);
+  sa.rot_pairs = rotary_dims / 2;
+  sa.v_norm = v_norm ? 1 : 0;
+  sa.k_eq_v = k_eq_v ? 1 : 0;
+  return decode_common("paged_decode_step", q, k_cache, v_cache, dev_table, n_slots,
+                       max_pages_per_seq, page_size, n_pages, batch_idx, input_pos, window,
+                       scale, B, Hq, Hkv, D, num_splits, workspace, workspace_bytes, out,
+                       err_word, &sa, stream);
+}
+
 int paged_decode_step(const pkv_bf16 *q, const pkv_bf16 *k, const pkv_bf16 *v,
                       const pkv_bf16 *gamma_q, const pkv_bf16 *gamma_k,
                       const int32_t *batch_idx, const int32_t *input_pos, float theta,
@@ -1503,21 +1564,10 @@ int paged_decode_step(const pkv_bf16 *q, const pkv_bf16 *k, const pkv_bf16 *v,
                       pkv_bf16 *v_cache, int window, float scale, int B, int Hq, int Hkv,
                       int D, int num_splits, void *workspace, size_t workspace_bytes,
                       pkv_bf16 *out, int32_t *err_word, void *stream) {
-  if (!(theta > 0.f) || !std::isfinite(theta))
-    return pkv::fail(PKV_E_BAD_ARG, "paged_decode_step: theta must be finite and > 0");
-  StepArgs sa;
-  sa.k_new = reinterpret_cast<const __nv_bfloat16 *>(k);
-  sa.v_new = reinterpret_cast<const __nv_bfloat16 *>(v);
-  sa.gamma_q = reinterpret_cast<const __nv_bfloat16 *>(gamma_q);
-  sa.gamma_k = reinterpret_cast<const __nv_bfloat16 *>(gamma_k);
-  sa.log2_theta = log2f(theta);
-  sa.eps = eps;
-  sa.k_cache = reinterpret_cast<__nv_bfloat16 *>(k_cache);
-  sa.v_cache = reinterpret_cast<__nv_bfloat16 *>(v_cache);
-  return decode_common("paged_decode_step", q, k_cache, v_cache, dev_table, n_slots,
-                       max_pages_per_seq, page_size, n_pages, batch_idx, input_pos, window,
-                       scale, B, Hq, Hkv, D, num_splits, workspace, workspace_bytes, out,
-                       err_word, &sa, stream);
+  return paged_decode_step_ex(q, k, v, gamma_q, gamma_k, batch_idx, input_pos, theta, eps, D, 0,
+                              0, dev_table, n_slots, max_pages_per_seq, page_size, n_pages,
+                              k_cache, v_cache, window, scale, B, Hq, Hkv, D, num_splits,
+                              workspace, workspace_bytes, out, err_word, stream);
 }
 
 }  // extern "C"

@@ -19,8 +19,15 @@
 
 #include <cuda_bf16.h>
 
+// Rotation factors of pair i. Pairs i >= rot_pairs are not rotated (Gemma-4
+// proportional RoPE: a zero inverse frequency gives cos 1, sin 0 there).
 __device__ __forceinline__ void pkv_rope_factor(int i, int D, float pos, float log2_theta,
-                                                float &cs, float &sn) {
+                                                int rot_pairs, float &cs, float &sn) {
+  if (i >= rot_pairs) {
+    cs = 1.f;
+    sn = 0.f;
+    return;
+  }
   // theta^(-2i/D) = 2^(-(2i/D) log2 theta)
   const float e = __fdiv_rn(2.0f * static_cast<float>(i), static_cast<float>(D));
   const float inv_freq = exp2f(-__fmul_rn(e, log2_theta));
@@ -74,10 +81,44 @@ __device__ __forceinline__ void pkv_norm_rope_core(const __nv_bfloat16 *x,
 template <int PAIRS>
 __device__ __forceinline__ void pkv_norm_rope_lane(const __nv_bfloat16 *x,
                                                    const __nv_bfloat16 *g, float pos,
-                                                   float log2_theta, float eps, int D, int lane,
-                                                   float (&lo)[PAIRS], float (&hi)[PAIRS]) {
+                                                   float log2_theta, int rot_pairs, float eps,
+                                                   int D, int lane, float (&lo)[PAIRS],
+                                                   float (&hi)[PAIRS]) {
   pkv_norm_rope_core<PAIRS>(
       x, g, eps, D, lane,
-      [&](int i, float &cs, float &sn) { pkv_rope_factor(i, D, pos, log2_theta, cs, sn); }, lo,
-      hi);
+      [&](int i, float &cs, float &sn) {
+        pkv_rope_factor(i, D, pos, log2_theta, rot_pairs, cs, sn);
+      },
+      lo, hi);
+}
+
+// RMSNorm without a gain (Gemma-4 v_norm, with_scale=False): the same sum of
+// squares and scale as the gained norm above, then one rounding per output.
+template <int PAIRS>
+__device__ __forceinline__ void pkv_rms_norm_lane(const __nv_bfloat16 *x, float eps, int D,
+                                                  int lane, float (&lo)[PAIRS],
+                                                  float (&hi)[PAIRS]) {
+  const int half = D >> 1;
+  float ss = 0.f;
+#pragma unroll
+  for (int j = 0; j < PAIRS; ++j) {
+    const int i = lane + 32 * j;
+    if (i < half) {
+      lo[j] = __bfloat162float(x[i]);
+      hi[j] = __bfloat162float(x[i + half]);
+      ss = __fmaf_rn(lo[j], lo[j], ss);
+      ss = __fmaf_rn(hi[j], hi[j], ss);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, o));
+  const float inv_rms = rsqrtf(__fadd_rn(__fdiv_rn(ss, static_cast<float>(D)), eps));
+#pragma unroll
+  for (int j = 0; j < PAIRS; ++j) {
+    const int i = lane + 32 * j;
+    if (i < half) {
+      lo[j] = __fmul_rn(lo[j], inv_rms);
+      hi[j] = __fmul_rn(hi[j], inv_rms);
+    }
+  }
 }

@@ -18,34 +18,44 @@ constexpr int kMaxPairsPerLane = 16;  // D <= 1024
 
 __device__ __forceinline__ void norm_rope_warp(const __nv_bfloat16 *__restrict__ x,
                                                const __nv_bfloat16 *__restrict__ g, float p,
-                                               float log2_theta, float eps, int D, int lane,
-                                               float (&lo)[kMaxPairsPerLane],
+                                               float log2_theta, int rot_pairs, float eps, int D,
+                                               int lane, float (&lo)[kMaxPairsPerLane],
                                                float (&hi)[kMaxPairsPerLane]) {
-  pkv_norm_rope_lane<kMaxPairsPerLane>(x, g, p, log2_theta, eps, D, lane, lo, hi);
+  pkv_norm_rope_lane<kMaxPairsPerLane>(x, g, p, log2_theta, rot_pairs, eps, D, lane, lo, hi);
 }
 
+// One warp per (row, head) over the q heads, the k heads and (when v is
+// given) the v heads: q and k get norm + rotary on the leading rot_pairs
+// pairs; v gets the gain-free RMSNorm.
 __global__ void qk_norm_rope_kernel(__nv_bfloat16 *__restrict__ q,
                                     __nv_bfloat16 *__restrict__ k,
+                                    __nv_bfloat16 *__restrict__ v,
                                     const __nv_bfloat16 *__restrict__ gq,
                                     const __nv_bfloat16 *__restrict__ gk,
                                     const int32_t *__restrict__ pos,
-                                    float log2_theta, float eps, int B, int Hq,
+                                    float log2_theta, float eps, int rot_pairs, int B, int Hq,
                                     int Hkv, int D) {
   pkv_wait_prior_grid();
   pkv_allow_next_grid();
   const int warps_per_block = blockDim.x >> 5;
   const long long w = blockIdx.x * 1LL * warps_per_block + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
-  const int H = Hq + Hkv;
+  const int H = Hq + Hkv + (v ? Hkv : 0);
   if (w >= 1LL * B * H) return;
   const int b = static_cast<int>(w / H);
   const int h = static_cast<int>(w % H);
-  const bool is_q = h < Hq;
-  __nv_bfloat16 *x = is_q ? q + (1LL * b * Hq + h) * D
-                          : k + (1LL * b * Hkv + (h - Hq)) * D;
   const int half = D >> 1;
   float lo[kMaxPairsPerLane], hi[kMaxPairsPerLane];
-  norm_rope_warp(x, is_q ? gq : gk, static_cast<float>(pos[b]), log2_theta, eps, D, lane, lo, hi);
+  __nv_bfloat16 *x;
+  if (h < Hq + Hkv) {
+    const bool is_q = h < Hq;
+    x = is_q ? q + (1LL * b * Hq + h) * D : k + (1LL * b * Hkv + (h - Hq)) * D;
+    norm_rope_warp(x, is_q ? gq : gk, static_cast<float>(pos[b]), log2_theta, rot_pairs, eps, D,
+                   lane, lo, hi);
+  } else {
+    x = v + (1LL * b * Hkv + (h - Hq - Hkv)) * D;
+    pkv_rms_norm_lane<kMaxPairsPerLane>(x, eps, D, lane, lo, hi);
+  }
 #pragma unroll
   for (int j = 0; j < kMaxPairsPerLane; ++j) {
     int i = lane + 32 * j;
@@ -83,7 +93,7 @@ __global__ void qk_norm_rope_append_kernel(
   if (is_q) {
     __nv_bfloat16 *x = q + (1LL * b * Hq + h) * D;
     float lo[kMaxPairsPerLane], hi[kMaxPairsPerLane];
-    norm_rope_warp(x, gq, static_cast<float>(pb), log2_theta, eps, D, lane, lo, hi);
+    norm_rope_warp(x, gq, static_cast<float>(pb), log2_theta, D / 2, eps, D, lane, lo, hi);
 #pragma unroll
     for (int j = 0; j < kMaxPairsPerLane; ++j) {
       int i = lane + 32 * j;
@@ -108,7 +118,7 @@ __global__ void qk_norm_rope_append_kernel(
   __nv_bfloat16 *x = k + (1LL * b * Hkv + hk) * D;
   const __nv_bfloat16 *vx = v + (1LL * b * Hkv + hk) * D;
   float lo[kMaxPairsPerLane], hi[kMaxPairsPerLane];
-  norm_rope_warp(x, gk, static_cast<float>(pb), log2_theta, eps, D, lane, lo, hi);
+  norm_rope_warp(x, gk, static_cast<float>(pb), log2_theta, D / 2, eps, D, lane, lo, hi);
   if (!bits) {
     if (page < 0) bits = PKV_ERR_PAGE_NEG;
     else if (page >= n_pages) bits = PKV_ERR_PAGE_RANGE;
@@ -136,29 +146,52 @@ __global__ void qk_norm_rope_append_kernel(
 
 }  // namespace
 
-extern "C" int qk_norm_rope(pkv_bf16 *q, pkv_bf16 *k, const pkv_bf16 *gamma_q,
-                            const pkv_bf16 *gamma_k, const int32_t *pos,
-                            float theta, float eps, int B, int Hq, int Hkv,
-                            int D, void *stream) {
+namespace {
+
+int launch_qkv(pkv_bf16 *q, pkv_bf16 *k, pkv_bf16 *v, const pkv_bf16 *gamma_q,
+               const pkv_bf16 *gamma_k, const int32_t *pos, float theta, float eps,
+               int rotary_dims, int B, int Hq, int Hkv, int D, void *stream, const char *fn) {
   if (B < 0 || Hq < 0 || Hkv < 0 || D < 2 || D % 2 || D > 64 * kMaxPairsPerLane)
-    return pkv::fail(PKV_E_BAD_ARG, "qk_norm_rope: bad shape (D even, <= 1024)");
-  if (!(theta > 0.f)) return pkv::fail(PKV_E_BAD_ARG, "qk_norm_rope: theta must be > 0");
-  if (!(eps >= 0.f)) return pkv::fail(PKV_E_BAD_ARG, "qk_norm_rope: eps must be >= 0");
+    return pkv::fail(PKV_E_BAD_ARG, "%s: bad shape (D even, <= 1024)", fn);
+  if (rotary_dims < 0 || rotary_dims > D || rotary_dims % 2)
+    return pkv::fail(PKV_E_BAD_ARG, "%s: rotary_dims must be even and in [0, D]", fn);
+  if (!(theta > 0.f)) return pkv::fail(PKV_E_BAD_ARG, "%s: theta must be > 0", fn);
+  if (!(eps >= 0.f)) return pkv::fail(PKV_E_BAD_ARG, "%s: eps must be >= 0", fn);
   if (Hkv > 0 && (gamma_q == nullptr) != (gamma_k == nullptr))
-    return pkv::fail(PKV_E_BAD_ARG, "qk_norm_rope: give both gains or neither");
-  if (B == 0 || Hq + Hkv == 0) return pkv::ok();
+    return pkv::fail(PKV_E_BAD_ARG, "%s: give both gains or neither", fn);
+  const int H = Hq + Hkv + (v ? Hkv : 0);
+  if (B == 0 || H == 0) return pkv::ok();
   if (!pos || (Hq && !q) || (Hkv && !k))
-    return pkv::fail(PKV_E_BAD_ARG, "qk_norm_rope: NULL tensor");
-  const long long warps = 1LL * B * (Hq + Hkv);
+    return pkv::fail(PKV_E_BAD_ARG, "%s: NULL tensor", fn);
+  const long long warps = 1LL * B * H;
   const int threads = 256, wpb = threads / 32;
   long long blocks = (warps + wpb - 1) / wpb;
   PKV_CUDA_CHECK(pkv::launch_pdl(
       qk_norm_rope_kernel, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0,
       static_cast<cudaStream_t>(stream), reinterpret_cast<__nv_bfloat16 *>(q),
-      reinterpret_cast<__nv_bfloat16 *>(k), reinterpret_cast<const __nv_bfloat16 *>(gamma_q),
-      reinterpret_cast<const __nv_bfloat16 *>(gamma_k), pos, log2f(theta), eps, B, Hq, Hkv,
-      D));
+      reinterpret_cast<__nv_bfloat16 *>(k), reinterpret_cast<__nv_bfloat16 *>(v),
+      reinterpret_cast<const __nv_bfloat16 *>(gamma_q),
+      reinterpret_cast<const __nv_bfloat16 *>(gamma_k), pos, log2f(theta), eps,
+      rotary_dims / 2, B, Hq, Hkv, D));
   return pkv::ok();
+}
+
+}  // namespace
+
+extern "C" int qk_norm_rope(pkv_bf16 *q, pkv_bf16 *k, const pkv_bf16 *gamma_q,
+                            const pkv_bf16 *gamma_k, const int32_t *pos,
+                            float theta, float eps, int B, int Hq, int Hkv,
+                            int D, void *stream) {
+  return launch_qkv(q, k, nullptr, gamma_q, gamma_k, pos, theta, eps, D, B, Hq, Hkv, D, stream,
+                    "qk_norm_rope");
+}
+
+extern "C" int qkv_norm_rope(pkv_bf16 *q, pkv_bf16 *k, pkv_bf16 *v, const pkv_bf16 *gamma_q,
+                             const pkv_bf16 *gamma_k, const int32_t *pos, float theta,
+                             float eps, int rotary_dims, int B, int Hq, int Hkv, int D,
+                             void *stream) {
+  return launch_qkv(q, k, v, gamma_q, gamma_k, pos, theta, eps, rotary_dims, B, Hq, Hkv, D,
+                    stream, "qkv_norm_rope");
 }
 
 extern "C" int qk_norm_rope_append(pkv_bf16 *q, pkv_bf16 *k, const pkv_bf16 *v,

@@ -22,7 +22,8 @@ import numpy as np
 import torch
 
 from . import (PageTable, kv_append, paged_decode_attn, paged_decode_attn_splits,
-               paged_decode_attn_workspace, paged_decode_step, qk_norm_rope)
+               paged_decode_attn_workspace, paged_decode_step, paged_decode_step_ex,
+               qk_norm_rope, qkv_norm_rope)
 
 
 @dataclasses.dataclass(frozen=True)
@@ -32,6 +33,13 @@ class LayerSpec:
     window: int = 0
     qk_norm: bool = False
     rope: bool = True
+    rotary_dims: int = 0      # 0: all of head_dim; fewer: Gemma-4 proportional RoPE
+    v_norm: bool = False      # Gemma-4 gain-free RMSNorm of the value
+    k_eq_v: bool = False      # Gemma-4 K=V: the value is the raw k projection
+
+    @property
+    def gemma_options(self) -> bool:
+        return bool(self.rotary_dims) or self.v_norm or self.k_eq_v
 
 
 def alloc_cache(Hkv: int, n_pages: int, page_size: int, D: int, device, fill: str = "zeros"):
@@ -67,10 +75,11 @@ def decode_layer_step(spec: LayerSpec, pt: PageTable, k_cache, v_cache, q, k, v,
                       table=None, fused: bool = True):
     """One layer's decode step: q/k norm + RoPE, K/V append, attention.
 
-    fused (default, rotary layers): one paged_decode_step call; q, k and v
-    are read only and seq_lens must equal input_pos + 1 (the kernel derives
-    it). Otherwise the chain qk_norm_rope -> kv_append -> paged_decode_attn,
-    which rotates q and k in place; both give the same bits.
+    fused (default, rotary layers): one paged_decode_step(_ex) call; q, k and
+    v are read only and seq_lens must equal input_pos + 1 (the kernel derives
+    it). Otherwise the chain qk_norm_rope (qkv_norm_rope with the Gemma-4
+    options) -> kv_append -> paged_decode_attn, which rotates q and k (and
+    normalises v) in place; both give the same bits.
 
     `pt` supplies the table geometry (n_slots, max_pages_per_seq, page_size,
     n_pages) and, unless `table` is given, the device table itself."""
@@ -78,13 +87,27 @@ def decode_layer_step(spec: LayerSpec, pt: PageTable, k_cache, v_cache, q, k, v,
     scale = scale if scale is not None else spec.head_dim ** -0.5
     gq = gamma_q if spec.qk_norm else None
     gk = gamma_k if spec.qk_norm else None
+    if spec.gemma_options and not spec.rope:
+        raise ValueError("rotary_dims, v_norm and k_eq_v need a rotary layer")
     if fused and spec.rope:
-        paged_decode_step(q, k, v, gq, gk, batch_idx, input_pos, spec.theta, eps, table,
-                          pt.n_slots, pt.max_pages_per_seq, pt.page_size, pt.n_pages, k_cache,
-                          v_cache, spec.window, scale, ws.splits, ws.buf, out, err,
-                          stream=stream)
+        if spec.gemma_options:
+            paged_decode_step_ex(q, k, v, gq, gk, batch_idx, input_pos, spec.theta, eps,
+                                 spec.rotary_dims or None, spec.v_norm, spec.k_eq_v, table,
+                                 pt.n_slots, pt.max_pages_per_seq, pt.page_size, pt.n_pages,
+                                 k_cache, v_cache, spec.window, scale, ws.splits, ws.buf, out,
+                                 err, stream=stream)
+        else:
+            paged_decode_step(q, k, v, gq, gk, batch_idx, input_pos, spec.theta, eps, table,
+                              pt.n_slots, pt.max_pages_per_seq, pt.page_size, pt.n_pages,
+                              k_cache, v_cache, spec.window, scale, ws.splits, ws.buf, out,
+                              err, stream=stream)
         return
-    if spec.rope:
+    if spec.k_eq_v:
+        v = k.clone()        # the raw k row, before k is rotated in place
+    if spec.gemma_options:
+        qkv_norm_rope(q, k, v if spec.v_norm else None, gq, gk, input_pos, spec.theta, eps,
+                      spec.rotary_dims or None, stream=stream)
+    elif spec.rope:
         qk_norm_rope(q, k, gq, gk, input_pos, spec.theta, eps, stream=stream)
     kv_append(k, v, batch_idx, input_pos, table, pt.n_slots, pt.max_pages_per_seq,
               pt.page_size, pt.n_pages, k_cache, v_cache, err, stream=stream)

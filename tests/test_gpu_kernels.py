@@ -138,6 +138,39 @@ def test_qk_norm_rope_parity(dev, B, Hq, Hkv, D, theta, norm):
         assert e.mean() <= 2.0 ** -9 * np.abs(ref).mean() + 1e-4
 
 
+@pytest.mark.parametrize("B,Hq,Hkv,D,theta,rd", [
+    (4, 8, 1, 512, 1e6, 128), (6, 8, 1, 256, 1e4, 256), (5, 16, 4, 128, 1e6, 0),
+    (3, 6, 2, 64, 1e4, 16)])
+def test_qkv_norm_rope_partial_rotary_and_v_norm(dev, B, Hq, Hkv, D, theta, rd):
+    """Gemma-4 options: RoPE on the leading rd dims (the rest pass through) and
+    the gain-free RMSNorm of v, against the oracle; the pass-through dims of q
+    and k equal the normalised inputs rounded once."""
+    rng = np.random.default_rng(B * 7000 + D + rd)
+    q = wl.randn_bf16(rng, (B, Hq, D))
+    k = wl.randn_bf16(rng, (B, Hkv, D))
+    v = wl.randn_bf16(rng, (B, Hkv, D), scale=3.0)
+    gq, gk = wl.gamma_bf16(rng, D), wl.gamma_bf16(rng, D)
+    pos = rng.integers(0, 2100, size=B).astype(np.int32)
+    dq, dk, dv = q.to(dev), k.to(dev), v.to(dev)
+    pkv.qkv_norm_rope(dq, dk, dv, gq.to(dev), gk.to(dev), torch.from_numpy(pos).to(dev), theta,
+                      1e-6, rd)
+    torch.cuda.synchronize()
+    rq, rk = oracle.qk_norm_rope(q.double().numpy(), k.double().numpy(), gq.double().numpy(),
+                                 gk.double().numpy(), pos, theta, 1e-6, rotary_dims=rd)
+    rv = oracle.v_norm(v.double().numpy(), 1e-6)
+    for got, ref in ((f64(dq), rq), (f64(dk), rk), (f64(dv), rv)):
+        e = np.abs(got - ref)
+        assert (e <= _norm_rope_bound(ref)).all(), e.max()
+        assert e.mean() <= 2.0 ** -9 * np.abs(ref).mean() + 1e-4
+    # with rotary_dims = D the call is qk_norm_rope bit for bit
+    if rd == D:
+        q2, k2 = q.to(dev), k.to(dev)
+        pkv.qk_norm_rope(q2, k2, gq.to(dev), gk.to(dev), torch.from_numpy(pos).to(dev), theta,
+                         1e-6)
+        torch.cuda.synchronize()
+        assert np.array_equal(bits(q2), bits(dq)) and np.array_equal(bits(k2), bits(dk))
+
+
 # ----------------------------------------------------------- paged attention
 ATTN_CASES = [
     # D, Hq, Hkv, ps, lens, window, splits

@@ -33,7 +33,8 @@ class StepCase:
     """A paged case for one decode step: row b appends at input_pos[b], so
     its pages cover input_pos[b] + 1 tokens; the append rows start as NaN."""
 
-    def __init__(self, seed, B, Hq, Hkv, D, ps, pos, slots=None, norm=True, theta=1e6):
+    def __init__(self, seed, B, Hq, Hkv, D, ps, pos, slots=None, norm=True, theta=1e6,
+                 rotary_dims=None, v_norm=False, k_eq_v=False):
         rng = np.random.default_rng(seed)
         self.pos = np.asarray(pos, np.int32)
         self.case = PagedCase(rng, B, Hq, Hkv, D, ps, self.pos.astype(np.int64) + 1,
@@ -52,6 +53,11 @@ class StepCase:
         self.gq = wl.gamma_bf16(rng, D) if norm else None
         self.gk = wl.gamma_bf16(rng, D) if norm else None
         self.theta = theta
+        self.rotary_dims, self.v_norm, self.k_eq_v = rotary_dims, v_norm, k_eq_v
+
+    @property
+    def gemma(self):
+        return self.rotary_dims is not None or self.v_norm or self.k_eq_v
 
 
 def _ws(B, Hq, Hkv, D, max_pages, ps, window, splits, dev):
@@ -75,11 +81,21 @@ def run_chain_and_step(sc: StepCase, dev, window, splits, eps=1e-6, table=None):
         err = torch.zeros(1, dtype=torch.int32, device=dev)
         ws = _ws(c.B, c.Hq, c.Hkv, c.D, c.max_pages, c.ps, window, splits, dev)
         if mode == "chain":
-            pkv.qk_norm_rope(q, k, g(sc.gq), g(sc.gk), pos, sc.theta, eps)
-            pkv.kv_append(k, v, bidx, pos, tbl, c.n_slots, c.max_pages, c.ps, c.P, d["kc"],
+            vv = k.clone() if sc.k_eq_v else v.clone()
+            if sc.gemma:
+                pkv.qkv_norm_rope(q, k, vv if sc.v_norm else None, g(sc.gq), g(sc.gk), pos,
+                                  sc.theta, eps, sc.rotary_dims)
+            else:
+                pkv.qk_norm_rope(q, k, g(sc.gq), g(sc.gk), pos, sc.theta, eps)
+            pkv.kv_append(k, vv, bidx, pos, tbl, c.n_slots, c.max_pages, c.ps, c.P, d["kc"],
                           d["vc"], err)
             pkv.paged_decode_attn(q, d["kc"], d["vc"], tbl, c.n_slots, c.max_pages, c.ps, c.P,
                                   bidx, pos + 1, window, scale, splits, ws, out, err)
+        elif sc.gemma:
+            pkv.paged_decode_step_ex(q, k, None if sc.k_eq_v else v, g(sc.gq), g(sc.gk), bidx,
+                                     pos, sc.theta, eps, sc.rotary_dims, sc.v_norm, sc.k_eq_v,
+                                     tbl, c.n_slots, c.max_pages, c.ps, c.P, d["kc"], d["vc"],
+                                     window, scale, splits, ws, out, err)
         else:
             pkv.paged_decode_step(q, k, v, g(sc.gq), g(sc.gk), bidx, pos, sc.theta, eps, tbl,
                                   c.n_slots, c.max_pages, c.ps, c.P, d["kc"], d["vc"], window,
@@ -131,6 +147,47 @@ def test_step_equals_chain(dev, B, Hq, Hkv, D, ps, pr, window, splits, norm):
     res = run_chain_and_step(sc, dev, window, splits)
     assert res["step"]["err"] == 0
     assert_step_equals_chain(res, sc)
+
+
+GEMMA_CASES = [
+    # B, Hq, Hkv, D, ps, pos range, window, rotary_dims, v_norm, k_eq_v
+    (12, 8, 1, 512, 64, (0, 2100), 0, 128, True, True),     # Gemma-4 full layer
+    (12, 8, 1, 256, 64, (0, 2100), 512, None, True, False),  # Gemma-4 sliding layer
+    (9, 16, 4, 128, 16, (0, 500), 0, 32, False, True),       # K=V without v_norm
+    (7, 8, 2, 64, 64, (0, 300), 0, 0, True, False),          # no rotation at all
+]
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,D,ps,pr,window,rd,vn,kv", GEMMA_CASES)
+def test_step_gemma_options_equal_chain(dev, B, Hq, Hkv, D, ps, pr, window, rd, vn, kv):
+    """paged_decode_step_ex (proportional RoPE, v_norm, K=V) against the chain
+    qkv_norm_rope -> kv_append -> paged_decode_attn, bit for bit."""
+    rng = np.random.default_rng(4600 + B + D)
+    pos = _positions(rng, B, pr[0], pr[1], ps)
+    sc = StepCase(4700 + B + D, B, Hq, Hkv, D, ps, pos, rotary_dims=rd, v_norm=vn, k_eq_v=kv)
+    res = run_chain_and_step(sc, dev, window, 0)
+    assert res["step"]["err"] == 0
+    assert_step_equals_chain(res, sc)
+
+
+def test_step_gemma_full_matches_oracle(dev):
+    """The Gemma-4 full-layer step from raw inputs against the oracle: q/k
+    RMSNorm, RoPE on the leading 128 of 512 dims, v = v_norm(raw k)."""
+    rng = np.random.default_rng(4800)
+    B, Hq, Hkv, D, ps = 10, 8, 1, 512, 64
+    pos = _positions(rng, B, 0, 2000, ps)
+    sc = StepCase(4801, B, Hq, Hkv, D, ps, pos, rotary_dims=128, v_norm=True, k_eq_v=True)
+    c = sc.case
+    res = run_chain_and_step(sc, dev, 0, 0)
+    qd, kd = c.q.double().numpy(), sc.k.double().numpy()
+    g = lambda t: t.double().numpy()
+    qr, kr = oracle.qk_norm_rope(qd, kd, g(sc.gq), g(sc.gk), sc.pos, sc.theta, 1e-6,
+                                 rotary_dims=128)
+    vr = oracle.v_norm(kd, 1e-6)
+    kc, vc = bits_to_f64(c.kc_bits), bits_to_f64(c.vc_bits)
+    assert oracle.kv_append(kc, vc, kr, vr, c.table, c.slots, sc.pos, ps, c.P) == 0
+    ref, _ = oracle.decode_attention(qr, kc, vc, c.table, c.slots, sc.pos + 1, 0, D ** -0.5, ps)
+    assert_attn_close(bits_to_f64(res["step"]["out"]), ref)
 
 
 def test_step_matches_oracle_end_to_end(dev):

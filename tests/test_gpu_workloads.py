@@ -47,8 +47,8 @@ def _prefill(rng, pt, caches, slot, n, Hkv, dev):
                       pt.page_size, pt.n_pages, kc, vc, None)
 
 
-def _check_step(w, spec, pt, model, kc, vc, q_raw, k_raw, v_raw, q_gpu, k_gpu, out, meta,
-                gq, gk, check_chain):
+def _check_step(w, spec, pt, model, kc, vc, q_raw, k_raw, v_raw, q_gpu, k_gpu, v_gpu, out,
+                meta, gq, gk, check_chain):
     table = pt.dev_table.cpu().numpy()
     assert np.array_equal(table, model.table)
     pos = meta.input_pos
@@ -57,15 +57,19 @@ def _check_step(w, spec, pt, model, kc, vc, q_raw, k_raw, v_raw, q_gpu, k_gpu, o
         rq, rk = oracle.qk_norm_rope(q_raw.double().numpy(), k_raw.double().numpy(),
                                      None if gq is None else gq.double().numpy(),
                                      None if gk is None else gk.double().numpy(),
-                                     pos, spec.theta, w.eps, norm=spec.qk_norm)
-        for got, ref in ((f64(q_gpu), rq), (f64(k_gpu), rk)):
+                                     pos, spec.theta, w.eps, norm=spec.qk_norm,
+                                     rotary_dims=spec.rotary_dims or None)
+        rv = (k_raw if spec.k_eq_v else v_raw).double().numpy()
+        if spec.v_norm:
+            rv = oracle.v_norm(rv, w.eps)
+        for got, ref in ((f64(q_gpu), rq), (f64(k_gpu), rk), (f64(v_gpu), rv)):
             assert (np.abs(got - ref) <= 2.0 ** -8 * np.abs(ref) + 2e-3).all()
-    # appended rows hold exactly the GPU's k and the raw v
+    # appended rows hold exactly the GPU's k and v
     kb, vb = bits(kc), bits(vc)
     for b in range(w.batch):
         row = oracle.physical_row(model.table, int(meta.batch_idx[b]), int(pos[b]), w.page_size)
         assert np.array_equal(kb[:, row, :], bits(k_gpu)[b])
-        assert np.array_equal(vb[:, row, :], bits(v_raw)[b])
+        assert np.array_equal(vb[:, row, :], bits(v_gpu)[b])
     # attention on the GPU's own inputs
     scale = spec.head_dim ** -0.5
     ref, _ = oracle.decode_attention(f64(q_gpu), bits_to_f64(kb), bits_to_f64(vb), model.table,
@@ -79,26 +83,30 @@ def _check_step(w, spec, pt, model, kc, vc, q_raw, k_raw, v_raw, q_gpu, k_gpu, o
             row = oracle.physical_row(model.table, int(meta.batch_idx[b]), int(pos[b]),
                                       w.page_size)
             kf[:, row, :] = rk[b]
-            vf[:, row, :] = v_raw[b].double().numpy()
+            vf[:, row, :] = rv[b]
         ref2, _ = oracle.decode_attention(rq, kf, vf, model.table, meta.batch_idx,
                                           meta.seq_lens, spec.window, scale, w.page_size)
         assert_attn_close(f64(out), ref2)
 
 
-def _rotated(spec, q, k, gq, gk, pos, eps, dev, fused):
-    """The rotated q and k the step attended with: the in-place result of the
-    chain, or (fused step) qk_norm_rope applied to copies of the inputs."""
-    if not (fused and spec.rope):
-        return q, k
-    qr, kr = q.clone(), k.clone()
+def _rotated(spec, q_raw, k_raw, v_raw, gq, gk, pos, eps, dev):
+    """The q, k and v the step attended with and appended, recomputed with
+    qkv_norm_rope on copies of the raw inputs (the chain's in-place results
+    and the fused kernel reproduce these bits)."""
+    qr, kr = q_raw.to(dev), k_raw.to(dev)
+    vr = (k_raw if spec.k_eq_v else v_raw).to(dev)
+    if not spec.rope:
+        return qr, kr, vr
     g = (lambda t: None if t is None or not spec.qk_norm else t.to(dev))
-    pkv.qk_norm_rope(qr, kr, g(gq), g(gk), pos, spec.theta, eps)
-    return qr, kr
+    pkv.qkv_norm_rope(qr, kr, vr if spec.v_norm else None, g(gq), g(gk), pos, spec.theta, eps,
+                      spec.rotary_dims or None)
+    return qr, kr, vr
 
 
 def _specs(w):
     rope = w.name != "tiny"
-    return [engine.LayerSpec(l.head_dim, l.theta, l.window, l.qk_norm, rope) for l in w.layers]
+    return [engine.LayerSpec(l.head_dim, l.theta, l.window, l.qk_norm, rope, l.rotary_dims,
+                             l.v_norm, l.k_eq_v) for l in w.layers]
 
 
 @pytest.mark.parametrize("fused", [True, False])
@@ -149,9 +157,9 @@ def test_static_workload(dev, name, steps, fused):
                                      fused=fused)
             torch.cuda.synchronize()
             if t in check_at:
-                qr, kr = _rotated(spec, q, k, gq, gk, d_pos, w.eps, dev, fused)
-                _check_step(w, spec, pt, model, kc, vc, q_raw, k_raw, v_raw, qr, kr, out, meta,
-                            gq, gk, check_chain=(t == steps - 1))
+                qr, kr, vr = _rotated(spec, q_raw, k_raw, v_raw, gq, gk, d_pos, w.eps, dev)
+                _check_step(w, spec, pt, model, kc, vc, q_raw, k_raw, v_raw, qr, kr, vr, out,
+                            meta, gq, gk, check_chain=(t == steps - 1))
         length = [L + 1 for L in length]
     assert pkv.pkv_read_error_word(err) == 0
 
@@ -248,8 +256,8 @@ def test_rollout_continuous_batching(dev, fused):
                                  w.eps, err=err, fused=fused)
         if t in check_at:
             torch.cuda.synchronize()
-            qr, kr = _rotated(spec, q, k, gq, gk, d_pos, w.eps, dev, fused)
-            _check_step(w, spec, pt, model, kc, vc, q_raw, k_raw, v_raw, qr, kr, out, meta,
+            qr, kr, vr = _rotated(spec, q_raw, k_raw, v_raw, gq, gk, d_pos, w.eps, dev)
+            _check_step(w, spec, pt, model, kc, vc, q_raw, k_raw, v_raw, qr, kr, vr, out, meta,
                         gq, gk, check_chain=(t == w.steps - 1))
         elif t % 16 == 0:
             assert np.array_equal(pt.dev_table.cpu().numpy(), model.table), t

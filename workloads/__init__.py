@@ -20,8 +20,9 @@ not available here; uniform length draws stand in for it.
              ~ U[100, 400], 512 steps; each sequence stops at a seeded
              length in [L0 + 16, 1024] and its slot is refilled at once.
   gemma      B=64, Hq=8, Hkv=1, page 64, L ~ U[256, 2048]; sliding layer
-             D=256, window 512, theta 1e4; full layer D=512, theta 1e6;
-             q/k RMSNorm as qwen3.
+             D=256, window 512, theta 1e4; full layer D=512, theta 1e6 with
+             proportional RoPE over the leading 25% (128 dims) and K=V; q/k
+             RMSNorm as qwen3 and the gain-free v RMSNorm on both layers.
 
 The base seed 3407 is the seed the pages' drivers use.
 """
@@ -42,6 +43,9 @@ class LayerShape:
     theta: float
     window: int = 0          # <= 0: no sliding window
     qk_norm: bool = False
+    rotary_dims: int = 0     # 0: rotary over all of head_dim (proportional RoPE: fewer)
+    v_norm: bool = False     # gain-free RMSNorm of the value
+    k_eq_v: bool = False     # value taken from the raw k projection
 
 
 @dataclasses.dataclass(frozen=True)
@@ -85,8 +89,9 @@ ROLLOUT = Workload("rollout", batch=64, max_batch_size=64, n_q_heads=32, n_kv_he
                    layers=(LayerShape(128, 1e6, qk_norm=True),), steps=512, seed_offset=4)
 GEMMA = Workload("gemma", batch=64, max_batch_size=64, n_q_heads=8, n_kv_heads=1,
                  page_size=64, n_pages=64 * 33 + 1, max_seq=2112,
-                 layers=(LayerShape(256, 1e4, window=512, qk_norm=True),
-                         LayerShape(512, 1e6, qk_norm=True)),
+                 layers=(LayerShape(256, 1e4, window=512, qk_norm=True, v_norm=True),
+                         LayerShape(512, 1e6, qk_norm=True, rotary_dims=128, v_norm=True,
+                                    k_eq_v=True)),
                  steps=4, seed_offset=5)
 
 WORKLOADS = {w.name: w for w in (TINY, QWEN3, LLAMA, ROLLOUT, GEMMA)}
