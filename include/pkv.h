@@ -124,6 +124,17 @@ int kv_append(const pkv_bf16 *k, const pkv_bf16 *v, const int32_t *batch_idx,
               pkv_bf16 *k_cache, pkv_bf16 *v_cache, int Hkv, int D,
               int32_t *err_word, void *stream);
 
+/* kv_append_prefill — the prefill scatter of [P3] PageTable
+ * (assign_prefill_no_paging): L packed tokens, token j with its own slot
+ * batch_idx[j] and position input_pos[j], k and v head-major bf16
+ * [Hkv][L][D] (the pages' [1, H, L, D]). Same address map, checks and error
+ * bits as kv_append, which this is with the head-major layout. */
+int kv_append_prefill(const pkv_bf16 *k, const pkv_bf16 *v, const int32_t *batch_idx,
+                      const int32_t *input_pos, int L, const int32_t *dev_table,
+                      int n_slots, int max_pages_per_seq, int page_size, int n_pages,
+                      pkv_bf16 *k_cache, pkv_bf16 *v_cache, int Hkv, int D,
+                      int32_t *err_word, void *stream);
+
 /* ---------------------------------------------------------------------
  * qk_norm_rope — per-head RMSNorm then RoPE, in place ([P1] attention
  * forward: q_norm / k_norm on the head axis before rotary; rotary helpers

@@ -77,6 +77,8 @@ _SIGS = {
     "pt_host_table": (_c_int, [_c_p, _c_ip, _c_int]),
     "kv_append": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_int, _c_p, _c_int, _c_int, _c_int,
                            _c_int, _c_p, _c_p, _c_int, _c_int, _c_p, _c_p]),
+    "kv_append_prefill": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_int, _c_p, _c_int, _c_int, _c_int,
+                                   _c_int, _c_p, _c_p, _c_int, _c_int, _c_p, _c_p]),
     "qk_norm_rope": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_p, _c_f, _c_f, _c_int, _c_int,
                               _c_int, _c_int, _c_p]),
     "qk_norm_rope_append": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_f, _c_f,
@@ -305,6 +307,18 @@ def kv_append(k, v, batch_idx, input_pos, dev_table, n_slots, max_pages_per_seq,
         _ptr(k), _ptr(v), _ptr(batch_idx), _ptr(input_pos), B, _ptr(dev_table), n_slots,
         max_pages_per_seq, page_size, n_pages, _ptr(k_cache), _ptr(v_cache), Hkv, D,
         _ptr(err_word), _stream(stream)), "kv_append")
+
+
+def kv_append_prefill(k, v, batch_idx, input_pos, dev_table, n_slots, max_pages_per_seq,
+                      page_size, n_pages, k_cache, v_cache, err_word=None, stream=None) -> None:
+    """Scatter L packed prefill tokens; k and v are head-major [Hkv][L][D]."""
+    _bf16(k, "k"), _bf16(v, "v"), _bf16(k_cache, "k_cache"), _bf16(v_cache, "v_cache")
+    _i32(batch_idx, "batch_idx"), _i32(input_pos, "input_pos"), _i32(dev_table, "dev_table")
+    Hkv, L, D = k.shape
+    _check(load_library().kv_append_prefill(
+        _ptr(k), _ptr(v), _ptr(batch_idx), _ptr(input_pos), L, _ptr(dev_table), n_slots,
+        max_pages_per_seq, page_size, n_pages, _ptr(k_cache), _ptr(v_cache), Hkv, D,
+        _ptr(err_word), _stream(stream)), "kv_append_prefill")
 
 
 def qk_norm_rope(q, k, gamma_q, gamma_k, pos, theta: float, eps: float = 1e-6,

@@ -158,3 +158,186 @@ class RolloutDriver:
             self.length[lane] += 1
         self.t += 1
         return StepMeta(np.array(self.slots, dtype=np.int32), pos, pos + 1, admitted)
+
+
+# --------------------------------------------------------------------------
+# Batch buckets and the continuous-batching scheduler
+# --------------------------------------------------------------------------
+
+def bucket_ladder(max_bs: int) -> list:
+    """The pages' CUDA-graph batch buckets (capture_decode_cudagraph):
+    1, 2, 4, 8, then every multiple of 16 up to max_bs."""
+    return [b for b in [1, 2, 4, 8] if b <= max_bs] + list(range(16, max_bs + 1, 16))
+
+
+def bucket_for(B: int, ladder: list) -> int:
+    """Smallest bucket holding B rows (a decode batch is padded up to it)."""
+    for b in ladder:
+        if b >= B:
+            return b
+    raise ValueError(f"batch {B} exceeds the largest bucket {ladder[-1]}")
+
+
+@dataclasses.dataclass
+class Sequence:
+    rid: int
+    prompt_len: int
+    max_new_tokens: int
+    generated: int = 0
+    slot: int = -1
+    finished: bool = False
+
+    @property
+    def total_length(self) -> int:
+        return self.prompt_len + self.generated
+
+
+class ContinuousBatcher:
+    """The scheduling of the pages' generate loop ("unsloth: compare
+    main...flex-moe-qwen3" · flex_gemma4_moe.py · generate) over a PageTable:
+
+      * admission (prefill first): while the head of the waiting queue fits
+        (can_reserve(total_length)), give it a slot reserved for its whole
+        length; an admitted batch is prefilled and the loop starts over;
+      * decode: each running sequence keeps its capacity or grows it by
+        reserve; when it cannot, it goes back to the front of the queue and
+        the newest running sequence is preempted (its slot and pages freed,
+        it returns to the front of the waiting queue, keeping its tokens);
+      * every prefill or decode appends one token; a sequence that reaches
+        max_new_tokens finishes and frees its slot.
+
+    The model work is supplied by prefill(batch) and decode(batch) callbacks
+    (each gets the Sequence list; decode rows are in running order). events
+    records ("prefill" | "decode", [rids]), ("preempt", rid) and ("finish",
+    rid) in order."""
+
+    def __init__(self, pt: PageTable, sequences, prefill=None, decode=None):
+        import collections
+        self.pt = pt
+        self.waiting = collections.deque(sequences)
+        self.running = collections.deque()
+        self.done = []
+        self.events = []
+        self._prefill = prefill
+        self._decode = decode
+
+    def _finish_if_done(self, s: Sequence) -> bool:
+        if s.generated >= s.max_new_tokens:
+            s.finished = True
+            self.done.append(s)
+            self.pt.free(s.slot)
+            self.events.append(("finish", s.rid))
+            s.slot = -1
+            return True
+        return False
+
+    def step(self) -> bool:
+        """One pass of the loop; False once nothing is waiting or running."""
+        if not (self.waiting or self.running):
+            return False
+        batch = []
+        while self.waiting and self.pt.can_reserve(self.waiting[0].total_length):
+            s = self.waiting.popleft()
+            s.slot = self.pt.assign(s.total_length)
+            batch.append(s)
+        if batch:
+            self.events.append(("prefill", [s.rid for s in batch]))
+            if self._prefill:
+                self._prefill(batch)
+            for s in batch:
+                s.generated += 1
+                if not self._finish_if_done(s):
+                    self.running.append(s)
+            return True
+        decode_batch = []
+        while self.running:
+            s = self.running.popleft()
+            if self.pt.capacity(s.slot) >= s.total_length:
+                decode_batch.append(s)
+            elif self.pt.can_reserve(s.total_length, s.slot):
+                self.pt.reserve(s.slot, s.total_length)
+                decode_batch.append(s)
+            else:
+                self.running.appendleft(s)
+                newest = self.running.pop()
+                self.waiting.appendleft(newest)
+                self.pt.free(newest.slot)
+                newest.slot = -1
+                self.events.append(("preempt", newest.rid))
+        if not decode_batch:
+            return True
+        self.events.append(("decode", [s.rid for s in decode_batch]))
+        if self._decode:
+            self._decode(decode_batch)
+        for s in decode_batch:
+            s.generated += 1
+            if not self._finish_if_done(s):
+                self.running.append(s)
+        return True
+
+    def run(self, max_steps: int = 100000) -> list:
+        for _ in range(max_steps):
+            if not self.step():
+                return self.done
+        raise RuntimeError("scheduler did not drain")
+
+
+class DecodeGraphs:
+    """One CUDA graph of the decode layer step per batch bucket, as the pages'
+    capture_decode_cudagraph does (graphs over static buffers, replayed after
+    copying the step's inputs in). A batch of B rows replays the smallest
+    bucket >= B; rows B.. of the bucket are padding rows on slot 0 (the
+    reserved slot: no keys, zero output, their append lands in the reserved
+    page 0). The page table is read through pt.dev_table, which the host
+    allocator updates between steps."""
+
+    def __init__(self, spec: LayerSpec, pt: PageTable, k_cache, v_cache, Hq: int, max_bs: int,
+                 device, gamma_q=None, gamma_k=None, eps: float = 1e-6, ladder=None):
+        self.spec, self.pt, self.kc, self.vc = spec, pt, k_cache, v_cache
+        self.gq, self.gk, self.eps = gamma_q, gamma_k, eps
+        self.ladder = ladder or bucket_ladder(max_bs)
+        Hkv, D = k_cache.shape[0], k_cache.shape[2]
+        bf = dict(dtype=torch.bfloat16, device=device)
+        i32 = dict(dtype=torch.int32, device=device)
+        self.q = torch.zeros((max_bs, Hq, D), **bf)
+        self.k = torch.zeros((max_bs, Hkv, D), **bf)
+        self.v = torch.zeros((max_bs, Hkv, D), **bf)
+        self.out = torch.zeros((max_bs, Hq, D), **bf)
+        self.batch_idx = torch.zeros(max_bs, **i32)
+        self.input_pos = torch.zeros(max_bs, **i32)
+        self.seq_lens = torch.ones(max_bs, **i32)
+        self.err = torch.zeros(1, **i32)
+        self.ws = {b: AttnWorkspace(b, Hq, Hkv, D, pt.max_pages_per_seq, pt.page_size,
+                                    spec.window, device) for b in self.ladder}
+        self.graphs = {}
+        for b in reversed(self.ladder):
+            self._call(b)                  # eager first use of every kernel
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                self._call(b)
+            self.graphs[b] = g
+        torch.cuda.synchronize()
+
+    def _call(self, b):
+        decode_layer_step(self.spec, self.pt, self.kc, self.vc, self.q[:b], self.k[:b],
+                          self.v[:b], self.batch_idx[:b], self.input_pos[:b],
+                          self.seq_lens[:b], self.out[:b], self.ws[b], self.gq, self.gk,
+                          self.eps, err=self.err)
+
+    def step(self, q, k, v, batch_idx, input_pos):
+        """Device tensors for B rows; returns the B rows of the output (a view
+        of the static buffer, valid until the next step)."""
+        B = q.shape[0]
+        b = bucket_for(B, self.ladder)
+        self.q[:B].copy_(q)
+        self.k[:B].copy_(k)
+        self.v[:B].copy_(v)
+        self.batch_idx[:B].copy_(batch_idx)
+        self.input_pos[:B].copy_(input_pos)
+        self.seq_lens[:B].copy_(input_pos + 1)
+        self.batch_idx[B:b].zero_()
+        self.input_pos[B:b].zero_()
+        self.seq_lens[B:b].fill_(1)
+        self.graphs[b].replay()
+        return self.out[:B]

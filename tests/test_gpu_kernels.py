@@ -105,6 +105,40 @@ def test_kv_append_error_bits_without_fault(dev):
     assert not bits(kc).any() and not bits(vc).any()
 
 
+def test_kv_append_prefill_packed_documents(dev):
+    """The prefill scatter of packed tokens (head-major [Hkv][L][D], one slot
+    and position per token, documents interleaved) equals the oracle's scatter
+    of the same tokens, bit for bit, with invalid tokens reported and skipped."""
+    rng = np.random.default_rng(77)
+    Hkv, D, ps, P, max_pages = 3, 128, 16, 40, 6
+    table = np.full((5, max_pages), -1, np.int32)
+    table[0] = 0
+    table[1:5] = rng.permutation(np.arange(1, P))[:4 * max_pages].reshape(4, max_pages)
+    lens = [37, 5, 60, 1]                       # prompt lengths of slots 1..4
+    slots = np.concatenate([np.full(n, s + 1) for s, n in enumerate(lens)]).astype(np.int32)
+    pos = np.concatenate([np.arange(n) for n in lens]).astype(np.int32)
+    perm = rng.permutation(len(slots))           # the pages do not sort tokens by document
+    slots, pos = slots[perm], pos[perm]
+    slots[3], pos[7] = 9, max_pages * ps        # a bad slot and a position past the table
+    L = len(slots)
+    k = wl.randn_bf16(rng, (Hkv, L, D))
+    v = wl.randn_bf16(rng, (Hkv, L, D))
+    kc0 = wl.randn_bf16(rng, (Hkv, P * ps, D))
+    vc0 = wl.randn_bf16(rng, (Hkv, P * ps, D))
+    dkc, dvc = kc0.to(dev), vc0.to(dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    d = lambda a: torch.from_numpy(a).to(dev)
+    pkv.kv_append_prefill(k.to(dev), v.to(dev), d(slots), d(pos), d(table), 5, max_pages, ps, P,
+                          dkc, dvc, err)
+    ref_k, ref_v = bits(kc0).copy(), bits(vc0).copy()
+    kt = bits(k).transpose(1, 0, 2).copy()       # token-major for the oracle
+    vt = bits(v).transpose(1, 0, 2).copy()
+    want = oracle.kv_append(ref_k, ref_v, kt, vt, table, slots, pos, ps, P)
+    assert want == pkv.PKV_ERR_SLOT | pkv.PKV_ERR_POS
+    assert pkv.pkv_read_error_word(err) == want
+    assert np.array_equal(bits(dkc), ref_k) and np.array_equal(bits(dvc), ref_v)
+
+
 # --------------------------------------------------------------- qk_norm_rope
 def _norm_rope_bound(ref):
     # one bf16 rounding (relative 2^-9) of an fp32 result, with slack
