@@ -9,7 +9,8 @@ computes, written from the pages' statement of the method:
   * ``norm_rope``  — per-head RMSNorm followed by rotate-half RoPE;
   * ``attention``  — GQA decode attention over a gathered, contiguous K/V
     with length and sliding-window masking, plus its log-sum-exp.
-  * ``prefill``    — document-causal attention over packed prefill tokens.
+  * ``prefill``    — document-causal (optionally sliding) attention over packed
+    prefill tokens, and its block mask (full / partial key blocks).
 
 Only the test suite, the package smoke check and the benchmark's CPU
 baseline may import this package. The product path (the CUDA library and its
@@ -25,12 +26,13 @@ from .paged_kv import (physical_row, kv_append, gather_pages,
                        ERR_POS, ERR_PAGE_RANGE, ERR_PAGE_NEG, ERR_SLOT)
 from .norm_rope import rms_norm, rope, qk_norm_rope, inv_freq, v_norm
 from .attention import decode_attention, decode_attention_row
-from .prefill import prefill_attention
+from .prefill import prefill_attention, prefill_block_mask, keep_matrix
 
 __all__ = [
     "PageTableModel", "NoSlot", "NoPages", "BadSlot", "BadArg", "PageTableError",
     "physical_row", "kv_append", "gather_pages",
     "ERR_POS", "ERR_PAGE_RANGE", "ERR_PAGE_NEG", "ERR_SLOT",
     "rms_norm", "rope", "qk_norm_rope", "inv_freq", "v_norm", "prefill_attention",
+    "prefill_block_mask", "keep_matrix",
     "decode_attention", "decode_attention_row",
 ]
