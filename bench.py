@@ -66,7 +66,8 @@ def parse_args():
                          "instead of the fused paged_decode_step")
     ap.add_argument("--layers", type=int, default=0,
                     help="layer caches to cycle (0: enough for 4x L2)")
-    ap.add_argument("--workload", default="rollout", choices=sorted(WORKLOAD_CHOICES),
+    ap.add_argument("--workload", default="rollout",
+                    choices=sorted(list(WORKLOAD_CHOICES) + ["prefill"]),
                     help="rollout (the headline line) or one of the static decode layers")
     return ap.parse_args()
 
@@ -556,12 +557,133 @@ def run_e2e(args, w, spec, engine, pkv, caches, n_layers, tables, bidx, pos, len
             "eager_value": byts / (ms_eager * 1e-3) / 1e9, "eager_ms_per_step": ms_eager / n}
 
 
+def prefill_docs(n_docs: int = 64, seed_salt: int = 31):
+    """Packed prefill: n_docs prompts with the rollout's admission lengths
+    U[100, 400], laid one after another (document id per token)."""
+    rng = np.random.default_rng(wl.ROLLOUT.seed(seed_salt))
+    lens = wl.uniform_lengths(rng, n_docs, 100, 400)
+    return np.repeat(np.arange(n_docs), lens).astype(np.int32), lens
+
+
+def prefill_flops(lens, Hq: int, D: int) -> float:
+    """QK^T and PV over the kept (causal, same-document) pairs: 4 D Hq per pair."""
+    lens = np.asarray(lens, dtype=np.float64)
+    return float(4.0 * D * Hq * np.sum(lens * (lens + 1) / 2))
+
+
+def run_prefill(args, world, rank, local):
+    """Document-causal prefill attention (prefill_attn) on 64 packed prompts
+    with Qwen3-4B heads (32 q / 8 kv, head_dim 128); tensor-core bound. A
+    step is one layer's attention call; the block mask (prefill_block_mask)
+    depends only on the documents, is built once per batch for all layers,
+    and is timed on its own."""
+    import paged_kv_decode_pagetable_gb300 as pkv
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (the product path has no CPU fallback)")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pkv.load_library()
+    Hq, Hkv, D = 32, 8, 128
+    docs, lens = prefill_docs()
+    L = len(docs)
+    g = torch.Generator(device=dev)
+    g.manual_seed(wl.ROLLOUT.seed(rank + 40))
+    sets = [(torch.randn((Hq, L, D), generator=g, device=dev).to(torch.bfloat16),
+             torch.randn((Hkv, L, D), generator=g, device=dev).to(torch.bfloat16),
+             torch.randn((Hkv, L, D), generator=g, device=dev).to(torch.bfloat16))
+            for _ in range(2)]
+    d_docs = torch.from_numpy(docs).to(dev)
+    out = torch.empty((Hq, L, D), dtype=torch.bfloat16, device=dev)
+    scale = D ** -0.5
+    W, K = args.warmup, min(args.steps, 200)
+
+    bm = pkv.prefill_block_mask(d_docs)
+
+    def call(t):
+        q, k, v = sets[t % 2]
+        pkv.prefill_attn(q, k, v, bm, scale, out)
+
+    for t in range(W):
+        call(t)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for t in range(K):
+            call(t)
+    graph.replay()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(not args.no_clocks, local)
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    stream = torch.cuda.current_stream()
+    e0.record(stream)
+    graph.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop()
+    own_ms = e0.elapsed_time(e1)
+    ms = reduce_max(own_ms, world)
+    # the block mask build, timed alone (graph of K builds)
+    mgraph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(mgraph):
+        for _ in range(K):
+            pkv.prefill_block_mask(d_docs)
+    mgraph.replay()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    mgraph.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    mask_us = e0.elapsed_time(e1) * 1e3 / K
+    flops = prefill_flops(lens, Hq, D)
+    n_blocks = int(bm.kv_num_blocks.sum().item() + bm.full_kv_num_blocks.sum().item())
+    value = reduce_sum(flops * K, world) / (ms * 1e-3) / 1e12
+    peaks, peak_kind = measured_peaks()
+    peak = float(peaks.get("bf16_tflops", 1900.0))
+    achieved = flops * K / (own_ms * 1e-3) / 1e12
+    cpu = None
+    if rank == 0 and world == 1:
+        import oracle
+        n = 3                                      # a bounded sample: the first 3 documents
+        end = int(np.sum(lens[:n]))
+        qs = sets[0][0][:, :end].float().cpu().numpy()
+        ks = sets[0][1][:, :end].float().cpu().numpy()
+        vs = sets[0][2][:, :end].float().cpu().numpy()
+        t0 = time.perf_counter()
+        oracle.prefill_attention(qs, ks, vs, docs[:end], scale)
+        sec = time.perf_counter() - t0
+        cpu = {"value": prefill_flops(lens[:n], Hq, D) / sec / 1e12, "unit": "TFLOP/s",
+               "cores": 1, "kind": "oracle",
+               "sample": f"the first {n} documents ({end} tokens), float64 NumPy, {sec:.1f} s"}
+    if rank == 0:
+        print(json.dumps({
+            "metric": "document-causal prefill attention TFLOP/s", "value": value,
+            "unit": "TFLOP/s", "n_gpus": world, "steps": K, "warmup": W, "ms_per_step": ms / K,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": f"packed prefill: 64 prompts U[100,400] ({L} tokens), "
+                                   "32 q / 8 kv heads, head_dim 128",
+                       "global_batch": 64 * world, "tokens": L, "flops_per_call": flops,
+                       "visited_blocks_per_head": n_blocks,
+                       "block_flops_per_call": 4.0 * 64 * 64 * D * Hq * n_blocks,
+                       "block_mask_us": mask_us, "attn_us_per_call": ms * 1e3 / K,
+                       "l2_policy": "two input sets of ~200 MB (larger than L2) alternated",
+                       "parallelism": f"replicas x{world}"},
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
+                         "unit": "TFLOP/s", "frac": achieved / peak, "peak_kind": peak_kind,
+                         "kernel": "prefill_attn_kernel<128> (mma.sync)", "traffic": None},
+            "cpu_baseline": cpu, "gpu_launches": K, "clocks": clocks}), flush=True)
+
+
 def main():
     args = parse_args()
     world, rank, local = dist_setup(args)
     try:
         if args.impl == "reference":
             run_reference(args, world, rank)
+        elif args.workload == "prefill":
+            run_prefill(args, world, rank, local)
         else:
             run_ours(args, world, rank, local)
     finally:

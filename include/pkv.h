@@ -283,6 +283,56 @@ int paged_decode_step_ex(const pkv_bf16 *q, const pkv_bf16 *k, const pkv_bf16 *v
                          pkv_bf16 *out, int32_t *err_word, void *stream);
 
 /* ---------------------------------------------------------------------
+ * Document-causal prefill attention over L packed prompt tokens
+ * ([P3] PagedKVCache.create_prefill_blockmask_no_paging; the sliding
+ * variant is [P1] _create_prefill_sliding_blockmask): docs[t] is the
+ * document id of token t (any order); query i keeps key j iff j <= i,
+ * docs[j] == docs[i] and, when window W > 0, i - j < W. W = 0 means no
+ * window.
+ *
+ * PKV_PREFILL_BLOCK is the block of the block mask and the attention
+ * kernel's tile: 64 query rows by 64 keys. n = ceil(L / 64).
+ * ------------------------------------------------------------------- */
+#define PKV_PREFILL_BLOCK 64
+
+/* prefill_block_mask — the block mask of that mask (create_block_mask's
+ * BlockMask with B = 1, H = None): for query block qb,
+ *   full_kv_indices[qb][0 .. full_kv_num_blocks[qb])  the key blocks whose
+ *       64 x 64 pairs all lie inside L and are all kept (no masking needed),
+ *   kv_indices[qb][0 .. kv_num_blocks[qb])            the other key blocks
+ *       with at least one kept pair inside L,
+ * both ascending. The counts are int32 [n]; the index arrays int32 [n][n]
+ * (row stride n; entries past a row's count are left unwritten). docs:
+ * int32 [L] device. All four outputs are device memory the caller owns. It
+ * depends only on docs and W, so one build serves every layer and head.
+ * One kernel; L = 0 launches nothing. Errors: PKV_E_BAD_ARG for L < 0,
+ * L > INT_MAX - 64, W < 0 or a NULL pointer; PKV_E_CUDA on a launch
+ * failure. */
+int prefill_block_mask(const int32_t *docs, int L, int window,
+                       int32_t *kv_num_blocks, int32_t *kv_indices,
+                       int32_t *full_kv_num_blocks, int32_t *full_kv_indices,
+                       void *stream);
+
+/* prefill_attn — the attention itself, on the packed tensors (no paging):
+ * q bf16 [Hq][L][D], k and v bf16 [Hkv][L][D] (the pages' [1, H, L, D]),
+ * docs int32 [L], out bf16 [Hq][L][D]; query head h reads kv head
+ * h / (Hq / Hkv).  out[h][i] = sum_j softmax_j(scale * q[h][i] . k_j) v_j
+ * over the kept j. The four block-mask arrays are those prefill_block_mask
+ * writes for the same docs, L and W: only the listed key blocks are
+ * visited, partial ones masked by the rule above, full ones unmasked (a
+ * block listed as full that is not makes its pairs count as kept; list
+ * entries outside [0, n) are skipped, so no list can make a read go out of
+ * bounds). A row with no visited key gets zeros. Requires D in {64, 128},
+ * Hq % Hkv == 0, Hq <= 65535, 16-byte aligned q, k, v, out, scale finite
+ * and > 0. One kernel; no workspace. Errors: PKV_E_BAD_ARG for the above
+ * or a NULL pointer, PKV_E_CUDA on a launch failure. */
+int prefill_attn(const pkv_bf16 *q, const pkv_bf16 *k, const pkv_bf16 *v,
+                 const int32_t *docs, const int32_t *kv_num_blocks,
+                 const int32_t *kv_indices, const int32_t *full_kv_num_blocks,
+                 const int32_t *full_kv_indices, int L, int Hq, int Hkv, int D,
+                 int window, float scale, pkv_bf16 *out, void *stream);
+
+/* ---------------------------------------------------------------------
  * paged_decode_attn_noalloc — paged_decode_attn without a caller workspace.
  * The pages have no counterpart to this call; it exists for callers that
  * cannot allocate device memory (a plain C program linking only this

@@ -79,6 +79,9 @@ _SIGS = {
                            _c_int, _c_p, _c_p, _c_int, _c_int, _c_p, _c_p]),
     "kv_append_prefill": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_int, _c_p, _c_int, _c_int, _c_int,
                                    _c_int, _c_p, _c_p, _c_int, _c_int, _c_p, _c_p]),
+    "prefill_block_mask": (_c_int, [_c_p, _c_int, _c_int, _c_p, _c_p, _c_p, _c_p, _c_p]),
+    "prefill_attn": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_int, _c_int,
+                              _c_int, _c_int, _c_int, _c_f, _c_p, _c_p]),
     "qk_norm_rope": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_p, _c_f, _c_f, _c_int, _c_int,
                               _c_int, _c_int, _c_p]),
     "qk_norm_rope_append": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_f, _c_f,
@@ -447,6 +450,65 @@ def paged_decode_attn_noalloc(q, k_cache, v_cache, dev_table, n_slots, max_pages
         page_size, n_pages, _ptr(batch_idx), _ptr(seq_lens), int(window), float(scale), B, Hq,
         Hkv, D, int(num_splits), _ptr(out), _ptr(err_word), _stream(stream)),
         "paged_decode_attn_noalloc")
+
+
+PREFILL_BLOCK = 64
+
+
+class PrefillBlockMask:
+    """The block mask prefill_block_mask writes (int32 device tensors):
+    kv_num_blocks [n], kv_indices [n][n] (partial blocks),
+    full_kv_num_blocks [n], full_kv_indices [n][n], for n = ceil(L / 64),
+    plus the docs and window it was built for."""
+
+    __slots__ = ("kv_num_blocks", "kv_indices", "full_kv_num_blocks", "full_kv_indices",
+                 "docs", "window")
+
+    def __init__(self, kv_num_blocks, kv_indices, full_kv_num_blocks, full_kv_indices, docs,
+                 window):
+        self.kv_num_blocks = kv_num_blocks
+        self.kv_indices = kv_indices
+        self.full_kv_num_blocks = full_kv_num_blocks
+        self.full_kv_indices = full_kv_indices
+        self.docs = docs
+        self.window = int(window)
+
+
+def prefill_block_mask(docs, window: int = 0, stream=None) -> PrefillBlockMask:
+    """Builds the document-causal (window > 0: sliding) block mask of the
+    packed tokens' document ids docs (int32 [L], device)."""
+    _i32(docs, "docs")
+    L = docs.numel()
+    n = -(-L // PREFILL_BLOCK)
+    dev = docs.device
+    bm = PrefillBlockMask(torch.empty(n, dtype=torch.int32, device=dev),
+                          torch.empty((n, n), dtype=torch.int32, device=dev),
+                          torch.empty(n, dtype=torch.int32, device=dev),
+                          torch.empty((n, n), dtype=torch.int32, device=dev), docs, window)
+    _check(load_library().prefill_block_mask(
+        _ptr(docs), L, int(window), _ptr(bm.kv_num_blocks), _ptr(bm.kv_indices),
+        _ptr(bm.full_kv_num_blocks), _ptr(bm.full_kv_indices), _stream(stream)),
+        "prefill_block_mask")
+    return bm
+
+
+def prefill_attn(q, k, v, block_mask: PrefillBlockMask, scale, out, stream=None) -> None:
+    """Document-causal attention over packed tokens: q [Hq][L][D], k/v
+    [Hkv][L][D], out [Hq][L][D]; block_mask from prefill_block_mask (its docs
+    and window are the mask's)."""
+    _bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v"), _bf16(out, "out")
+    bm = block_mask
+    for name in ("docs", "kv_num_blocks", "kv_indices", "full_kv_num_blocks",
+                 "full_kv_indices"):
+        _i32(getattr(bm, name), name)
+    Hq, L, D = q.shape
+    Hkv = k.shape[0]
+    if bm.docs.numel() != L or bm.kv_num_blocks.numel() != -(-L // PREFILL_BLOCK):
+        raise BadArgError("prefill_attn: block mask built for another length")
+    _check(load_library().prefill_attn(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(bm.docs), _ptr(bm.kv_num_blocks), _ptr(bm.kv_indices),
+        _ptr(bm.full_kv_num_blocks), _ptr(bm.full_kv_indices), L, Hq, Hkv, D, bm.window,
+        float(scale), _ptr(out), _stream(stream)), "prefill_attn")
 
 
 def pkv_read_error_word(err_word, stream=None) -> int:

@@ -1,0 +1,180 @@
+"""GPU parity of the document-causal prefill path (prefill_block_mask and
+prefill_attn) with the float64 oracle, through the C ABI, on the GPU's own
+bf16 inputs. Cases span several 64-token blocks with a ragged tail, one
+token, a single document, contiguous documents of random lengths, documents
+interleaved in no order (the pages do not sort tokens), sliding windows, and
+more than 128 key blocks (the builder's second pass).
+
+The block mask is integer work: equal to the oracle's, entry for entry.
+
+Attention bar, from the kernel's arithmetic: the probabilities P enter the
+P.V product as bf16 (relative error <= 2^-9 each) and the output is rounded
+once to bf16 (<= 2^-9 |o|), so |o_gpu - o| <= 2^-9 (max|v| + |o|) <=
+2^-8 max|v|; prefill has many rows with two or three kept keys, where this is
+reached (the decode rows are long enough that the fixed 1e-2 bar holds
+there). Each element must be within 2^-8 max|v| + 2e-3 and the mean error
+within 1e-3."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as wl
+from gpu_util import f64
+
+pytestmark = pytest.mark.gpu
+pkv = pytest.importorskip("paged_kv_decode_pagetable_gb300")
+BLOCK = 64
+
+
+@pytest.fixture(scope="module")
+def dev():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    pkv.load_library()
+    return torch.device("cuda:0")
+
+
+def _docs(rng, kind, L):
+    if kind == "one":
+        return np.zeros(L, np.int32)
+    if kind == "contiguous":
+        cuts = np.sort(rng.choice(np.arange(1, L), size=min(5, L - 1), replace=False))
+        return np.repeat(np.arange(len(cuts) + 1), np.diff(np.r_[0, cuts, L])).astype(np.int32)
+    if kind == "many":      # rollout-like prompts of 100..400 tokens, packed in order
+        lens = wl.uniform_lengths(rng, L // 100 + 1, 100, 400)
+        return np.repeat(np.arange(len(lens)), lens)[:L].astype(np.int32)
+    return rng.integers(0, 4, size=L).astype(np.int32)      # interleaved
+
+
+def _check_mask(bm, docs, window):
+    kv_num, kv_idx, full_num, full_idx = oracle.prefill_block_mask(docs, BLOCK, window)
+    g_kv_num = bm.kv_num_blocks.cpu().numpy()
+    g_full_num = bm.full_kv_num_blocks.cpu().numpy()
+    g_kv = bm.kv_indices.cpu().numpy()
+    g_full = bm.full_kv_indices.cpu().numpy()
+    assert np.array_equal(g_kv_num, kv_num) and np.array_equal(g_full_num, full_num)
+    for qb in range(len(kv_num)):
+        assert list(g_kv[qb, :kv_num[qb]]) == kv_idx[qb], qb
+        assert list(g_full[qb, :full_num[qb]]) == full_idx[qb], qb
+
+
+@pytest.mark.parametrize("L,kind,window", [
+    (1, "one", 0), (63, "one", 0), (64, "one", 0), (65, "interleaved", 0),
+    (300, "contiguous", 0), (777, "interleaved", 0), (200, "one", 64), (777, "contiguous", 37),
+    (1000, "interleaved", 130), (4100, "many", 0), (9000, "many", 0), (9000, "many", 512),
+    (8400, "interleaved", 0)])
+def test_block_mask_equals_oracle(dev, L, kind, window):
+    rng = np.random.default_rng(L + window)
+    docs = _docs(rng, kind, L)
+    bm = pkv.prefill_block_mask(torch.from_numpy(docs).to(dev), window)
+    torch.cuda.synchronize()
+    _check_mask(bm, docs, window)
+
+
+def _run(dev, q, k, v, docs, window, scale, bm=None):
+    Hq, L, D = q.shape
+    if bm is None:
+        bm = pkv.prefill_block_mask(torch.from_numpy(docs).to(dev), window)
+    out = torch.full((Hq, L, D), float("nan"), dtype=torch.bfloat16, device=dev)
+    pkv.prefill_attn(q.to(dev), k.to(dev), v.to(dev), bm, scale, out)
+    torch.cuda.synchronize()
+    return out, bm
+
+
+def _compare(got, ref, v):
+    assert np.isfinite(got).all()
+    e = np.abs(got - ref)
+    bound = 2.0 ** -8 * float(np.abs(v.double().numpy()).max()) + 2e-3
+    assert e.max() <= bound and e.mean() <= 1e-3, (float(e.max()), bound, float(e.mean()))
+
+
+@pytest.mark.parametrize("L,Hq,Hkv,D,kind,window", [
+    (300, 8, 2, 128, "contiguous", 0), (257, 4, 4, 64, "interleaved", 0),
+    (64, 8, 1, 128, "one", 0), (1, 2, 1, 64, "one", 0), (65, 4, 2, 128, "interleaved", 0),
+    (777, 16, 4, 128, "contiguous", 0), (200, 6, 3, 64, "contiguous", 0),
+    (300, 4, 1, 128, "one", 100), (500, 4, 2, 64, "contiguous", 64),
+    (257, 4, 2, 128, "interleaved", 7), (640, 8, 2, 128, "many", 0)])
+def test_prefill_attention_parity(dev, L, Hq, Hkv, D, kind, window):
+    rng = np.random.default_rng(L * 10 + D + Hq + window)
+    q = wl.randn_bf16(rng, (Hq, L, D))
+    k = wl.randn_bf16(rng, (Hkv, L, D))
+    v = wl.randn_bf16(rng, (Hkv, L, D))
+    docs = _docs(rng, kind, L)
+    scale = D ** -0.5
+    out, _ = _run(dev, q, k, v, docs, window, scale)
+    ref = oracle.prefill_attention(q.double().numpy(), k.double().numpy(), v.double().numpy(),
+                                   docs, scale, window=window)
+    _compare(f64(out), ref, v)
+
+
+def test_prefill_full_size_sampled_documents(dev):
+    """The benchmark's launch: 64 packed prompts of U[100, 400] tokens, 32 q /
+    8 kv heads, head_dim 128. A document's rows depend on its own tokens only
+    (pinned in the oracle tests), so whole documents are checked against the
+    oracle run on that document alone: the first, one in the middle and the
+    last."""
+    rng = np.random.default_rng(77)
+    lens = wl.uniform_lengths(rng, 64, 100, 400)
+    docs = np.repeat(np.arange(64), lens).astype(np.int32)
+    L, Hq, Hkv, D = len(docs), 32, 8, 128
+    q = wl.randn_bf16(rng, (Hq, L, D))
+    k = wl.randn_bf16(rng, (Hkv, L, D))
+    v = wl.randn_bf16(rng, (Hkv, L, D))
+    scale = D ** -0.5
+    out, bm = _run(dev, q, k, v, docs, 0, scale)
+    _check_mask(bm, docs, 0)
+    got = f64(out)
+    starts = np.r_[0, np.cumsum(lens)]
+    for d in (0, 31, 63):
+        sl = slice(int(starts[d]), int(starts[d + 1]))
+        ref = oracle.prefill_attention(q[:, sl].double().numpy(), k[:, sl].double().numpy(),
+                                       v[:, sl].double().numpy(), docs[sl], scale)
+        _compare(got[:, sl], ref, v)
+
+
+def test_prefill_mask_lists_are_bounds_safe(dev):
+    """List entries outside [0, n) are skipped (the output is bit-identical to
+    the unmodified mask's), and a query block whose lists are empty gets
+    zeros."""
+    rng = np.random.default_rng(5)
+    L, Hq, Hkv, D = 300, 4, 2, 128
+    q = wl.randn_bf16(rng, (Hq, L, D))
+    k = wl.randn_bf16(rng, (Hkv, L, D))
+    v = wl.randn_bf16(rng, (Hkv, L, D))
+    docs = _docs(rng, "contiguous", L)
+    out, bm = _run(dev, q, k, v, docs, 0, 0.1)
+    n = bm.kv_num_blocks.numel()
+    kv_num = bm.kv_num_blocks.clone()
+    kv_idx = bm.kv_indices.clone()
+    for qb in range(n):
+        c = int(kv_num[qb])
+        if c + 2 <= n:
+            kv_idx[qb, c] = -3
+            kv_idx[qb, c + 1] = n + 5
+            kv_num[qb] = c + 2
+    bad = pkv.PrefillBlockMask(kv_num, kv_idx, bm.full_kv_num_blocks, bm.full_kv_indices,
+                               bm.docs, 0)
+    out2, _ = _run(dev, q, k, v, docs, 0, 0.1, bad)
+    assert torch.equal(out, out2)
+    empty = pkv.PrefillBlockMask(torch.zeros_like(kv_num), kv_idx,
+                                 torch.zeros_like(kv_num), bm.full_kv_indices, bm.docs, 0)
+    out3, _ = _run(dev, q, k, v, docs, 0, 0.1, empty)
+    assert torch.count_nonzero(out3) == 0
+
+
+def test_prefill_bad_arguments(dev):
+    docs = torch.zeros(8, dtype=torch.int32, device=dev)
+    bm = pkv.prefill_block_mask(docs)
+    q = torch.zeros((2, 8, 96), dtype=torch.bfloat16, device=dev)
+    with pytest.raises(pkv.BadArgError):       # D = 96 unsupported
+        pkv.prefill_attn(q, q, q, bm, 0.1, q.clone())
+    q = torch.zeros((3, 8, 64), dtype=torch.bfloat16, device=dev)
+    k = torch.zeros((2, 8, 64), dtype=torch.bfloat16, device=dev)
+    with pytest.raises(pkv.BadArgError):       # Hq % Hkv != 0
+        pkv.prefill_attn(q, k, k, bm, 0.1, q.clone())
+    with pytest.raises(pkv.BadArgError):       # negative window
+        pkv.prefill_block_mask(docs, -1)
+    q = torch.zeros((2, 9, 64), dtype=torch.bfloat16, device=dev)
+    with pytest.raises(pkv.BadArgError):       # mask built for another length
+        pkv.prefill_attn(q, q, q, bm, 0.1, q.clone())
