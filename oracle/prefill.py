@@ -41,7 +41,7 @@ def keep_matrix(docs, window: int = 0) -> np.ndarray:
     j = np.arange(L)[None, :]
     keep = (i >= j) & (docs[:, None] == docs[None, :])
     if window > 0:
-        keep &= (i - j) < window
+        keep &= j > i - window          # i - j < W, without an L x L integer temporary
     return keep
 
 
