@@ -546,9 +546,19 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
     fence_proxy_async();
   }
   // Warm L2 with the row metadata and the page table while the previous
-  // kernel finishes: prefetches only pull lines into L2 (the point of
-  // coherence), so they cannot observe stale data; the reads that count
-  // come after the grid dependency wait.
+  // kernel finishes (prefetches only pull lines into L2, the point of
+  // coherence).
+  //
+  // The set-up below (row cache, prefix sums, the producer's share of the
+  // cost line) runs before the grid dependency wait and reads only
+  // seq_lens, batch_idx and shared memory. That is safe because every kernel
+  // of this library releases its dependents only after its own wait has
+  // returned: when this grid starts, every launch before the immediately
+  // preceding one has completed, and the immediately preceding kernel of
+  // this library never writes seq_lens or batch_idx. A kernel that writes
+  // them and releases its dependents early must not be launched right
+  // before this one (the header states this). Global writes, the query and
+  // the cache come after the wait.
   {
     const int gt = blockIdx.x * kThreads + tid, gs = gridDim.x * kThreads;
     for (int i = gt * 32; i < p.B; i += gs * 32) {
@@ -559,8 +569,6 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
     const long long tlim = tbl < (1LL << 20) ? tbl : (1LL << 20);
     for (long long i = 32LL * gt; i < tlim; i += 32LL * gs) prefetch_l2(p.table + i);
   }
-  pkv_wait_prior_grid();
-  pkv_allow_next_grid();
   for (int b = tid; b < p.B; b += kThreads) {
     const RowInfo r = row_info(p, b, err, blockIdx.x == 0);
     rows[b] = make_int2(r.n_tiles > 0 ? r.slot : -1, r.L | (r.clamped ? kClampBit : 0));
@@ -587,7 +595,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
     __syncwarp();
   }
   __syncthreads();
-  UnitIter it0;
+  UnitIter it0, itp;
   {
     const int total = p.Hkv * pre[p.B];
     if (p.fixed_splits == 0) {
@@ -604,6 +612,15 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
       it0.pos = static_cast<int>(1LL * total * blockIdx.x / gridDim.x);
       it0.end = static_cast<int>(1LL * total * (blockIdx.x + 1) / gridDim.x);
     }
+    itp = it0;   // the producer's share of the cost line (shared memory only)
+    if (warp == kCWarps && p.fixed_splits == 0) {
+      const int cost = p.Hkv * prc[p.B];
+      const long long c0 = 1LL * itp.qc * blockIdx.x, c1 = c0 + itp.qc;
+      locate_range(p, pre, prc, static_cast<int>(c0 < cost ? c0 : cost),
+                   static_cast<int>(c1 < cost ? c1 : cost), lane, itp);
+    }
+    pkv_wait_prior_grid();
+    pkv_allow_next_grid();
     if (parts_out) {  // parts per (row, kv head) for the combine, spread over the CTAs
       for (int rh = blockIdx.x + gridDim.x * tid; rh < p.B * p.Hkv; rh += gridDim.x * kThreads) {
         const int b = rh / p.Hkv, g = rh - b * p.Hkv;
@@ -689,16 +706,10 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
       }
       return ((u.g * p.n_pages + page) << p.log2_ps) + (key & (ps - 1));
     };
-    UnitIter it = it0;
+    UnitIter it = itp;
     Unit w, wn;
     int it_k = 0, it_v = 0, it_q = 0;
     bool ok = true;
-    if (p.fixed_splits == 0) {
-      const int cost = p.Hkv * prc[p.B];
-      const long long c0 = 1LL * it.qc * blockIdx.x, c1 = c0 + it.qc;
-      locate_range(p, pre, prc, static_cast<int>(c0 < cost ? c0 : cost),
-                   static_cast<int>(c1 < cost ? c1 : cost), lane, it);
-    }
     bool have = next_unit(p, rows, pre, prc, it, w, lane);
     int page_first = have ? box_page(w, lane) : -1;
     while (ok && have) {
