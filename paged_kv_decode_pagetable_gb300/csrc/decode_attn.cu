@@ -619,10 +619,14 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
       locate_range(p, pre, prc, static_cast<int>(c0 < cost ? c0 : cost),
                    static_cast<int>(c1 < cost ? c1 : cost), lane, itp);
     }
-    pkv_wait_prior_grid();
-    pkv_allow_next_grid();
-    if (parts_out) {  // parts per (row, kv head) for the combine, spread over the CTAs
-      for (int rh = blockIdx.x + gridDim.x * tid; rh < p.B * p.Hkv; rh += gridDim.x * kThreads) {
+    // the consumer warps wait here; the producer warp also looks up its first
+    // unit and that unit's pages first, and waits just before its first copy
+    if (warp < kCWarps) {
+      pkv_wait_prior_grid();
+      pkv_allow_next_grid();
+    }
+    if (parts_out && warp < kCWarps) {  // parts per (row, kv head) for the combine
+      for (int rh = blockIdx.x + gridDim.x * tid; rh < p.B * p.Hkv; rh += gridDim.x * kCThreads) {
         const int b = rh / p.Hkv, g = rh - b * p.Hkv;
         const int n = pre[b + 1] - pre[b];
         int parts = n;
@@ -712,6 +716,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
     bool ok = true;
     bool have = next_unit(p, rows, pre, prc, it, w, lane);
     int page_first = have ? box_page(w, lane) : -1;
+    pkv_wait_prior_grid();
     while (ok && have) {
       bool have_next = false, looked_ahead = false;
       int page_next = -1;
