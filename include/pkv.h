@@ -25,14 +25,13 @@
  *     and read per-step metadata (positions, lengths, table) from device
  *     memory, so a fixed-shape call can be captured in a CUDA graph.
  *   - Kernels are launched with programmatic dependent launch: each waits
- *     for the kernel before it (griddepcontrol.wait) and only then lets the
- *     next one start, so in-stream order is kept. The decode attention and
- *     the fused step read seq_lens and batch_idx BEFORE that wait, to plan
- *     their work while the previous kernel drains. So seq_lens and
- *     batch_idx must not be written by the kernel launched immediately
- *     before them when that kernel itself lets its dependents start early.
- *     Copies, ordinary kernels, and the kernels of this library (which
- *     never write them) are all fine there.
+ *     for the kernel before it (griddepcontrol.wait) before it touches
+ *     memory that kernel may write, so in-stream order is kept. The decode
+ *     attention and the fused step read seq_lens, batch_idx and the page
+ *     table BEFORE that wait, to plan their work while earlier kernels
+ *     drain. So those three must be written by copies or by kernels that do
+ *     not let their dependents start early (ordinary kernels); none of this
+ *     library's kernels writes them.
  *   - Device-side faults are never raised on purpose: an invalid index read
  *     from device memory sets a bit in the caller's int32 error word
  *     (atomic OR) and the access is skipped.

@@ -550,15 +550,17 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
   // coherence).
   //
   // The set-up below (row cache, prefix sums, the producer's share of the
-  // cost line) runs before the grid dependency wait and reads only
-  // seq_lens, batch_idx and shared memory. That is safe because every kernel
-  // of this library releases its dependents only after its own wait has
-  // returned: when this grid starts, every launch before the immediately
-  // preceding one has completed, and the immediately preceding kernel of
-  // this library never writes seq_lens or batch_idx. A kernel that writes
-  // them and releases its dependents early must not be launched right
-  // before this one (the header states this). Global writes, the query and
-  // the cache come after the wait.
+  // cost line and its first unit's page entries) runs before the grid
+  // dependency wait and reads only seq_lens, batch_idx, the page table and
+  // shared memory. That is safe because the kernels that may still be
+  // running when this grid starts never write those: a kernel without
+  // programmatic launch completes before its successor starts; the kernels
+  // of this library release their dependents only after their own wait
+  // returned, except the combine, which releases them at once and writes
+  // only its output (so at most the combine and the attention kernel before
+  // it can still be running). A kernel that writes them and releases its
+  // dependents early must not precede this one (the header states this).
+  // Global writes, the query and the cache come after the wait.
   {
     const int gt = blockIdx.x * kThreads + tid, gs = gridDim.x * kThreads;
     for (int i = gt * 32; i < p.B; i += gs * 32) {
@@ -1216,8 +1218,11 @@ __global__ void combine_kernel(const float *__restrict__ o_part,
                                const int *__restrict__ parts_in, const Problem p,
                                __nv_bfloat16 *__restrict__ out) {
   constexpr int CH = (D + 127) / 128;   // float4 column chunks per lane
-  pkv_wait_prior_grid();
+  // The next kernel may start (and plan) as soon as every CTA of this grid
+  // is running; it waits for this grid to complete before it touches the
+  // workspace or the output.
   pkv_allow_next_grid();
+  pkv_wait_prior_grid();
   const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (r >= p.B * p.Hq) return;
