@@ -30,7 +30,10 @@
 // zero-filled), the block index two tiles ahead read early. Per tile the warp
 // computes S = Q K^T, masks partial tiles (causal, document, window, inside
 // L), keeps an online softmax in the exp2 domain and adds P V, with P taken
-// straight from the S accumulators as the A operand. The CTAs of the last
+// straight from the S accumulators as the A operand. In a partial tile each
+// warp skips the 16-key groups that cannot hold a kept pair for any of its 16
+// rows (after its last row, outside the window, or with document ids outside
+// its rows' range): half of a diagonal tile's work on average. The CTAs of the last
 // query blocks are scheduled first.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -52,11 +55,18 @@ struct PCfg {
   static constexpr int ROWB = D * 2;
   static constexpr int CH = D / 8;              // 16-byte chunks per row
   static constexpr int TILE = kBN * ROWB;
-  static constexpr int OFF_K = kBM * ROWB;      // Q tile at 0
+  // K buffers 0 and 1, then V buffers 0 and 1. The Q tile (kBM == kBN rows)
+  // shares K buffer 1: it is read into registers before that buffer's first
+  // fill.
+  static constexpr int OFF_K = 0;
+  static constexpr int OFF_Q = TILE;
   static constexpr int OFF_V = OFF_K + 2 * TILE;
   static constexpr int OFF_DQ = OFF_V + 2 * TILE;        // int [kBM]
   static constexpr int OFF_DK = OFF_DQ + kBM * 4;        // int [2][kBN]
   static constexpr int SMEM = OFF_DK + 2 * kBN * 4;
+  // CTAs per SM the launch bounds ask for: registers and shared memory allow
+  // 3 at D = 128 (66 KB each) and 4 at D = 64
+  static constexpr int MIN_CTAS = D == 128 ? 3 : 4;
 };
 
 __device__ __forceinline__ uint32_t p_smem(const void *p) {
@@ -229,7 +239,7 @@ __global__ void __launch_bounds__(kMThreads)
 // Attention
 // ---------------------------------------------------------------------------
 template <int D>
-__global__ void __launch_bounds__(kPThreads)
+__global__ void __launch_bounds__(kPThreads, PCfg<D>::MIN_CTAS)
     prefill_attn_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
                         const __nv_bfloat16 *__restrict__ v, const int32_t *__restrict__ docs,
                         const int32_t *__restrict__ kv_num, const int32_t *__restrict__ kv_idx,
@@ -251,7 +261,7 @@ __global__ void __launch_bounds__(kPThreads)
   const __nv_bfloat16 *qh = q + static_cast<size_t>(h) * L * D;
   const __nv_bfloat16 *kh = k + static_cast<size_t>(g) * L * D;
   const __nv_bfloat16 *vh = v + static_cast<size_t>(g) * L * D;
-  const uint32_t sQ = p_smem(psm), sK = sQ + C::OFF_K, sV = sQ + C::OFF_V;
+  const uint32_t s0 = p_smem(psm), sQ = s0 + C::OFF_Q, sK = s0 + C::OFF_K, sV = s0 + C::OFF_V;
   int *dq = reinterpret_cast<int *>(psm + C::OFF_DQ);
   int *dk = reinterpret_cast<int *>(psm + C::OFF_DK);
 
@@ -281,42 +291,93 @@ __global__ void __launch_bounds__(kPThreads)
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
   const int qi0 = row0 + warp * 16 + gid, qi1 = qi0 + 8;
   int dq0 = 0, dq1 = 0;
+  // this warp's rows inside L and the range of their document ids
+  const int rlo = row0 + warp * 16, rhi = min(rlo + 15, L - 1);
+  int wdlo = 2147483647, wdhi = -2147483647 - 1;
   if (total == 0) cp_wait<0>();
 
   for (int t = 0; t < total; ++t) {
     const int nn = t + 2 < total ? block_at(t + 2) : -1;   // read two tiles ahead
     const int buf = t & 1;
-    if (t + 1 < total) {   // the next key tile into the other buffer
-      const int nb = buf ^ 1;
-      load_tile<D>(sK + nb * C::TILE, kh, max(nxt, 0) * kBN, L, dk + nb * kBN, docs, tid);
-      load_tile<D>(sV + nb * C::TILE, vh, max(nxt, 0) * kBN, L, dk + nb * kBN, docs, tid);
-      cp_commit();
-      cp_wait<1>();
+    if (t > 0) {
+      if (t + 1 < total) {   // the next key tile into the other buffer
+        const int nb = buf ^ 1;
+        load_tile<D>(sK + nb * C::TILE, kh, max(nxt, 0) * kBN, L, dk + nb * kBN, docs, tid);
+        load_tile<D>(sV + nb * C::TILE, vh, max(nxt, 0) * kBN, L, dk + nb * kBN, docs, tid);
+        cp_commit();
+        cp_wait<1>();
+      } else {
+        cp_wait<0>();
+      }
+      __syncthreads();
     } else {
+      // Q and the first tile; Q goes to registers, then K buffer 1 (where Q
+      // sits) takes the second tile
       cp_wait<0>();
-    }
-    __syncthreads();
-    if (t == 0) {
+      __syncthreads();
 #pragma unroll
       for (int ks = 0; ks < KS; ++ks)
         p_ldsm_x4(sQ + p_swz<D>(warp * 16 + (lane & 15), 2 * ks + (lane >> 4)), qa[ks][0],
                   qa[ks][1], qa[ks][2], qa[ks][3]);
       dq0 = dq[warp * 16 + gid];
       dq1 = dq[warp * 16 + gid + 8];
+      const int dr = (lane & 15) <= rhi - rlo ? dq[warp * 16 + (lane & 15)] : dq[warp * 16];
+      wdlo = dr;
+      wdhi = dr;
+#pragma unroll
+      for (int o = 1; o < 16; o <<= 1) {
+        wdlo = min(wdlo, __shfl_xor_sync(0xffffffffu, wdlo, o));
+        wdhi = max(wdhi, __shfl_xor_sync(0xffffffffu, wdhi, o));
+      }
+      __syncthreads();   // every warp holds its Q fragments
+      if (total > 1) {
+        load_tile<D>(sK + C::TILE, kh, max(nxt, 0) * kBN, L, dk + kBN, docs, tid);
+        load_tile<D>(sV + C::TILE, vh, max(nxt, 0) * kBN, L, dk + kBN, docs, tid);
+        cp_commit();
+      }
     }
     const int *dkt = dk + buf * kBN;
-    if (cur >= 0) {
-      const bool full = t < fn;
-      const int j0 = cur * kBN;
+    const bool full = t < fn;
+    const int j0 = cur * kBN;
+    // 16-key groups of this tile that may hold a kept pair for one of this
+    // warp's rows (bit g: keys j0 + 16g .. j0 + 16g + 15); a group whose keys
+    // all come after the warp's last row, all fall outside the window, lie
+    // past L, or whose document ids miss the rows' id range adds nothing
+    int act = 0;
+    if (cur >= 0 && rlo < L) {
+      act = 0xf;
+      if (!full) {
+        int lo0 = dkt[lane], hi0 = lo0, lo1 = dkt[lane + 32], hi1 = lo1;
+#pragma unroll
+        for (int o = 1; o < 16; o <<= 1) {   // within each half-warp
+          lo0 = min(lo0, __shfl_xor_sync(0xffffffffu, lo0, o));
+          hi0 = max(hi0, __shfl_xor_sync(0xffffffffu, hi0, o));
+          lo1 = min(lo1, __shfl_xor_sync(0xffffffffu, lo1, o));
+          hi1 = max(hi1, __shfl_xor_sync(0xffffffffu, hi1, o));
+        }
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          const int src = (g & 1) << 4;
+          const int glo = __shfl_sync(0xffffffffu, g < 2 ? lo0 : lo1, src);
+          const int ghi = __shfl_sync(0xffffffffu, g < 2 ? hi0 : hi1, src);
+          const int kf = j0 + 16 * g;
+          const bool may = kf <= rhi && (window == 0 || kf + 15 > rlo - window) &&
+                           ghi >= wdlo && glo <= wdhi;
+          if (!may) act &= ~(1 << g);
+        }
+      }
+    }
+    if (act) {
       const uint32_t kb = sK + buf * C::TILE, vb = sV + buf * C::TILE;
-      // ---- S = Q K^T: 16 rows x 64 keys per warp ----
+      // ---- S = Q K^T: 16 rows x 64 keys per warp, active key groups only ----
       float s[8][4];
 #pragma unroll
       for (int n = 0; n < 8; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
 #pragma unroll
-      for (int ks = 0; ks < KS; ++ks) {
+      for (int np = 0; np < 4; ++np) {
+        if (!((act >> np) & 1)) continue;
 #pragma unroll
-        for (int np = 0; np < 4; ++np) {
+        for (int ks = 0; ks < KS; ++ks) {
           uint32_t b0, b1, b2, b3;
           p_ldsm_x4(kb + p_swz<D>(np * 16 + (lane & 7) + ((lane >> 4) << 3),
                                   2 * ks + ((lane >> 3) & 1)),
@@ -334,7 +395,9 @@ __global__ void __launch_bounds__(kPThreads)
         for (int e = 0; e < 2; ++e) {
           const int kl = n * 8 + 2 * tig + e, key = j0 + kl;
           bool v0 = true, v1 = true;
-          if (!full) {
+          if (!((act >> (n >> 1)) & 1)) {
+            v0 = v1 = false;
+          } else if (!full) {
             const int dkey = dkt[kl];
             v0 = key <= qi0 && key < L && dkey == dq0 && (window == 0 || qi0 - key < window);
             v1 = key <= qi1 && key < L && dkey == dq1 && (window == 0 || qi1 - key < window);
@@ -376,15 +439,16 @@ __global__ void __launch_bounds__(kPThreads)
       }
       // ---- O += P V: P from the S accumulators, V^T fragments by ldmatrix.trans ----
 #pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        const uint32_t a0 = p_pack(s[2 * t][0], s[2 * t][1]);
-        const uint32_t a1 = p_pack(s[2 * t][2], s[2 * t][3]);
-        const uint32_t a2 = p_pack(s[2 * t + 1][0], s[2 * t + 1][1]);
-        const uint32_t a3 = p_pack(s[2 * t + 1][2], s[2 * t + 1][3]);
+      for (int kq = 0; kq < 4; ++kq) {
+        if (!((act >> kq) & 1)) continue;   // P is zero there
+        const uint32_t a0 = p_pack(s[2 * kq][0], s[2 * kq][1]);
+        const uint32_t a1 = p_pack(s[2 * kq][2], s[2 * kq][3]);
+        const uint32_t a2 = p_pack(s[2 * kq + 1][0], s[2 * kq + 1][1]);
+        const uint32_t a3 = p_pack(s[2 * kq + 1][2], s[2 * kq + 1][3]);
 #pragma unroll
         for (int dp = 0; dp < NO / 2; ++dp) {
           uint32_t b0, b1, b2, b3;
-          p_ldsm_x4_t(vb + p_swz<D>(t * 16 + (lane & 7) + (((lane >> 3) & 1) << 3),
+          p_ldsm_x4_t(vb + p_swz<D>(kq * 16 + (lane & 7) + (((lane >> 3) & 1) << 3),
                                     2 * dp + (lane >> 4)),
                       b0, b1, b2, b3);
           p_mma(o[2 * dp], a0, a1, a2, a3, b0, b1);
