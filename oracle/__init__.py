@@ -9,6 +9,8 @@ computes, written from the pages' statement of the method:
   * ``norm_rope``  — per-head RMSNorm followed by rotate-half RoPE;
   * ``attention``  — GQA decode attention over a gathered, contiguous K/V
     with length and sliding-window masking, plus its log-sum-exp.
+  * ``block_mask`` — logical -> physical conversion of a block mask's kv
+    indices through the page table;
   * ``prefill``    — document-causal (optionally sliding) attention over packed
     prefill tokens, and its block mask (full / partial key blocks).
 
@@ -27,12 +29,13 @@ from .paged_kv import (physical_row, kv_append, gather_pages,
 from .norm_rope import rms_norm, rope, qk_norm_rope, inv_freq, v_norm
 from .attention import decode_attention, decode_attention_row
 from .prefill import prefill_attention, prefill_block_mask, keep_matrix
+from .block_mask import convert_logical_block_mask
 
 __all__ = [
     "PageTableModel", "NoSlot", "NoPages", "BadSlot", "BadArg", "PageTableError",
     "physical_row", "kv_append", "gather_pages",
     "ERR_POS", "ERR_PAGE_RANGE", "ERR_PAGE_NEG", "ERR_SLOT",
     "rms_norm", "rope", "qk_norm_rope", "inv_freq", "v_norm", "prefill_attention",
-    "prefill_block_mask", "keep_matrix",
+    "prefill_block_mask", "keep_matrix", "convert_logical_block_mask",
     "decode_attention", "decode_attention_row",
 ]
