@@ -291,6 +291,30 @@ int paged_decode_step_ex(const pkv_bf16 *q, const pkv_bf16 *k, const pkv_bf16 *v
                          pkv_bf16 *out, int32_t *err_word, void *stream);
 
 /* ---------------------------------------------------------------------
+ * convert_logical_block_mask — re-points a block mask built over logical
+ * positions at the paged cache ([P3] PageTable.convert_logical_block_mask):
+ *   new_kv_indices[b][h][r][c] = table[slot_b][kv_indices[b][h][r][c]]
+ *       for c < max_blocks, and 0 for max_blocks <= c < n_cols,
+ * slot_b = batch_idx[b] (batch_idx NULL: slot_b = b). The key-block size of
+ * the mask must equal page_size (the caller's contract, as on the pages).
+ * kv_indices: int32 [B][H][rows][max_blocks]; new_kv_indices: int32
+ * [B][H][rows][n_cols], n_cols >= max_blocks (the pages use the table
+ * width). The block counts are unchanged (reuse them); convert full and
+ * partial index arrays with one call each. Device pointers, caller-owned.
+ * Table entries are copied as they are (-1 for an unreserved block). An
+ * index outside [0, max_pages_per_seq) gives -1 and PKV_ERR_POS; a slot
+ * outside [0, n_slots) gives -1 for all of that row's entries and
+ * PKV_ERR_SLOT (err_word may be NULL). One kernel. Errors: PKV_E_BAD_ARG
+ * for a bad shape or a NULL pointer, PKV_E_CUDA on a launch failure.
+ * ------------------------------------------------------------------- */
+int convert_logical_block_mask(const int32_t *dev_table, int n_slots,
+                               int max_pages_per_seq, const int32_t *batch_idx,
+                               int B, int H, int rows, int max_blocks,
+                               const int32_t *kv_indices, int n_cols,
+                               int32_t *new_kv_indices, int32_t *err_word,
+                               void *stream);
+
+/* ---------------------------------------------------------------------
  * Document-causal prefill attention over L packed prompt tokens
  * ([P3] PagedKVCache.create_prefill_blockmask_no_paging; the sliding
  * variant is [P1] _create_prefill_sliding_blockmask): docs[t] is the

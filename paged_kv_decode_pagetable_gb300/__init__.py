@@ -80,6 +80,8 @@ _SIGS = {
     "kv_append_prefill": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_int, _c_p, _c_int, _c_int, _c_int,
                                    _c_int, _c_p, _c_p, _c_int, _c_int, _c_p, _c_p]),
     "prefill_block_mask": (_c_int, [_c_p, _c_int, _c_int, _c_p, _c_p, _c_p, _c_p, _c_p]),
+    "convert_logical_block_mask": (_c_int, [_c_p, _c_int, _c_int, _c_p, _c_int, _c_int, _c_int,
+                                            _c_int, _c_p, _c_int, _c_p, _c_p, _c_p]),
     "prefill_attn": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_int, _c_int,
                               _c_int, _c_int, _c_int, _c_f, _c_p, _c_p]),
     "qk_norm_rope": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_p, _c_f, _c_f, _c_int, _c_int,
@@ -450,6 +452,25 @@ def paged_decode_attn_noalloc(q, k_cache, v_cache, dev_table, n_slots, max_pages
         page_size, n_pages, _ptr(batch_idx), _ptr(seq_lens), int(window), float(scale), B, Hq,
         Hkv, D, int(num_splits), _ptr(out), _ptr(err_word), _stream(stream)),
         "paged_decode_attn_noalloc")
+
+
+def convert_logical_block_mask(kv_indices, dev_table, n_slots, max_pages_per_seq,
+                               batch_idx=None, n_cols=None, err_word=None, stream=None):
+    """Logical -> physical key-block indices of a block mask (int32
+    [B][H][rows][max_blocks], device) through the page table; returns int32
+    [B][H][rows][n_cols] (n_cols defaults to max(max_blocks, max_pages_per_seq))."""
+    _i32(kv_indices, "kv_indices"), _i32(dev_table, "dev_table"), _i32(batch_idx, "batch_idx")
+    if kv_indices.dim() != 4:
+        raise BadArgError("kv_indices must be [B][H][rows][max_blocks]")
+    B, H, R, M = kv_indices.shape
+    if n_cols is None:
+        n_cols = max(M, max_pages_per_seq)
+    out = torch.empty((B, H, R, n_cols), dtype=torch.int32, device=kv_indices.device)
+    _check(load_library().convert_logical_block_mask(
+        _ptr(dev_table), n_slots, max_pages_per_seq, _ptr(batch_idx), B, H, R, M,
+        _ptr(kv_indices), n_cols, _ptr(out), _ptr(err_word), _stream(stream)),
+        "convert_logical_block_mask")
+    return out
 
 
 PREFILL_BLOCK = 64
