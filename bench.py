@@ -680,7 +680,7 @@ def run_prefill(args, world, rank, local):
                        "parallelism": f"replicas x{world}"},
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
                          "unit": "TFLOP/s", "frac": achieved / peak, "peak_kind": peak_kind,
-                         "kernel": "prefill_attn_kernel<128> (mma.sync)", "traffic": None},
+                         "kernel": "prefill_tc_kernel<128> (tcgen05)", "traffic": None},
             "cpu_baseline": cpu, "gpu_launches": K, "clocks": clocks}), flush=True)
 
 

@@ -354,10 +354,13 @@ int prefill_block_mask(const int32_t *docs, int L, int window,
  * visited, partial ones masked by the rule above, full ones unmasked (a
  * block listed as full that is not makes its pairs count as kept; list
  * entries outside [0, n) are skipped, so no list can make a read go out of
- * bounds). A row with no visited key gets zeros. Requires D in {64, 128},
- * Hq % Hkv == 0, Hq <= 65535, 16-byte aligned q, k, v, out, scale finite
- * and > 0. One kernel; no workspace. Errors: PKV_E_BAD_ARG for the above
- * or a NULL pointer, PKV_E_CUDA on a launch failure. */
+ * bounds; the lists are expected ascending, as prefill_block_mask writes
+ * them). A row with no visited key gets zeros. Requires D in {64, 128},
+ * Hq % Hkv == 0, Hq <= 65535, 16-byte aligned q, k, v, out and docs, scale
+ * finite and > 0. One kernel (tcgen05 MMAs with TMEM accumulators, one
+ * persistent CTA per SM over work items of 128 query rows and one head); no
+ * workspace. Errors: PKV_E_BAD_ARG for the above or a NULL pointer,
+ * PKV_E_CUDA on a launch failure. */
 int prefill_attn(const pkv_bf16 *q, const pkv_bf16 *k, const pkv_bf16 *v,
                  const int32_t *docs, const int32_t *kv_num_blocks,
                  const int32_t *kv_indices, const int32_t *full_kv_num_blocks,

@@ -21,6 +21,14 @@ int ok();
 // Number of SMs of the current device (cached per device; 0 if unknown).
 int sm_count();
 
+// Document-causal prefill attention on tcgen05 (prefill_tc.cu), D in {64, 128};
+// arguments already validated by the public entry point.
+template <int D>
+int launch_prefill_tc(const pkv_bf16 *q, const pkv_bf16 *k, const pkv_bf16 *v,
+                      const int32_t *docs, const int32_t *kv_num, const int32_t *kv_idx,
+                      const int32_t *full_num, const int32_t *full_idx, int L, int Hq, int Hkv,
+                      int window, float scale, pkv_bf16 *out, cudaStream_t s);
+
 inline bool aligned16(const void *p) {
   return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
 }

@@ -1,0 +1,769 @@
+// prefill_attn on the 5th-generation tensor cores (tcgen05, TMEM, TMA).
+//
+// Same operation and block mask as prefill_attn.cu's header states
+// ("unsloth: compare main...transformers-continuous-batching-qwen3" ·
+// flex_paged_attention.py · create_prefill_blockmask_no_paging, and the
+// sliding variant of the Gemma-4 script): query i keeps key j iff j <= i,
+// docs[j] == docs[i] and, with W > 0, i - j < W.
+//
+// Design: a persistent kernel, one CTA per SM, walking work
+// items of (128 query rows = two 64-row query blocks, query head).
+//   warp 16 (producer, one lane): per item, the Q tile by TMA (3-D map
+//     {column, token, head}: rows past L read zeros), then the union of the
+//     two query blocks' key-block lists (merged on the fly, ascending), each
+//     key block's K and V tiles and its 64 document ids by TMA into a
+//     3-stage ring, with a small descriptor (block, full / first / last
+//     flags) in the stage.
+//   warp 17 (MMA, one lane): S = Q K^T into one of two TMEM buffers
+//     (M = 128, N = 64, K-major SW128 operands), then, one tile behind,
+//     O += P V into TMEM (P K-major from shared memory, V MN-major).
+//   warps 0-15 (softmax): warps w, w + 4, w + 8, w + 12 share the 32 query
+//     rows of TMEM lanes 32(w%4)..32(w%4)+31, one row per thread, and split
+//     the 64 keys of a tile and the D columns of O in quarters. S from TMEM, masks on
+//     partial blocks, the row maximum combined through shared memory, online
+//     softmax in the exp2 domain with lazy rescaling (O in TMEM is rescaled
+//     only when a row's maximum grows by more than 2^8), P as bf16 into a
+//     swizzled shared buffer for the next MMA, and at an item's end O / l
+//     to global memory.
+// Every wait on an mbarrier is bounded; a wait that gives up sets an abort
+// flag, every role leaves its loop, and the rows of unfinished items are
+// written as NaN, so a fault never passes silently.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cmath>
+#include <mutex>
+
+#include "pkv_internal.h"
+
+namespace {
+
+constexpr int kQR = 128;      // query rows per work item
+constexpr int kKB = 64;       // keys per tile (the block mask's block)
+constexpr int kNS = 3;        // K/V ring stages
+constexpr int kSplit = 4;                  // softmax warps per TMEM lane group
+constexpr int kSoftWarps = 4 * kSplit;     // each: 32 rows x 16 keys of a tile
+constexpr int kKW = 64 / kSplit;           // keys per softmax warp
+constexpr int kProdWarp = kSoftWarps, kMmaWarp = kSoftWarps + 1;
+constexpr int kTCThreads = (kSoftWarps + 2) * 32;
+constexpr int kSpin = 1 << 22;
+constexpr float kLazyLog2 = 8.f;   // rescale O only when a row maximum grows past 2^8
+
+// tile descriptor flags
+constexpr int kFull = 1, kFirst = 2, kLast = 4, kMaskAll = 8;
+
+template <int D>
+struct TC {
+  static constexpr int ATOMS = D / 64;              // 128-byte (64-column) swizzle atoms
+  static constexpr int Q_ATOM = kQR * 128;          // bytes of one atom of the Q tile
+  static constexpr int KV_ATOM = kKB * 128;
+  static constexpr int Q_BYTES = ATOMS * Q_ATOM;
+  static constexpr int KV_BYTES = ATOMS * KV_ATOM;
+  static constexpr int P_BYTES = kQR * kKB * 2;
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_K = OFF_Q + Q_BYTES;
+  static constexpr int OFF_V = OFF_K + kNS * KV_BYTES;
+  static constexpr int OFF_P = OFF_V + kNS * KV_BYTES;
+  static constexpr int OFF_SD = OFF_P + 2 * P_BYTES;          // int [kNS][64] key documents
+  static constexpr int OFF_XCH = OFF_SD + kNS * kKB * 4;       // float [2][kSplit][128 rows]
+  static constexpr int OFF_META = OFF_XCH + 2 * kSplit * kQR * 4;  // int4 [kNS]
+  static constexpr int OFF_BAR = OFF_META + kNS * 16;
+  // qfull, qempty, kvfull[NS], kvempty[NS], sfull[2], sfree[2], pfull[2], pvdone[2],
+  // ofree[2] (per O buffer, so that no waiter can fall two phases behind),
+  // drain, xbar[4] (the softmax groups' exchanges)
+  static constexpr int N_BAR = 2 + 2 * kNS + 2 + 2 + 2 + 2 + 2 + 1 + 4;
+  static constexpr int OFF_MISC = OFF_BAR + N_BAR * 8;       // tmem address, abort flag
+  static constexpr int SMEM = OFF_MISC + 16 + 1024;          // + slack to align to 1024
+  static constexpr int TMEM_COLS = 512;   // S[2] (2 x 64) + O[2] (2 x 128): items alternate O
+  static constexpr int S_COL = 0, O_COL = 128, O_STRIDE = 128;
+  static constexpr int CTAS_PER_SM = 1;
+  static_assert(OFF_P % 1024 == 0 && OFF_K % 1024 == 0 && OFF_V % 1024 == 0, "atom alignment");
+  static_assert(OFF_SD % 128 == 0, "TMA destination alignment");
+  static_assert(SMEM <= 232448 / CTAS_PER_SM, "shared memory per SM");
+};
+
+// ---- PTX wrappers ----------------------------------------------------------
+__device__ __forceinline__ uint32_t t_smem(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void t_bar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
+}
+__device__ __forceinline__ void t_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void t_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+// waits for completion number k (0, 1, ...) of the barrier's phases; false
+// if it gave up (the abort flag is then raised for everyone)
+__device__ __forceinline__ bool t_wait(uint32_t bar, int k, volatile int *abort_flag) {
+  const uint32_t parity = static_cast<uint32_t>(k) & 1u;
+  for (int i = 0; i < kSpin; ++i) {
+    uint32_t done;
+    asm volatile(
+        "{\n.reg .pred q;\nmbarrier.try_wait.parity.shared::cta.b64 q, [%1], %2;\n"
+        "selp.u32 %0, 1, 0, q;\n}\n"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    if (done) return true;
+    if ((i & 63) == 63 && *abort_flag) return false;
+  }
+  *abort_flag = 1;
+  return false;
+}
+// the same, by every lane of a warp, with one verdict for the warp (so the
+// warp-collective TMEM accesses that follow are never reached by part of it)
+__device__ __forceinline__ bool t_wait_warp(uint32_t bar, int k, volatile int *abort_flag) {
+  return __all_sync(0xffffffffu, t_wait(bar, k, abort_flag));
+}
+// bounded wait that ignores the abort flag (used to drain the tensor core
+// before the TMEM is released)
+__device__ __forceinline__ void t_wait_drain(uint32_t bar) {
+  for (int i = 0; i < kSpin; ++i) {
+    uint32_t done;
+    asm volatile(
+        "{\n.reg .pred q;\nmbarrier.try_wait.parity.shared::cta.b64 q, [%1], 0;\n"
+        "selp.u32 %0, 1, 0, q;\n}\n"
+        : "=r"(done)
+        : "r"(bar)
+        : "memory");
+    if (done) return;
+  }
+}
+__device__ __forceinline__ void t_tma_1d(uint32_t dst, const CUtensorMap *tm, int x, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.1d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2}], [%3];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void t_tma_3d(uint32_t dst, const CUtensorMap *tm, int x, int y, int z,
+                                         uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
+}
+// shared-memory matrix descriptor: SW128 atoms, version 1
+__device__ __forceinline__ uint64_t t_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu) |
+         (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
+         (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (static_cast<uint64_t>(1) << 46) |
+         (static_cast<uint64_t>(2) << 61);
+}
+// instruction descriptor, kind::f16: f32 accumulator, bf16 A and B, A
+// K-major, B K-major (b_mn = 0) or MN-major (b_mn = 1), M = 128
+__host__ __device__ constexpr uint32_t t_idesc(int N, int b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(b_mn) << 16) |
+         (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(kQR >> 4) << 24);
+}
+__device__ __forceinline__ void t_mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                      uint32_t accumulate) {
+  asm volatile(
+      "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
+}
+__device__ __forceinline__ void t_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   bar)
+               : "memory");
+}
+__device__ __forceinline__ void t_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void t_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void t_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void t_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15]));
+}
+__device__ __forceinline__ void t_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void t_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t t_pack(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t *>(&v);
+}
+
+struct Item {
+  int row0, h;
+};
+// work item i of n_items, the last query tiles first; items of one query
+// tile are consecutive over the heads
+__device__ __forceinline__ Item item_of(int i, int n2, int Hq) {
+  Item it;
+  const int ct = n2 - 1 - i / Hq;
+  it.row0 = ct * kQR;
+  it.h = i - (i / Hq) * Hq;
+  return it;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kTCThreads, TC<D>::CTAS_PER_SM)
+    prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
+                      const __grid_constant__ CUtensorMap tmK,
+                      const __grid_constant__ CUtensorMap tmV,
+                      const __grid_constant__ CUtensorMap tmD, const int32_t *__restrict__ docs,
+                      const int32_t *__restrict__ kv_num, const int32_t *__restrict__ kv_idx,
+                      const int32_t *__restrict__ full_num,
+                      const int32_t *__restrict__ full_idx, int nblk, int L, int Hq, int G,
+                      int window, float scale_log2, __nv_bfloat16 *__restrict__ out) {
+  using C = TC<D>;
+  extern __shared__ uint8_t tc_raw[];
+  uint8_t *sm = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(tc_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t sQ = t_smem(sm + C::OFF_Q), sK = t_smem(sm + C::OFF_K),
+                 sV = t_smem(sm + C::OFF_V), sP = t_smem(sm + C::OFF_P),
+                 sD = t_smem(sm + C::OFF_SD);
+  int4 *meta = reinterpret_cast<int4 *>(sm + C::OFF_META);
+  const uint32_t bar0 = t_smem(sm + C::OFF_BAR);
+  const uint32_t qfull = bar0, qempty = bar0 + 8, kvfull = bar0 + 16,
+                 kvempty = kvfull + 8 * kNS, sfull = kvempty + 8 * kNS, sfree = sfull + 16,
+                 pfull = sfree + 16, pvdone = pfull + 16, ofree = pvdone + 16, drain = ofree + 16,
+                 xbar = drain + 8;
+  uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + C::OFF_MISC);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + C::OFF_MISC + 4);
+
+  if (tid == 0) {
+    t_bar_init(qfull, 1);
+    t_bar_init(qempty, 1);
+    for (int i = 0; i < kNS; ++i) {
+      t_bar_init(kvfull + 8 * i, 1);
+      t_bar_init(kvempty + 8 * i, 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      t_bar_init(sfull + 8 * i, 1);
+      t_bar_init(sfree + 8 * i, kSoftWarps);
+      t_bar_init(pfull + 8 * i, kSoftWarps);
+      t_bar_init(pvdone + 8 * i, 1);
+    }
+    t_bar_init(ofree, kSoftWarps);
+    t_bar_init(ofree + 8, kSoftWarps);
+    t_bar_init(drain, 1);
+    for (int i = 0; i < 4; ++i) t_bar_init(xbar + 8 * i, kSplit);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     t_smem(tslot)),
+                 "r"(C::TMEM_COLS));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  t_fence_before();
+  __syncthreads();
+  t_fence_after();
+  const uint32_t tmem = *tslot;
+  pkv_wait_prior_grid();
+  pkv_allow_next_grid();
+
+  const int n2 = (nblk + 1) / 2;
+  const int n_items = n2 * Hq;
+
+  if (warp == kProdWarp) {
+    // ============================ producer ============================
+    if (lane == 0) {
+      int g = 0, it = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++it) {
+        const Item w = item_of(item, n2, Hq);
+        const int hk = w.h / G;
+        if (it > 0 && !t_wait(qempty, it - 1, abort_flag)) break;
+        t_expect_tx(qfull, C::Q_BYTES);
+#pragma unroll
+        for (int a = 0; a < C::ATOMS; ++a) t_tma_3d(sQ + a * C::Q_ATOM, &tmQ, 64 * a, w.row0, w.h, qfull);
+        // the union of the two query blocks' lists, ascending
+        const int qb0 = w.row0 / kKB, qb1 = qb0 + 1;
+        const bool has1 = qb1 < nblk;
+        const int32_t *lf0 = full_idx + static_cast<size_t>(qb0) * nblk;
+        const int32_t *lp0 = kv_idx + static_cast<size_t>(qb0) * nblk;
+        const int32_t *lf1 = has1 ? full_idx + static_cast<size_t>(qb1) * nblk : lf0;
+        const int32_t *lp1 = has1 ? kv_idx + static_cast<size_t>(qb1) * nblk : lp0;
+        const int cf0 = min(max(full_num[qb0], 0), nblk), cp0 = min(max(kv_num[qb0], 0), nblk);
+        const int cf1 = has1 ? min(max(full_num[qb1], 0), nblk) : 0;
+        const int cp1 = has1 ? min(max(kv_num[qb1], 0), nblk) : 0;
+        int i0 = 0, i1 = 0, i2 = 0, i3 = 0;
+        auto head = [&](const int32_t *a, int cnt, int &i) -> int {
+          while (i < cnt) {
+            const int x = a[i];
+            if (x >= 0 && x < nblk) return x;
+            ++i;
+          }
+          return INT_MAX;
+        };
+        int pend = -1, pend_flags = 0, emitted = 0;
+        auto emit = [&](int kb, int flags) -> bool {
+          const int s = g % kNS;
+          if (g >= kNS && !t_wait(kvempty + 8 * s, g / kNS - 1, abort_flag)) return false;
+          meta[s] = make_int4(kb, flags, w.row0, w.h);
+          t_expect_tx(kvfull + 8 * s, 2 * C::KV_BYTES + kKB * 4);
+          t_tma_1d(sD + s * kKB * 4, &tmD, kb * kKB, kvfull + 8 * s);   // past L: zeros
+#pragma unroll
+          for (int a = 0; a < C::ATOMS; ++a) {
+            t_tma_3d(sK + s * C::KV_BYTES + a * C::KV_ATOM, &tmK, 64 * a, kb * kKB, hk,
+                     kvfull + 8 * s);
+            t_tma_3d(sV + s * C::KV_BYTES + a * C::KV_ATOM, &tmV, 64 * a, kb * kKB, hk,
+                     kvfull + 8 * s);
+          }
+          ++g;
+          return true;
+        };
+        while (ok) {
+          const int h0 = head(lf0, cf0, i0), h1 = head(lp0, cp0, i1);
+          const int h2 = head(lf1, cf1, i2), h3 = head(lp1, cp1, i3);
+          const int kb = min(min(h0, h1), min(h2, h3));
+          if (kb == INT_MAX) break;
+          const bool in_f0 = h0 == kb, in_f1 = h2 == kb;
+          if (h0 == kb) ++i0;
+          if (h1 == kb) ++i1;
+          if (h2 == kb) ++i2;
+          if (h3 == kb) ++i3;
+          const int flags = (in_f0 && (!has1 || in_f1)) ? kFull : 0;
+          if (pend >= 0) {
+            ok = emit(pend, pend_flags | (emitted == 0 ? kFirst : 0));
+            ++emitted;
+          }
+          pend = kb;
+          pend_flags = flags;
+        }
+        if (!ok) break;
+        if (pend < 0) {   // no listed block: one fully masked tile, so the rows get zeros
+          pend = 0;
+          pend_flags = kMaskAll;
+        }
+        ok = emit(pend, pend_flags | kLast | (emitted == 0 ? kFirst : 0));
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ============================== MMA ===============================
+    if (lane == 0) {
+      constexpr uint32_t idS = t_idesc(kKB, 0), idO = t_idesc(D, 1);
+      int g = 0, it = 0, pv_item = 0, prev_flags = 0;
+      bool ok = true, pv_pending = false;
+      // P V of tile gp into O[item & 1]; an item's first one overwrites that
+      // buffer, once the epilogue of the item two back has read it
+      auto do_pv = [&](int gp, int flags) -> bool {
+        const int bp = gp & 1, sp = gp % kNS;
+        if (!t_wait(pfull + 8 * bp, gp >> 1, abort_flag)) return false;
+        if ((flags & kFirst) && pv_item > 1 &&
+            !t_wait(ofree + 8 * (pv_item & 1), (pv_item - 2) >> 1, abort_flag))
+          return false;
+        t_fence_after();
+        const uint32_t ocol = C::O_COL + C::O_STRIDE * (pv_item & 1);
+#pragma unroll
+        for (int k = 0; k < kKB / 16; ++k) {
+          const uint64_t a = t_desc(sP + bp * C::P_BYTES + k * 32, 16, 1024);
+          const uint64_t b = t_desc(sV + sp * C::KV_BYTES + k * 2048, C::KV_ATOM, 1024);
+          t_mma(tmem + ocol, a, b, idO, (k > 0 || !(flags & kFirst)) ? 1u : 0u);
+        }
+        t_commit(pvdone + 8 * bp);
+        t_commit(kvempty + 8 * sp);
+        if (flags & kLast) ++pv_item;
+        return true;
+      };
+      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++it) {
+        if (!t_wait(qfull, it, abort_flag)) break;
+        int flags = 0;
+        do {
+          const int s = g % kNS, b = g & 1;
+          if (!t_wait(kvfull + 8 * s, g / kNS, abort_flag)) {
+            ok = false;
+            break;
+          }
+          flags = meta[s].y;
+          if (g >= 2 && !t_wait(sfree + 8 * b, (g >> 1) - 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          t_fence_after();
+#pragma unroll
+          for (int k = 0; k < D / 16; ++k) {
+            const uint64_t a = t_desc(sQ + (k >> 2) * C::Q_ATOM + (k & 3) * 32, 16, 1024);
+            const uint64_t bd =
+                t_desc(sK + s * C::KV_BYTES + (k >> 2) * C::KV_ATOM + (k & 3) * 32, 16, 1024);
+            t_mma(tmem + C::S_COL + b * kKB, a, bd, idS, k > 0 ? 1u : 0u);
+          }
+          t_commit(sfull + 8 * b);
+          if (flags & kLast) t_commit(qempty);
+          // P V one tile behind S (across items too: the next item's first S
+          // goes in before the previous item's last P V)
+          if (pv_pending && !do_pv(g - 1, prev_flags)) {
+            ok = false;
+            break;
+          }
+          pv_pending = true;
+          prev_flags = flags;
+          ++g;
+        } while (!(flags & kLast));
+      }
+      if (ok && pv_pending) do_pv(g - 1, prev_flags);
+      // every issued MMA completes before the TMEM is released
+      t_commit(drain);
+      t_wait_drain(drain);
+    }
+  } else {
+    // ============================ softmax =============================
+    const int lg = warp & 3, hf = warp >> 2;          // lane group, key / column quarter
+    const int row = 32 * lg + lane;
+    const uint32_t trow = tmem + (static_cast<uint32_t>(32 * lg) << 16);
+    float *xch = reinterpret_cast<float *>(sm + C::OFF_XCH);   // [2 slots][kSplit][128]
+    // exchange number xn of the group (the kSplit warps on these rows): each
+    // publishes a per-row value, all wait (bounded) for the group's arrivals
+    // and read every value; slots alternate, so a slot is rewritten only
+    // after every member has read it
+    int xn = 0;
+    auto exchange = [&](float mine, float (&all)[kSplit]) -> bool {
+      const int slot = xn & 1;
+      xch[(slot * kSplit + hf) * kQR + row] = mine;
+      __syncwarp();
+      if (lane == 0) t_arrive(xbar + 8 * lg);
+      if (!t_wait_warp(xbar + 8 * lg, xn, abort_flag)) return false;
+#pragma unroll
+      for (int q = 0; q < kSplit; ++q) all[q] = xch[(slot * kSplit + q) * kQR + row];
+      ++xn;
+      return true;
+    };
+    constexpr int OH = D / kSplit;                                // O columns of this warp
+    // the epilogue of an item (O / l to global memory) runs after the next
+    // item's first tile, when that item's last P V is long done
+    bool ep = false;
+    int ep_g = 0, ep_it = 0, ep_qi = 0, ep_h = 0;
+    float ep_il = 0.f;
+    auto epilogue = [&]() -> bool {
+      if (!t_wait_warp(pvdone + 8 * (ep_g & 1), ep_g >> 1, abort_flag)) return false;
+      t_fence_after();
+      const bool valid = ep_qi < L;
+      const uint32_t ocol = C::O_COL + C::O_STRIDE * (ep_it & 1) + OH * hf;
+      __nv_bfloat16 *orow = out + (static_cast<size_t>(ep_h) * L + (valid ? ep_qi : 0)) * D + OH * hf;
+      const float il = ep_il;
+#pragma unroll
+      for (int c = 0; c < OH / 16; ++c) {
+        uint32_t r[16];
+        t_ld16(trow + ocol + 16 * c, r);
+        t_wait_ld();
+        if (valid) {
+          uint4 v0, v1;
+          v0.x = t_pack(__uint_as_float(r[0]) * il, __uint_as_float(r[1]) * il);
+          v0.y = t_pack(__uint_as_float(r[2]) * il, __uint_as_float(r[3]) * il);
+          v0.z = t_pack(__uint_as_float(r[4]) * il, __uint_as_float(r[5]) * il);
+          v0.w = t_pack(__uint_as_float(r[6]) * il, __uint_as_float(r[7]) * il);
+          v1.x = t_pack(__uint_as_float(r[8]) * il, __uint_as_float(r[9]) * il);
+          v1.y = t_pack(__uint_as_float(r[10]) * il, __uint_as_float(r[11]) * il);
+          v1.z = t_pack(__uint_as_float(r[12]) * il, __uint_as_float(r[13]) * il);
+          v1.w = t_pack(__uint_as_float(r[14]) * il, __uint_as_float(r[15]) * il);
+          *reinterpret_cast<uint4 *>(orow + 16 * c) = v0;
+          *reinterpret_cast<uint4 *>(orow + 16 * c + 8) = v1;
+        }
+      }
+      t_fence_before();
+      __syncwarp();
+      if (lane == 0) t_arrive(ofree + 8 * (ep_it & 1));
+      ep = false;
+      return true;
+    };
+    int g = 0, it = -1;
+    bool ok = true;
+    for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+      ++it;
+      const Item w = item_of(item, n2, Hq);
+      const uint32_t ocol_it = C::O_COL + C::O_STRIDE * (it & 1) + OH * hf;
+      const int qi = w.row0 + row;
+      const bool valid = qi < L;
+      const int dq = valid ? docs[qi] : 0;
+      float m = -INFINITY, l = 0.f;   // l: this half's share of the row sum
+      int flags = 0;
+      do {
+        const int s = g % kNS, b = g & 1;
+        if (!t_wait_warp(kvfull + 8 * s, g / kNS, abort_flag)) {
+          ok = false;
+          break;
+        }
+        const int4 md = meta[s];
+        flags = md.y;
+        const int j0 = md.x * kKB + kKW * hf;   // first key of this warp
+        const bool partial = !(flags & kFull);
+        if (!t_wait_warp(sfull + 8 * b, g >> 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        const int *dks = reinterpret_cast<const int *>(sm + C::OFF_SD) + s * kKB + kKW * hf;
+        t_fence_after();
+        float sv[kKW];
+        {
+          uint32_t r[16];
+          t_ld16(trow + C::S_COL + b * kKB + kKW * hf, r);
+          t_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) sv[j] = __uint_as_float(r[j]);
+        }
+        t_fence_before();   // S buffer b may be overwritten from here
+        __syncwarp();
+        if (lane == 0) t_arrive(sfree + 8 * b);
+        if (flags & kMaskAll) {
+#pragma unroll
+          for (int c = 0; c < kKW; ++c) sv[c] = -INFINITY;
+        } else if (partial) {
+#pragma unroll
+          for (int c = 0; c < kKW; ++c) {
+            const int key = j0 + c;
+            const bool keep = valid && key <= qi && key < L && dks[c] == dq &&
+                              (window == 0 || qi - key < window);
+            sv[c] = keep ? sv[c] : -INFINITY;
+          }
+        }
+        // raw-score maximum of this warp's keys (four chains), then of the row
+        float x0 = sv[0], x1 = sv[1], x2 = sv[2], x3 = sv[3];
+#pragma unroll
+        for (int c = 4; c < kKW; c += 4) {
+          x0 = fmaxf(x0, sv[c]);
+          x1 = fmaxf(x1, sv[c + 1]);
+          x2 = fmaxf(x2, sv[c + 2]);
+          x3 = fmaxf(x3, sv[c + 3]);
+        }
+        float mall[kSplit];
+        if (!exchange(fmaxf(fmaxf(x0, x1), fmaxf(x2, x3)), mall)) {
+          ok = false;
+          break;
+        }
+        float mraw = mall[0];
+#pragma unroll
+        for (int q = 1; q < kSplit; ++q) mraw = fmaxf(mraw, mall[q]);
+        const float mt = mraw * scale_log2;   // -inf stays -inf (scale > 0)
+        // lazy online softmax: a stale maximum is kept unless the new one
+        // exceeds it by more than 2^8 (O and l use the same maximum, so the
+        // result is exact either way); the group's warps decide alike
+        float alpha = 1.f;
+        bool resc = false;
+        if (mt != -INFINITY) {
+          if (m == -INFINITY) {
+            m = mt;
+          } else if (mt > m + kLazyLog2) {
+            alpha = exp2f(m - mt);
+            m = mt;
+            resc = true;
+          }
+        }
+        const float mneg = m == -INFINITY ? 0.f : -m;
+        float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+        for (int c = 0; c < kKW; c += 4) {   // masked scores are -inf: exp2 gives 0
+          sv[c] = exp2f(fmaf(sv[c], scale_log2, mneg));
+          sv[c + 1] = exp2f(fmaf(sv[c + 1], scale_log2, mneg));
+          sv[c + 2] = exp2f(fmaf(sv[c + 2], scale_log2, mneg));
+          sv[c + 3] = exp2f(fmaf(sv[c + 3], scale_log2, mneg));
+          s0 += sv[c];
+          s1 += sv[c + 1];
+          s2 += sv[c + 2];
+          s3 += sv[c + 3];
+        }
+        l = l * alpha + ((s0 + s1) + (s2 + s3));
+        if (__any_sync(0xffffffffu, resc)) {   // this warp's columns of O *= alpha
+          if (!t_wait_warp(pvdone + 8 * ((g - 1) & 1), (g - 1) >> 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          t_fence_after();
+#pragma unroll
+          for (int c = 0; c < OH / 16; ++c) {
+            uint32_t r[16];
+            t_ld16(trow + ocol_it + 16 * c, r);
+            t_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * alpha);
+            t_st16(trow + ocol_it + 16 * c, r);
+          }
+          t_wait_st();
+        }
+        // P into buffer b (free once the P V of tile g - 2 is done): this
+        // warp's 16 keys are 16-byte chunks 2 hf and 2 hf + 1 of the row
+        if (g >= 2 && !t_wait_warp(pvdone + 8 * b, (g >> 1) - 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        {
+          uint8_t *prow = sm + C::OFF_P + b * C::P_BYTES + row * 128;
+#pragma unroll
+          for (int q4 = 0; q4 < kKW / 8; ++q4) {
+            const int ch = (kKW / 8) * hf + q4;
+            uint4 v;
+            v.x = t_pack(sv[8 * q4 + 0], sv[8 * q4 + 1]);
+            v.y = t_pack(sv[8 * q4 + 2], sv[8 * q4 + 3]);
+            v.z = t_pack(sv[8 * q4 + 4], sv[8 * q4 + 5]);
+            v.w = t_pack(sv[8 * q4 + 6], sv[8 * q4 + 7]);
+            *reinterpret_cast<uint4 *>(prow + ((ch ^ (row & 7)) << 4)) = v;
+          }
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        t_fence_before();
+        __syncwarp();
+        if (lane == 0) t_arrive(pfull + 8 * b);
+        if (ep && !epilogue()) {   // the previous item's output
+          ok = false;
+          break;
+        }
+        if (flags & kLast) {   // this item's row sum; its output comes after the next tile
+          float lall[kSplit];
+          if (!exchange(l, lall)) {
+            ok = false;
+            break;
+          }
+          float lt = lall[0];   // the same order in every warp of the group
+#pragma unroll
+          for (int q = 1; q < kSplit; ++q) lt += lall[q];
+          ep = true;
+          ep_g = g;
+          ep_it = it;
+          ep_qi = qi;
+          ep_h = w.h;
+          ep_il = lt > 0.f ? 1.f / lt : 0.f;
+        }
+        ++g;
+      } while (!(flags & kLast));
+    }
+    if (ok && ep && !epilogue()) ok = false;
+    if (!ok || *abort_flag) {   // a wait gave up: mark this CTA's rows as failed
+      for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+        const Item w = item_of(item, n2, Hq);
+        const int qi = w.row0 + row;
+        if (qi >= L) continue;
+        __nv_bfloat16 *orow = out + (static_cast<size_t>(w.h) * L + qi) * D + OH * hf;
+        for (int c = 0; c < OH; ++c) orow[c] = __float2bfloat16_rn(NAN);
+      }
+    }
+  }
+  t_fence_before();
+  __syncthreads();
+  t_fence_after();
+  if (warp == 0)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(C::TMEM_COLS));
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                   CUtensorMapFloatOOBfill);
+
+EncodeTiledFn tc_encode_fn() {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  std::call_once(once, [] {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult qr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                         cudaEnableDefault, &qr) == cudaSuccess &&
+        qr == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+// 1-D map over the int32 document ids, 64-id boxes; ids past L read zeros
+int docs_map(CUtensorMap *tm, const int32_t *docs, int L) {
+  EncodeTiledFn fn = tc_encode_fn();
+  if (!fn) return pkv::fail(PKV_E_CUDA, "cuTensorMapEncodeTiled unavailable");
+  cuuint64_t dims[1] = {static_cast<cuuint64_t>(L)};
+  cuuint64_t strides[1] = {0};
+  cuuint32_t box[1] = {static_cast<cuuint32_t>(kKB)};
+  cuuint32_t estr[1] = {1u};
+  CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_INT32, 1, const_cast<int32_t *>(docs), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return pkv::fail(PKV_E_CUDA, "cuTensorMapEncodeTiled (docs) failed (%d)", static_cast<int>(r));
+  return PKV_OK;
+}
+
+// 3-D map {column, token, head} over a [heads][L][D] bf16 tensor with
+// [box_rows][64] boxes, 128-byte swizzle; tokens past L read zeros
+int head_map(CUtensorMap *tm, const void *base, int heads, int L, int D, int box_rows) {
+  EncodeTiledFn fn = tc_encode_fn();
+  if (!fn) return pkv::fail(PKV_E_CUDA, "cuTensorMapEncodeTiled unavailable");
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(L),
+                        static_cast<cuuint64_t>(heads)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(D) * 2 * L};
+  cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(box_rows), 1u};
+  cuuint32_t estr[3] = {1u, 1u, 1u};
+  CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return pkv::fail(PKV_E_CUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+  return PKV_OK;
+}
+
+}  // namespace
+
+// Launch of the tcgen05 prefill kernel (declared in pkv_internal.h); the
+// public entry point prefill_attn validates the arguments first.
+namespace pkv {
+template <int D>
+int launch_prefill_tc(const pkv_bf16 *q, const pkv_bf16 *k, const pkv_bf16 *v,
+                      const int32_t *docs, const int32_t *kv_num, const int32_t *kv_idx,
+                      const int32_t *full_num, const int32_t *full_idx, int L, int Hq, int Hkv,
+                      int window, float scale, pkv_bf16 *out, cudaStream_t s) {
+  static std::mutex mu;
+  static bool done[64] = {false};
+  int dev = 0;
+  PKV_CUDA_CHECK(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= 64) return pkv::fail(PKV_E_CUDA, "device id out of range");
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!done[dev]) {
+      PKV_CUDA_CHECK(cudaFuncSetAttribute(prefill_tc_kernel<D>,
+                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          TC<D>::SMEM));
+      done[dev] = true;
+    }
+  }
+  CUtensorMap tmQ, tmK, tmV, tmD;
+  int st = head_map(&tmQ, q, Hq, L, D, kQR);
+  if (st == PKV_OK) st = head_map(&tmK, k, Hkv, L, D, kKB);
+  if (st == PKV_OK) st = head_map(&tmV, v, Hkv, L, D, kKB);
+  if (st == PKV_OK) st = docs_map(&tmD, docs, L);
+  if (st != PKV_OK) return st;
+  const int n = (L + kKB - 1) / kKB;
+  const long long items = 1LL * ((n + 1) / 2) * Hq;
+  const long long cap = 1LL * TC<D>::CTAS_PER_SM * pkv::sm_count();
+  const int grid = static_cast<int>(items < cap ? items : cap);
+  PKV_CUDA_CHECK(pkv::launch_pdl(prefill_tc_kernel<D>, dim3(grid), dim3(kTCThreads), TC<D>::SMEM,
+                                 s, tmQ, tmK, tmV, tmD, docs, kv_num, kv_idx, full_num, full_idx, n, L,
+                                 Hq, Hq / Hkv, window, scale * 1.4426950408889634f,
+                                 reinterpret_cast<__nv_bfloat16 *>(out)));
+  return PKV_OK;
+}
+template int launch_prefill_tc<64>(const pkv_bf16 *, const pkv_bf16 *, const pkv_bf16 *,
+                                   const int32_t *, const int32_t *, const int32_t *,
+                                   const int32_t *, const int32_t *, int, int, int, int, float,
+                                   pkv_bf16 *, cudaStream_t);
+template int launch_prefill_tc<128>(const pkv_bf16 *, const pkv_bf16 *, const pkv_bf16 *,
+                                    const int32_t *, const int32_t *, const int32_t *,
+                                    const int32_t *, const int32_t *, int, int, int, int, float,
+                                    pkv_bf16 *, cudaStream_t);
+}  // namespace pkv
