@@ -67,7 +67,7 @@ def parse_args():
     ap.add_argument("--layers", type=int, default=0,
                     help="layer caches to cycle (0: enough for 4x L2)")
     ap.add_argument("--workload", default="rollout",
-                    choices=sorted(list(WORKLOAD_CHOICES) + ["prefill"]),
+                    choices=sorted(list(WORKLOAD_CHOICES) + ["prefill", "prefill-long"]),
                     help="rollout (the headline line) or one of the static decode layers")
     return ap.parse_args()
 
@@ -565,9 +565,13 @@ def run_e2e(args, w, spec, engine, pkv, caches, n_layers, tables, bidx, pos, len
             "eager_value": byts / (ms_eager * 1e-3) / 1e9, "eager_ms_per_step": ms_eager / n}
 
 
-def prefill_docs(n_docs: int = 64, seed_salt: int = 31):
+def prefill_docs(long: bool = False, n_docs: int = 64, seed_salt: int = 31):
     """Packed prefill: n_docs prompts with the rollout's admission lengths
-    U[100, 400], laid one after another (document id per token)."""
+    U[100, 400] (long: 8 documents of 2048 tokens), laid one after another
+    (document id per token)."""
+    if long:
+        lens = np.full(8, 2048, dtype=np.int64)
+        return np.repeat(np.arange(8), lens).astype(np.int32), lens
     rng = np.random.default_rng(wl.ROLLOUT.seed(seed_salt))
     lens = wl.uniform_lengths(rng, n_docs, 100, 400)
     return np.repeat(np.arange(n_docs), lens).astype(np.int32), lens
@@ -592,7 +596,8 @@ def run_prefill(args, world, rank, local):
     dev = torch.device("cuda", local)
     pkv.load_library()
     Hq, Hkv, D = 32, 8, 128
-    docs, lens = prefill_docs()
+    long = args.workload == "prefill-long"
+    docs, lens = prefill_docs(long)
     L = len(docs)
     g = torch.Generator(device=dev)
     g.manual_seed(wl.ROLLOUT.seed(rank + 40))
@@ -653,7 +658,7 @@ def run_prefill(args, world, rank, local):
     cpu = None
     if rank == 0 and world == 1:
         import oracle
-        n = 3                                      # a bounded sample: the first 3 documents
+        n = 1 if long else 3                       # a bounded sample: the first documents
         end = int(np.sum(lens[:n]))
         qs = sets[0][0][:, :end].float().cpu().numpy()
         ks = sets[0][1][:, :end].float().cpu().numpy()
@@ -670,9 +675,11 @@ def run_prefill(args, world, rank, local):
             "unit": "TFLOP/s", "n_gpus": world, "steps": K, "warmup": W, "ms_per_step": ms / K,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
-            "config": {"workload": f"packed prefill: 64 prompts U[100,400] ({L} tokens), "
-                                   "32 q / 8 kv heads, head_dim 128",
-                       "global_batch": 64 * world, "tokens": L, "flops_per_call": flops,
+            "config": {"workload": (f"packed prefill: 8 documents of 2048 tokens ({L} tokens), "
+                                    if long else
+                                    f"packed prefill: 64 prompts U[100,400] ({L} tokens), ")
+                                   + "32 q / 8 kv heads, head_dim 128",
+                       "global_batch": len(lens) * world, "tokens": L, "flops_per_call": flops,
                        "visited_blocks_per_head": n_blocks,
                        "block_flops_per_call": 4.0 * 64 * 64 * D * Hq * n_blocks,
                        "block_mask_us": mask_us, "attn_us_per_call": ms * 1e3 / K,
@@ -690,7 +697,7 @@ def main():
     try:
         if args.impl == "reference":
             run_reference(args, world, rank)
-        elif args.workload == "prefill":
+        elif args.workload in ("prefill", "prefill-long"):
             run_prefill(args, world, rank, local)
         else:
             run_ours(args, world, rank, local)
