@@ -234,8 +234,9 @@ __global__ void __launch_bounds__(kTCThreads, TC<D>::CTAS_PER_SM)
                       int window, float scale_log2, __nv_bfloat16 *__restrict__ out) {
   using C = TC<D>;
   extern __shared__ uint8_t tc_raw[];
-  uint8_t *sm = reinterpret_cast<uint8_t *>(
-      (reinterpret_cast<uintptr_t>(tc_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  // 1024-byte aligned base, by offsetting the shared array itself (an integer
+  // round trip would hide the state space and turn every access generic)
+  uint8_t *sm = tc_raw + ((1024u - (t_smem(tc_raw) & 1023u)) & 1023u);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t sQ = t_smem(sm + C::OFF_Q), sK = t_smem(sm + C::OFF_K),
                  sV = t_smem(sm + C::OFF_V), sP = t_smem(sm + C::OFF_P),
