@@ -51,8 +51,10 @@ constexpr int kTCThreads = (kSoftWarps + 2) * 32;
 constexpr int kSpin = 1 << 22;
 constexpr float kLazyLog2 = 8.f;   // rescale O only when a row maximum grows past 2^8
 
-// tile descriptor flags
-constexpr int kFull = 1, kFirst = 2, kLast = 4, kMaskAll = 8;
+// tile descriptor flags; kNeed0 / kNeed1: the block is listed for the
+// item's first / second 64-row query block (rows of a block that does not
+// list it keep nothing there)
+constexpr int kFull = 1, kFirst = 2, kLast = 4, kMaskAll = 8, kNeed0 = 16, kNeed1 = 32;
 
 template <int D>
 struct TC {
@@ -340,11 +342,12 @@ __global__ void __launch_bounds__(kTCThreads, TC<D>::CTAS_PER_SM)
           const int kb = min(min(h0, h1), min(h2, h3));
           if (kb == INT_MAX) break;
           const bool in_f0 = h0 == kb, in_f1 = h2 == kb;
+          const int need = (h0 == kb || h1 == kb ? kNeed0 : 0) | (h2 == kb || h3 == kb ? kNeed1 : 0);
           if (h0 == kb) ++i0;
           if (h1 == kb) ++i1;
           if (h2 == kb) ++i2;
           if (h3 == kb) ++i3;
-          const int flags = (in_f0 && (!has1 || in_f1)) ? kFull : 0;
+          const int flags = ((in_f0 && (!has1 || in_f1)) ? kFull : 0) | need;
           if (pend >= 0) {
             ok = emit(pend, pend_flags | (emitted == 0 ? kFirst : 0));
             ++emitted;
@@ -525,6 +528,22 @@ __global__ void __launch_bounds__(kTCThreads, TC<D>::CTAS_PER_SM)
         t_fence_before();   // S buffer b may be overwritten from here
         __syncwarp();
         if (lane == 0) t_arrive(sfree + 8 * b);
+        // a block not listed for this lane group's query block keeps nothing
+        // for its rows: P = 0 there, no exchange, no softmax update (all warps
+        // of the group take this branch together)
+        const bool need = (flags & (lg < 2 ? kNeed0 : kNeed1)) != 0;
+        if (!need) {
+          if (g >= 2 && !t_wait_warp(pvdone + 8 * b, (g >> 1) - 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          uint8_t *prow = sm + C::OFF_P + b * C::P_BYTES + row * 128;
+#pragma unroll
+          for (int q4 = 0; q4 < kKW / 8; ++q4) {
+            const int ch = (kKW / 8) * hf + q4;
+            *reinterpret_cast<uint4 *>(prow + ((ch ^ (row & 7)) << 4)) = make_uint4(0, 0, 0, 0);
+          }
+        } else {
         if (flags & kMaskAll) {
 #pragma unroll
           for (int c = 0; c < kKW; ++c) sv[c] = -INFINITY;
@@ -619,6 +638,7 @@ __global__ void __launch_bounds__(kTCThreads, TC<D>::CTAS_PER_SM)
             *reinterpret_cast<uint4 *>(prow + ((ch ^ (row & 7)) << 4)) = v;
           }
         }
+        }   // need
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         t_fence_before();
         __syncwarp();
