@@ -206,6 +206,13 @@ __device__ __forceinline__ void t_wait_ld() {
 __device__ __forceinline__ void t_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
+// 2^x on the MUFU unit (the PTX approximate instruction, subnormal results
+// flushed to zero: they are below what the bf16 P can hold anyway)
+__device__ __forceinline__ float t_ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 __device__ __forceinline__ uint32_t t_pack(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t *>(&v);
@@ -592,10 +599,10 @@ __global__ void __launch_bounds__(kTCThreads, TC<D>::CTAS_PER_SM)
         float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
 #pragma unroll
         for (int c = 0; c < kKW; c += 4) {   // masked scores are -inf: exp2 gives 0
-          sv[c] = exp2f(fmaf(sv[c], scale_log2, mneg));
-          sv[c + 1] = exp2f(fmaf(sv[c + 1], scale_log2, mneg));
-          sv[c + 2] = exp2f(fmaf(sv[c + 2], scale_log2, mneg));
-          sv[c + 3] = exp2f(fmaf(sv[c + 3], scale_log2, mneg));
+          sv[c] = t_ex2(fmaf(sv[c], scale_log2, mneg));
+          sv[c + 1] = t_ex2(fmaf(sv[c + 1], scale_log2, mneg));
+          sv[c + 2] = t_ex2(fmaf(sv[c + 2], scale_log2, mneg));
+          sv[c + 3] = t_ex2(fmaf(sv[c + 3], scale_log2, mneg));
           s0 += sv[c];
           s1 += sv[c + 1];
           s2 += sv[c + 2];
