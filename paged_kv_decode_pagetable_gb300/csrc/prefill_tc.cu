@@ -118,7 +118,7 @@ __device__ __forceinline__ bool t_wait(uint32_t bar, int k, volatile int *abort_
   *abort_flag = 1;
   return false;
 }
-// the same, by every lane of a warp, with one verdict for the warp (so the
+// the same, by every lane of a warp, with one result for the warp (so the
 // warp-collective TMEM accesses that follow are never reached by part of it)
 __device__ __forceinline__ bool t_wait_warp(uint32_t bar, int k, volatile int *abort_flag) {
   return __all_sync(0xffffffffu, t_wait(bar, k, abort_flag));
