@@ -178,3 +178,25 @@ def test_prefill_bad_arguments(dev):
     q = torch.zeros((2, 9, 64), dtype=torch.bfloat16, device=dev)
     with pytest.raises(pkv.BadArgError):       # mask built for another length
         pkv.prefill_attn(q, q, q, bm, 0.1, q.clone())
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_prefill_rising_scores_rescale_every_tile(dev, D):
+    """Scores that climb by about 16 (log2 units) per 64-key tile: every row's
+    maximum outgrows the kept one on each new tile, so the kernel rescales
+    its running output on every tile (the path random inputs rarely take)."""
+    rng = np.random.default_rng(90 + D)
+    L, Hq, Hkv = 700, 4, 2
+    base = wl.randn_bf16(rng, (D,)).double().numpy()
+    base = base / np.sqrt((base ** 2).sum()) * np.sqrt(D)          # |base|^2 = D
+    a = np.arange(L) / 64.0                                          # +1 per tile
+    q = torch.from_numpy(np.broadcast_to(base, (Hq, L, D)).copy()).to(torch.bfloat16)
+    k = torch.from_numpy((a[None, :, None] * base[None, None, :]).repeat(Hkv, 0)).to(torch.bfloat16)
+    v = wl.randn_bf16(rng, (Hkv, L, D))
+    docs = np.zeros(L, np.int32)
+    docs[400:] = 1
+    scale = D ** -0.5
+    out, _ = _run(dev, q, k, v, docs, 0, scale)
+    ref = oracle.prefill_attention(q.double().numpy(), k.double().numpy(), v.double().numpy(),
+                                   docs, scale)
+    _compare(f64(out), ref, v)
