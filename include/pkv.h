@@ -356,8 +356,8 @@ int prefill_block_mask(const int32_t *docs, int L, int window,
  * entries outside [0, n) are skipped, so no list can make a read go out of
  * bounds; the lists are expected ascending, as prefill_block_mask writes
  * them). A row with no visited key gets zeros. Requires D in {64, 128},
- * Hq % Hkv == 0, Hq <= 65535, 16-byte aligned q, k, v, out and docs, scale
- * finite and > 0. One kernel (tcgen05 MMAs with TMEM accumulators, one
+ * Hq % Hkv == 0, Hq <= 65535, ceil(L / 128) * Hq < 2^31, 16-byte aligned q,
+ * k, v, out and docs, scale finite and > 0. One kernel (tcgen05 MMAs with TMEM accumulators, one
  * persistent CTA per SM over work items of 128 query rows and one head); no
  * workspace. Errors: PKV_E_BAD_ARG for the above or a NULL pointer,
  * PKV_E_CUDA on a launch failure. */

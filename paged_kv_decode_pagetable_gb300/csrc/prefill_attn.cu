@@ -169,6 +169,9 @@ extern "C" int prefill_attn(const pkv_bf16 *q, const pkv_bf16 *k, const pkv_bf16
     return pkv::fail(PKV_E_BAD_ARG, "prefill_attn: need Hq %% Hkv == 0");
   if (L < 0 || L > 0x7fffffff - kBM || Hq > 65535 || window < 0)
     return pkv::fail(PKV_E_BAD_ARG, "prefill_attn: bad size or window");
+  // work items of 128 query rows and one head are counted in 32 bits
+  if (1LL * ((L + 2 * kBM - 1) / (2 * kBM)) * Hq > 0x7fffffffLL)
+    return pkv::fail(PKV_E_BAD_ARG, "prefill_attn: L x Hq too large");
   if (!(scale > 0.f) || !std::isfinite(scale))
     return pkv::fail(PKV_E_BAD_ARG, "prefill_attn: scale must be finite and > 0");
   if (L == 0) return pkv::ok();
