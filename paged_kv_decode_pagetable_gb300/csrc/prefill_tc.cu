@@ -554,6 +554,10 @@ __global__ void __launch_bounds__(kTCThreads, TC<D>::CTAS_PER_SM)
         if (flags & kMaskAll) {
 #pragma unroll
           for (int c = 0; c < kKW; ++c) sv[c] = -INFINITY;
+        } else if (partial && window == 0 && j0 + kKW <= w.row0 && valid) {
+          // keys all before the item's rows and inside L: the document test alone
+#pragma unroll
+          for (int c = 0; c < kKW; ++c) sv[c] = dks[c] == dq ? sv[c] : -INFINITY;
         } else if (partial) {
 #pragma unroll
           for (int c = 0; c < kKW; ++c) {
