@@ -561,9 +561,9 @@ __global__ void __launch_bounds__(kTCThreads, TC<D>::CTAS_PER_SM)
         } else if (partial) {
 #pragma unroll
           for (int c = 0; c < kKW; ++c) {
-            const int key = j0 + c;
-            const bool keep = valid && key <= qi && key < L && dks[c] == dq &&
-                              (window == 0 || qi - key < window);
+            const int key = j0 + c;   // every term evaluated: no branch per element
+            const bool keep = valid & (key <= qi) & (key < L) & (dks[c] == dq) &
+                              ((window == 0) | (qi - key < window));
             sv[c] = keep ? sv[c] : -INFINITY;
           }
         }
