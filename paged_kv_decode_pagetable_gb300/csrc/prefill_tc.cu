@@ -12,19 +12,21 @@
 //     {column, token, head}: rows past L read zeros), then the union of the
 //     two query blocks' key-block lists (merged on the fly, ascending), each
 //     key block's K and V tiles and its 64 document ids by TMA into a
-//     3-stage ring, with a small descriptor (block, full / first / last
-//     flags) in the stage.
+//     3-stage ring, with a small descriptor (block; full / first / last
+//     flags; which of the two query blocks list it) in the stage.
 //   warp 17 (MMA, one lane): S = Q K^T into one of two TMEM buffers
 //     (M = 128, N = 64, K-major SW128 operands), then, one tile behind,
-//     O += P V into TMEM (P K-major from shared memory, V MN-major).
+//     O += P V into one of two TMEM O buffers (items alternate; P K-major
+//     from shared memory, V MN-major).
 //   warps 0-15 (softmax): warps w, w + 4, w + 8, w + 12 share the 32 query
 //     rows of TMEM lanes 32(w%4)..32(w%4)+31, one row per thread, and split
-//     the 64 keys of a tile and the D columns of O in quarters. S from TMEM, masks on
-//     partial blocks, the row maximum combined through shared memory, online
-//     softmax in the exp2 domain with lazy rescaling (O in TMEM is rescaled
-//     only when a row's maximum grows by more than 2^8), P as bf16 into a
-//     swizzled shared buffer for the next MMA, and at an item's end O / l
-//     to global memory.
+//     the 64 keys of a tile and the D columns of O in quarters. S from TMEM,
+//     branch-free masks on partial blocks, the row maximum combined through
+//     shared memory, online softmax in the exp2 domain with lazy rescaling
+//     (O in TMEM is rescaled only when a row's maximum grows by more than
+//     2^8), P as bf16 into a swizzled shared buffer for the next MMA (zeros
+//     for the rows of a query block that does not list the key block), and
+//     an item's O / l to global memory after the next item's first tile.
 // Every wait on an mbarrier is bounded; a wait that gives up sets an abort
 // flag, every role leaves its loop, and the rows of unfinished items are
 // written as NaN, so a fault never passes silently.
