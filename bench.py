@@ -3,22 +3,30 @@
 
 Workload: the continuous-batching rollout with Qwen3-4B head shapes — 64
 slots, 32 q / 8 kv heads, head_dim 128, page 64, max_seq 1024, prompts
-U[100, 400], each sequence stopping at a seeded length and its slot and
-pages reused at once (fragmented placement). A step is one layer's decode
-step: q/k RMSNorm + RoPE, the K/V append, split-KV attention and combine —
-by default the fused paged_decode_step kernel plus the combine (--chain:
-three separate kernels). --workload picks one of the static decode layers
-instead (qwen3 B=8, llama B=16, gemma sliding D=256 / full D=512).
+U[100, 400], 512 decode steps, each sequence stopping at a seeded length and
+its slot and pages reused at once (fragmented placement). A step is one
+layer's decode step: q/k RMSNorm + RoPE, the K/V append, split-KV attention
+and combine — by default the fused paged_decode_step kernel plus the combine
+(--chain: three separate kernels). --workload picks one of the static decode
+layers instead (qwen3 B=8, llama B=16, gemma sliding D=256 / full D=512).
+
+The rollout schedule always has its 512 steps. --steps K times K steps drawn
+evenly across it (step floor((i + 1/2) * 512 / K) for i < K: every step once
+at K = 512), so a short run samples the whole schedule, not its opening. The
+whole schedule is also timed once per run (config.schedule), with the
+attention split by quarter (admission-heavy opening vs long-row end).
 
 value      algorithmic KV-read bytes of the attention (K+V of every key,
            q in, out, table entries) / device time of the whole step, GB/s;
            inputs resident in HBM, 4+ layer caches cycled so every step's
            keys come from DRAM (working set > 4x L2).
 roofline   the same bytes / the attention kernels' own time, vs the measured
-           HBM copy bandwidth.
+           HBM copy bandwidth; config.hot_l2 repeats it on one layer cache.
 e2e        the same metric through the public Python API with pinned host
            inputs copied in and the output read back every step.
-cpu_baseline / --impl reference: the float64 CPU oracle on a bounded sample.
+cpu_baseline / --impl reference: the float64 CPU oracle on a bounded sample
+           (a process pool over (row, kv head) on the host cores, and one
+           thread); config.pt_us times the host allocator calls.
 """
 from __future__ import annotations
 
@@ -46,15 +54,14 @@ import workloads as wl  # noqa: E402
 
 METRIC = "paged decode-attn KV-read GB/s (% of GB300 HBM peak); µs per decode step"
 UNIT = "GB/s"
-WORKLOAD_DESC = ("rollout continuous batching, Qwen3-4B heads: B=64 slots, 32 q / 8 kv heads, "
-                 "head_dim 128, page 64, max_seq 1024, prompts U[100,400], seeded stops with "
-                 "slot/page reuse, q/k RMSNorm + RoPE theta 1e6")
+WORKLOAD_DESC = ("512-step rollout, continuous batching: B=64 slots, Qwen3-4B heads 32/8, D=128, "
+                 "page 64, max_seq 1024, prompts U[100,400]")
 
 
 def parse_args():
     ap = argparse.ArgumentParser(description=__doc__)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=4000)
+    ap.add_argument("--steps", type=int, default=512)
     ap.add_argument("--warmup", type=int, default=16)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--e2e-steps", type=int, default=400)
@@ -82,6 +89,15 @@ def attn_bytes(seq_lens: np.ndarray, B, Hq, Hkv, D, ps, window: int = 0) -> int:
     lo = L - n
     pages = np.where(n > 0, (L + ps - 1) // ps - lo // ps, 0)
     return int(Hkv * n.sum() * D * 2 * 2 + B * Hq * D * 2 * 2 + pages.sum() * 4)
+
+
+def schedule_sample(S: int, K: int, offset: float = 0.5) -> np.ndarray:
+    """K step indices spread evenly over a schedule of S steps: step
+    floor((i + offset) * S / K) for i < K. At K = S (offset in [0, 1)) every
+    step appears once; K < S takes the middle step of each of K equal stretches;
+    K > S repeats every step K/S times, to within one."""
+    i = np.arange(K, dtype=np.float64)
+    return np.minimum(np.floor((i + offset) * S / K), S - 1).astype(np.int64)
 
 
 # name -> (workload, layer index, description)
@@ -282,28 +298,113 @@ def oracle_sample(w, lens_rows, rng, seconds, pool, D=128, window=0, min_rows=1)
     return total_bytes, elapsed, rows
 
 
+# A process pool over (row, kv head): each task is the oracle's attention for
+# one kv head of one row (its G query heads), on pages of a per-worker pool.
+_POOL = {}
+
+
+def _pool_init(seed, Hq, Hkv, ps, D, pages, window):
+    rng = np.random.default_rng(seed)
+    _POOL.update(
+        kc=rng.standard_normal((Hkv, pages * ps, D)).astype(np.float32),
+        vc=rng.standard_normal((Hkv, pages * ps, D)).astype(np.float32),
+        rng=rng, G=Hq // Hkv, ps=ps, D=D, pages=pages, window=window)
+
+
+def _pool_task(task):
+    import oracle
+    L, g = task
+    P = _POOL
+    rng, ps, D, G = P["rng"], P["ps"], P["D"], P["G"]
+    nb = -(-L // ps)
+    table = np.zeros((2, nb), np.int32)
+    table[1] = rng.integers(0, P["pages"], size=nb)
+    q = rng.standard_normal((1, G, D))
+    oracle.decode_attention(q, P["kc"][g:g + 1], P["vc"][g:g + 1], table, [1], [L],
+                            P["window"], D ** -0.5, ps)
+    return L
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_pool_sample(w, lens_rows, seconds, rows_per_s, D=128, window=0):
+    """The oracle on every host core: a spawn-started process pool over (row,
+    kv head) tasks for rows with the given lengths (cycled), sized from the
+    single-thread rate so that the pool works about `seconds` of wall time;
+    pool start-up is not timed. Returns (bytes, seconds, rows, processes)."""
+    import multiprocessing as mp
+    n = host_cores()
+    Hq, Hkv, ps = w.n_q_heads, w.n_kv_heads, w.page_size
+    rows = max(n, int(rows_per_s * n * seconds))
+    lens = [int(lens_rows[i % len(lens_rows)]) for i in range(rows)]
+    tasks = [(L, g) for L in lens for g in range(Hkv)]
+    ctx = mp.get_context("spawn")
+    with ctx.Pool(n, initializer=_pool_init,
+                  initargs=(w.seed(11), Hq, Hkv, ps, D, 64, window)) as pool:
+        pool.map(_pool_task, [(int(lens_rows[0]), 0)] * (2 * n), chunksize=1)   # warm
+        t0 = time.perf_counter()
+        for _ in pool.imap_unordered(_pool_task, tasks, chunksize=max(1, Hkv // 2)):
+            pass
+        sec = time.perf_counter() - t0
+    byts = sum(attn_bytes(np.array([L]), 1, Hq, Hkv, D, ps, window) for L in lens)
+    return byts, sec, rows, n
+
+
+def cpu_baselines(w, lens_rows, seconds, D=128, window=0, seed_salt=7):
+    """Single-thread and all-core oracle legs on rows with the given lengths;
+    the all-core leg is the reported cpu_baseline, the single-thread one rides
+    along in it."""
+    rng = np.random.default_rng(w.seed(seed_salt))
+    b1, s1, n1 = oracle_sample(w, lens_rows, rng, seconds, PagePool(w, rng, D), D, window)
+    one = b1 / s1 / 1e9
+    bn, sn, nn, procs = oracle_pool_sample(w, lens_rows, seconds, n1 / s1, D, window)
+    return {"value": bn / sn / 1e9, "unit": UNIT, "cores": procs, "kind": "oracle",
+            "sample": f"{nn} rows with the lengths of the timed steps' rows (cycled), "
+                      f"float64 NumPy, a spawn process pool of {procs} over (row, kv head), "
+                      f"{sn:.1f} s wall",
+            "single_thread": {"value": one, "cores": 1,
+                              "sample": f"{n1} rows, one thread, {s1:.1f} s"}}
+
+
+def rollout_lengths(w) -> np.ndarray:
+    """seq_lens [S][B] of the rollout schedule's S steps, from the schedule
+    alone (no allocator needed for lengths)."""
+    sched = wl.rollout_schedule(w)
+    length = [r.prompt_len for r in sched.first]
+    out = []
+    for t in range(sched.steps):
+        for lane, r in sched.start[t]:
+            length[lane] = r.prompt_len
+        out.append(np.array(length) + 1)
+        length = [L + 1 for L in length]
+    return np.stack(out)
+
+
 def run_reference(args, world, rank):
     """The CPU oracle as the reference arm: each step a bounded sample of the
-    step's rows (two rows), warm-up steps untimed."""
+    step's rows (two rows), on the same steps of the 512-step schedule that
+    our arm times; warm-up steps untimed."""
     if rank != 0:
         return
     w = wl.ROLLOUT
-    total = args.warmup + args.steps
-    sched = wl.rollout_schedule(w, steps=total)
-    # lengths per step from the schedule alone (no allocator needed for lengths)
-    length = [r.prompt_len for r in sched.first]
+    lens_all = rollout_lengths(w)
+    S = len(lens_all)
+    warm = schedule_sample(S, max(args.warmup, 1), 0.0)[:args.warmup]
+    timed = schedule_sample(S, args.steps)
     rng = np.random.default_rng(w.seed(99))
     pool = PagePool(w, rng)
     tot_bytes, tot_s, rows = 0, 0.0, 0
-    for t in range(total):
-        for lane, r in sched.start[t]:
-            length[lane] = r.prompt_len
-        lens = np.array(length) + 1
+    for j, t in enumerate(list(warm) + list(timed)):
+        lens = lens_all[t]
         sample = lens[[(2 * t) % w.batch, (2 * t + 1) % w.batch]]
         b, s, n = oracle_sample(w, sample, rng, 0.0, pool, min_rows=2)
-        if t >= args.warmup:
+        if j >= len(warm):
             tot_bytes, tot_s, rows = tot_bytes + b, tot_s + s, rows + n
-        length = [L + 1 for L in length]
     value = tot_bytes / tot_s / 1e9
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
@@ -311,6 +412,8 @@ def run_reference(args, world, rank):
         "ms_per_step": tot_s / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": WORKLOAD_DESC, "global_batch": w.batch,
+                   "schedule_steps": S,
+                   "timed_schedule_steps": f"{args.steps} steps spread evenly over the {S}",
                    "sample": "2 rows per step (of 64), oracle on host cores",
                    "parallelism": "replicas"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
@@ -322,6 +425,51 @@ def run_reference(args, world, rank):
 
 
 # ---------------------------------------------------------------- GPU arm ---
+def pt_timing(w):
+    """Host allocator cost over the rollout schedule: every pt_assign,
+    pt_reserve and pt_free the schedule issues, timed one by one through the
+    Python binding (ctypes call included), with the device mirror of the table
+    on (row writes queued with cudaMemcpyAsync on the current stream) and off
+    (host state only). µs per call: median and mean."""
+    import paged_kv_decode_pagetable_gb300 as pkv
+    from paged_kv_decode_pagetable_gb300 import engine
+
+    class Timed:
+        def __init__(self, pt):
+            self.pt, self.t = pt, {"assign": [], "reserve": [], "free": []}
+
+        def _run(self, name, *a):
+            t0 = time.perf_counter_ns()
+            r = getattr(self.pt, name)(*a)
+            self.t[name].append(time.perf_counter_ns() - t0)
+            return r
+
+        def assign(self, L):
+            return self._run("assign", L)
+
+        def reserve(self, s, L):
+            return self._run("reserve", s, L)
+
+        def free(self, s):
+            return self._run("free", s)
+
+    out = {}
+    for mode, device in (("device_mirror", torch.cuda.current_device()), ("host_only", None)):
+        pt = pkv.PageTable(w.max_batch_size, w.page_size, w.n_pages, w.max_pages_per_seq,
+                           device=device)
+        tp = Timed(pt)
+        drv = engine.RolloutDriver(tp, wl.rollout_schedule(w))
+        for _ in range(w.steps):
+            drv.next_step()
+        torch.cuda.synchronize()
+        out[mode] = {name: {"calls": len(v), "median_us": float(np.median(v)) / 1e3,
+                            "mean_us": float(np.mean(v)) / 1e3}
+                     for name, v in tp.t.items() if v}
+    out["note"] = ("through the ctypes binding; device_mirror includes queueing the table-row "
+                   "copy (cudaMemcpyAsync from pageable host memory)")
+    return out
+
+
 def run_ours(args, world, rank, local):
     import paged_kv_decode_pagetable_gb300 as pkv
     from paged_kv_decode_pagetable_gb300 import engine
@@ -338,17 +486,23 @@ def run_ours(args, world, rank, local):
                             lay.rotary_dims, lay.v_norm, lay.k_eq_v)
     B, Hq, Hkv, D, ps = w.batch, w.n_q_heads, w.n_kv_heads, spec.head_dim, w.page_size
     W, K = args.warmup, args.steps
-    total = W + K
-    if wname == "rollout":
-        tables, bidx, pos, lens = rollout_metadata(w, total)
+    rollout = wname == "rollout"
+    if rollout:
+        # the schedule always has its configured steps; warm-up and timed steps
+        # are drawn evenly across it
+        S = w.steps
+        tables, bidx, pos, lens = rollout_metadata(w, S)
+        warm_idx = schedule_sample(S, max(W, 1), 0.0)[:W]
+        timed_idx = schedule_sample(S, K)
     else:
         # a fixed batch appends one token per step until the table rows are
         # full, then the same steps repeat (re-appending the same positions)
-        period = min(total, w.max_seq - int(wl.static_lengths(w).max()))
-        idx = np.arange(total) % period
-        tables, bidx, pos, lens = (a[idx] for a in static_metadata(w, period))
+        S = min(W + K, w.max_seq - int(wl.static_lengths(w).max()))
+        tables, bidx, pos, lens = static_metadata(w, S)
+        warm_idx = np.arange(W) % S
+        timed_idx = (W + np.arange(K)) % S
     step_bytes = np.array([attn_bytes(lens[t], B, Hq, Hkv, D, ps, spec.window)
-                           for t in range(total)])
+                           for t in range(S)])
     d_tables = torch.from_numpy(tables).to(dev)
     d_bidx = torch.from_numpy(bidx).to(dev)
     d_pos = torch.from_numpy(pos).to(dev)
@@ -356,7 +510,7 @@ def run_ours(args, world, rank, local):
 
     props = torch.cuda.get_device_properties(dev)
     l2 = getattr(props, "L2_cache_size", 126 * 2 ** 20) or 126 * 2 ** 20
-    kv_step = float(np.mean(step_bytes))
+    kv_step = float(np.mean(step_bytes[timed_idx]))
     n_layers = args.layers or max(2, math.ceil(4 * l2 / kv_step))
     caches = [engine.alloc_cache(Hkv, w.n_pages, ps, D, dev, fill="randn") for _ in range(n_layers)]
 
@@ -377,36 +531,49 @@ def run_ours(args, world, rank, local):
                                                           w.n_pages)
         dev_table = None
 
-    def step(t):
-        kc, vc = caches[t % n_layers]
+    # step j of a sequence runs schedule step t on layer cache j mod n_layers,
+    # so consecutive calls read different caches
+    def step(j, t):
+        kc, vc = caches[j % n_layers]
         engine.decode_layer_step(spec, Geom, kc, vc, q, k, v, d_bidx[t], d_pos[t], d_lens[t], out,
                                  ws, gq, gk, w.eps, err=err, table=d_tables[t],
                                  fused=not args.chain)
 
-    def attn_only(t):
-        kc, vc = caches[t % n_layers]
+    def attn_only(j, t):
+        kc, vc = caches[j % n_layers]
         pkv.paged_decode_attn(q, kc, vc, d_tables[t], w.n_slots, w.max_pages_per_seq, ps,
                               w.n_pages, d_bidx[t], d_lens[t], spec.window, D ** -0.5, ws.splits,
                               ws.buf, out, err)
 
+    def capture(fn, idx, layer=None):
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr):
+            for j, t in enumerate(idx):
+                fn(j if layer is None else layer, int(t))
+        return gr
+
+    stream = torch.cuda.current_stream()
+
+    def time_graph(gr):
+        gr.replay()                       # the first launch of a graph uploads it
+        torch.cuda.synchronize()
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        gr.replay()
+        a1.record(stream)
+        torch.cuda.synchronize()
+        return a0.elapsed_time(a1)
+
     # warm-up: W eager steps (first use of every kernel), then capture
-    for t in range(W):
-        step(t)
+    for j, t in enumerate(warm_idx):
+        step(j, int(t))
     torch.cuda.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph):
-        for t in range(W, total):
-            step(t)
-    graph_attn = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph_attn):
-        for t in range(W, total):
-            attn_only(t)
+    graph = capture(step, timed_idx)
+    graph_attn = capture(attn_only, timed_idx)
     torch.cuda.synchronize()
-    # one untimed replay: the first launch of a graph uploads it
     graph.replay()
     torch.cuda.synchronize()
 
-    stream = torch.cuda.current_stream()
     sampler = ClockSampler(not args.no_clocks, local)
     barrier(world)
     torch.cuda.synchronize()
@@ -418,49 +585,84 @@ def run_ours(args, world, rank, local):
     barrier(world)
     clocks = sampler.stop()
     t_step_ms = e0.elapsed_time(e1)
+    del graph
 
-    # attention kernels alone over the same steps (after one untimed replay)
-    graph_attn.replay()
-    torch.cuda.synchronize()
-    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a0.record(stream)
-    graph_attn.replay()
-    a1.record(stream)
-    torch.cuda.synchronize()
-    t_attn_ms = a0.elapsed_time(a1)
+    # attention kernels alone over the same steps
+    t_attn_ms = time_graph(graph_attn)
+    del graph_attn
+    timed_bytes = float(step_bytes[timed_idx].sum())
+    peaks, peak_kind = measured_peaks()
+    peak = float(peaks.get("hbm_gbs", 6800.0))
+
+    # hot L2: the same attention calls, all on one layer cache
+    t_hot_ms = time_graph(capture(attn_only, timed_idx, layer=0))
+    hot = {"attn_us_per_call": t_hot_ms / K * 1e3,
+           "gbs": timed_bytes / (t_hot_ms * 1e-3) / 1e9,
+           "frac": timed_bytes / (t_hot_ms * 1e-3) / 1e9 / peak,
+           "note": "same steps, one layer cache: consecutive calls re-read mostly the same pages"}
+
+    schedule = None
+    if rollout:
+        # the whole schedule once, and its attention by quarter
+        all_idx = np.arange(S)
+        t_full_ms = time_graph(capture(step, all_idx))
+        t_full_attn_ms = time_graph(capture(attn_only, all_idx))
+        full_bytes = float(step_bytes.sum())
+        phases = []
+        for qd in range(4):
+            idx = all_idx[qd * S // 4:(qd + 1) * S // 4]
+            ms = time_graph(capture(attn_only, idx))
+            byts = float(step_bytes[idx].sum())
+            phases.append({"steps": f"{int(idx[0])}-{int(idx[-1])}",
+                           "mean_seq_len": float(lens[idx].mean()),
+                           "mean_kv_mb": byts / len(idx) / 1e6,
+                           "attn_us_per_call": ms / len(idx) * 1e3,
+                           "frac": byts / (ms * 1e-3) / 1e9 / peak})
+        sched = wl.rollout_schedule(w)
+        schedule = {"steps": S, "us_per_step": t_full_ms / S * 1e3,
+                    "attn_us_per_call": t_full_attn_ms / S * 1e3,
+                    "attn_gbs": full_bytes / (t_full_attn_ms * 1e-3) / 1e9,
+                    "attn_frac": full_bytes / (t_full_attn_ms * 1e-3) / 1e9 / peak,
+                    "step_gbs": full_bytes / (t_full_ms * 1e-3) / 1e9,
+                    "mean_kv_mb": full_bytes / S / 1e6,
+                    "seq_len": f"{int(lens.min())}-{int(lens.max())}",
+                    "slot_reuses": int(sum(len(f) for f in sched.finish)),
+                    "timed_steps_with_reuse": int(sum(1 for t in timed_idx if sched.finish[t])),
+                    "attn_by_quarter": phases}
     errv = pkv.pkv_read_error_word(err)
     if errv != 0:
         raise SystemExit(f"device error word {errv}")
 
-    timed_bytes = float(step_bytes[W:].sum())
     t_max = reduce_max(t_step_ms, world)
     value = reduce_sum(timed_bytes, world) / (t_max * 1e-3) / 1e9
     attn_gbs = timed_bytes / (t_attn_ms * 1e-3) / 1e9
-    peaks, peak_kind = measured_peaks()
-    peak = float(peaks.get("hbm_gbs", 6800.0))
     launches_per_step = (3 if args.chain else 1) + (1 if ws.max_parts > 1 else 0)
 
     # ---- end to end through the public API: pinned host in, output back ----
+    n_e2e = min(args.e2e_steps, K)
+    e2e_idx = schedule_sample(S, n_e2e) if rollout else timed_idx[:n_e2e]
     e2e = run_e2e(args, w, spec, engine, pkv, caches, n_layers, tables, bidx, pos, lens,
-                  step_bytes, gq, gk, ws, dev, world)
+                  step_bytes, gq, gk, ws, dev, world, warm_idx, e2e_idx)
 
-    # ---- CPU oracle baseline on a bounded sample (rank 0, N=1 only) ----
-    cpu = None
+    # ---- CPU oracle baselines on a bounded sample (rank 0, N=1 only) ----
+    cpu, pt_us = None, None
     if rank == 0 and world == 1:
-        rng = np.random.default_rng(w.seed(7))
-        b, s, n = oracle_sample(w, lens[W], rng, args.cpu_seconds, PagePool(w, rng, D), D,
-                                spec.window)
-        cpu = {"value": b / s / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
-               "sample": f"{n} rows with the lengths of timed step 0's batch (cycled), float64 "
-                         f"NumPy on 1 host thread, {s:.1f} s"}
+        rows = np.concatenate([lens[t] for t in timed_idx])
+        cpu = cpu_baselines(w, rows, args.cpu_seconds, D, spec.window)
+        if rollout:
+            pt_us = pt_timing(w)
 
     if rank == 0:
+        tl = lens[timed_idx]
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
             "warmup": W, "ms_per_step": t_max / K, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": desc or WORKLOAD_DESC, "global_batch": B * world,
-                       "seq_len": f"{int(lens[W:].min())}-{int(lens[W:].max())}",
+                       "seq_len": f"{int(tl.min())}-{int(tl.max())}",
+                       "timed_steps": (f"{K} steps spread evenly over the {S}-step schedule"
+                                       if rollout else f"steps {W}.. of a fixed batch"),
+                       "mean_kv_mb_per_step": timed_bytes / K / 1e6,
                        "num_splits": ws.splits or "auto (length-balanced parts)",
                        "max_parts_per_row": ws.max_parts, "layer_caches_cycled": n_layers,
                        "l2_policy": f"inputs larger than L2: {n_layers} layer caches of "
@@ -469,12 +671,13 @@ def run_ours(args, world, rank, local):
                        "us_per_step": t_max / K * 1e3, "attn_us_per_call": t_attn_ms / K * 1e3,
                        "layer_step": ("qk_norm_rope + kv_append + paged_decode_attn"
                                       if args.chain else "paged_decode_step (fused)"),
+                       "schedule": schedule, "hot_l2": hot, "pt_us": pt_us,
                        "parallelism": f"replicas x{world}"},
             "roofline": {"bound": "hbm", "achieved": attn_gbs, "peak": peak, "unit": "GB/s",
                          "frac": attn_gbs / peak, "peak_kind": peak_kind,
                          "kernel": f"decode_attn_kernel<{D}, false> + combine_kernel<{D}>",
                          "traffic": profile_traffic(f"{args.workload}_decode_attn_{D}",
-                                                    float(step_bytes[W:].mean()))},
+                                                    timed_bytes / K)},
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": K * launches_per_step,
@@ -484,7 +687,7 @@ def run_ours(args, world, rank, local):
 
 
 def run_e2e(args, w, spec, engine, pkv, caches, n_layers, tables, bidx, pos, lens, step_bytes,
-            gq, gk, ws, dev, world):
+            gq, gk, ws, dev, world, warm_idx, idx):
     """The metric through the public API with host buffers: every step copies
     its q, k, v, page table and row metadata from pinned host memory to the
     device, runs the layer step, and copies the output back to pinned host
@@ -494,8 +697,7 @@ def run_e2e(args, w, spec, engine, pkv, caches, n_layers, tables, bidx, pos, len
     steps are replayed from a CUDA graph captured over the API calls; the
     same steps issued eagerly from Python are reported as eager_value."""
     B, Hq, Hkv, D = w.batch, w.n_q_heads, w.n_kv_heads, spec.head_dim
-    n = min(args.e2e_steps, args.steps)
-    W = args.warmup
+    n = len(idx)
     ring = 8
     gen = torch.Generator().manual_seed(w.seed(3))
     nq, nkv = B * Hq * D * 2, B * Hkv * D * 2
@@ -503,10 +705,11 @@ def run_e2e(args, w, spec, engine, pkv, caches, n_layers, tables, bidx, pos, len
     offs = np.cumsum([0, nq, nkv, nkv, ntab, nmeta])      # 16-byte multiples at these shapes
     qkv = [torch.randn(B * (Hq + 2 * Hkv) * D, generator=gen).to(torch.bfloat16)
            for _ in range(ring)]
+    seq = [int(t) for t in list(warm_idx[:8]) + list(idx)]
     h_in = []
-    for t in range(W + n):
+    for j, t in enumerate(seq):
         buf = torch.empty(int(offs[-1]), dtype=torch.uint8).pin_memory()
-        buf[offs[0]:offs[3]].view(torch.bfloat16).copy_(qkv[t % ring])
+        buf[offs[0]:offs[3]].view(torch.bfloat16).copy_(qkv[j % ring])
         buf[offs[3]:offs[4]].view(torch.int32).copy_(torch.from_numpy(tables[t]).reshape(-1))
         buf[offs[4]:offs[5]].view(torch.int32).copy_(
             torch.from_numpy(np.stack([bidx[t], pos[t], lens[t]])).reshape(-1))
@@ -525,16 +728,16 @@ def run_e2e(args, w, spec, engine, pkv, caches, n_layers, tables, bidx, pos, len
                                                           w.page_size, w.n_pages)
         dev_table = None
 
-    def one(t):
-        j = t % ring
-        d_in.copy_(h_in[t], non_blocking=True)
-        kc, vc = caches[t % n_layers]
+    def one(j):
+        d_in.copy_(h_in[j], non_blocking=True)
+        kc, vc = caches[j % n_layers]
         engine.decode_layer_step(spec, Geom, kc, vc, q, k, v, d_meta[0], d_meta[1], d_meta[2],
                                  out, ws, gq, gk, w.eps, table=d_table, fused=not args.chain)
-        h_out[j].copy_(out, non_blocking=True)
+        h_out[j % ring].copy_(out, non_blocking=True)
 
-    for t in range(min(W, 8)):
-        one(t)
+    n_warm = len(seq) - n
+    for j in range(n_warm):
+        one(j)
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
 
@@ -548,15 +751,15 @@ def run_e2e(args, w, spec, engine, pkv, caches, n_layers, tables, bidx, pos, len
         torch.cuda.synchronize()
         return reduce_max(e0.elapsed_time(e1), world)
 
-    ms_eager = timed(lambda: [one(t) for t in range(W, W + n)])
+    ms_eager = timed(lambda: [one(j) for j in range(n_warm, n_warm + n)])
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
-        for t in range(W, W + n):
-            one(t)
+        for j in range(n_warm, n_warm + n):
+            one(j)
     g.replay()
     torch.cuda.synchronize()
     ms = timed(g.replay)
-    byts = reduce_sum(float(step_bytes[W:W + n].sum()), world)
+    byts = reduce_sum(float(step_bytes[np.asarray(idx)].sum()), world)
     h2d = int(offs[-1])
     return {"value": byts / (ms * 1e-3) / 1e9, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(B * Hq * D * 2), "steps": n, "ms_per_step": ms / n,

@@ -34,3 +34,37 @@ def test_decode_bytes_equal_a_per_key_count():
             total += Hkv * len(keys) * D * 2 * 2
             total += 4 * len({k // ps for k in keys})
         assert bench.attn_bytes(lens, B, Hq, Hkv, D, ps, window) == total, window
+
+
+def test_schedule_sample_spreads_timed_steps_over_the_whole_schedule():
+    """The rollout bench times K steps of its fixed 512-step schedule: every
+    step exactly once at K = 512, the step in the middle of each of K equal
+    stretches below that, every step K/512 times above it."""
+    S = 512
+    assert list(bench.schedule_sample(S, S)) == list(range(S))
+    for K in (1, 3, 20, 100, 511):
+        idx = bench.schedule_sample(S, K)
+        assert len(idx) == K and np.all(np.diff(idx) > 0)
+        for i, t in enumerate(idx):
+            assert (i * S) // K <= t < (i + 1) * S / K      # the middle of stretch i
+    idx = bench.schedule_sample(S, 3 * S)
+    assert np.array_equal(np.bincount(idx, minlength=S), np.full(S, 3))
+    assert list(bench.schedule_sample(S, 4, 0.0)) == [0, 128, 256, 384]
+
+
+def test_rollout_lengths_equal_the_allocator_driven_schedule():
+    """The reference arm's per-step lengths (from the schedule alone) equal the
+    seq_lens the GPU arm gets from the PageTable-driven schedule, so both arms
+    time the same rows."""
+    import workloads as wl
+    pytest = __import__("pytest")
+    pkv = pytest.importorskip("paged_kv_decode_pagetable_gb300")
+    try:
+        pkv.load_library()
+    except RuntimeError:
+        pytest.skip("libpkv.so not built")
+    w = wl.ROLLOUT
+    lens = bench.rollout_lengths(w)
+    _, _, _, lens_pt = bench.rollout_metadata(w, w.steps)
+    assert lens.shape == (512, 64) and np.array_equal(lens, lens_pt)
+    assert lens.min() >= 101 and lens.max() <= 1024
