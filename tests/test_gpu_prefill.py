@@ -7,13 +7,13 @@ more than 128 key blocks (the builder's second pass).
 
 The block mask is integer work: equal to the oracle's, entry for entry.
 
-Attention bar, from the kernel's arithmetic: the probabilities P enter the
-P.V product as bf16 (relative error <= 2^-9 each) and the output is rounded
-once to bf16 (<= 2^-9 |o|), so |o_gpu - o| <= 2^-9 (max|v| + |o|) <=
-2^-8 max|v|; prefill has many rows with two or three kept keys, where this is
-reached (the decode rows are long enough that the fixed 1e-2 bar holds
-there). Each element must be within 2^-8 max|v| + 2e-3 and the mean error
-within 1e-3."""
+Attention bar: the decode path's, max abs 1e-2 and mean abs 1e-3, on every
+query row that keeps at least 16 keys, and the mean over all rows. Rows with
+fewer kept keys (a document's first tokens) may miss 1e-2 without any fault:
+with one or two keys the output is about as large as v itself, and rounding
+it once to bf16 (half an ulp, 2^-9 relative) plus the bf16 probabilities in
+P.V give |o_gpu - o| <= 2^-9 (max|v| + |o|) <= 2^-8 max|v|, about 0.018 for
+N(0, 1) values. Those rows are held to 2^-8 max|v| + 2e-3."""
 import numpy as np
 import pytest
 import torch
@@ -82,11 +82,23 @@ def _run(dev, q, k, v, docs, window, scale, bm=None):
     return out, bm
 
 
-def _compare(got, ref, v):
+def _compare(got, ref, v, kept):
+    """got, ref: [Hq][L][D]; kept: keys kept by each of the L query rows."""
     assert np.isfinite(got).all()
     e = np.abs(got - ref)
-    bound = 2.0 ** -8 * float(np.abs(v.double().numpy()).max()) + 2e-3
-    assert e.max() <= bound and e.mean() <= 1e-3, (float(e.max()), bound, float(e.mean()))
+    long_rows = np.asarray(kept) >= 16
+    assert e.mean() <= 1e-3, float(e.mean())
+    if long_rows.any():
+        el = e[:, long_rows]
+        assert el.max() <= 1e-2, (float(el.max()), int(long_rows.sum()))
+    if (~long_rows).any():
+        bound = 2.0 ** -8 * float(np.abs(v.double().numpy()).max()) + 2e-3
+        es = e[:, ~long_rows]
+        assert es.max() <= bound, (float(es.max()), bound)
+
+
+def _kept(docs, window=0):
+    return oracle.keep_matrix(docs, window).sum(axis=1)
 
 
 @pytest.mark.parametrize("L,Hq,Hkv,D,kind,window", [
@@ -105,7 +117,7 @@ def test_prefill_attention_parity(dev, L, Hq, Hkv, D, kind, window):
     out, _ = _run(dev, q, k, v, docs, window, scale)
     ref = oracle.prefill_attention(q.double().numpy(), k.double().numpy(), v.double().numpy(),
                                    docs, scale, window=window)
-    _compare(f64(out), ref, v)
+    _compare(f64(out), ref, v, _kept(docs, window))
 
 
 def test_prefill_full_size_sampled_documents(dev):
@@ -130,7 +142,7 @@ def test_prefill_full_size_sampled_documents(dev):
         sl = slice(int(starts[d]), int(starts[d + 1]))
         ref = oracle.prefill_attention(q[:, sl].double().numpy(), k[:, sl].double().numpy(),
                                        v[:, sl].double().numpy(), docs[sl], scale)
-        _compare(got[:, sl], ref, v)
+        _compare(got[:, sl], ref, v, _kept(docs[sl]))
 
 
 def test_prefill_mask_lists_are_bounds_safe(dev):
@@ -199,4 +211,41 @@ def test_prefill_rising_scores_rescale_every_tile(dev, D):
     out, _ = _run(dev, q, k, v, docs, 0, scale)
     ref = oracle.prefill_attention(q.double().numpy(), k.double().numpy(), v.double().numpy(),
                                    docs, scale)
-    _compare(f64(out), ref, v)
+    _compare(f64(out), ref, v, _kept(docs))
+
+
+def test_prefill_long_documents_sampled_rows(dev):
+    """The long-document launch: 8 documents of 2048 tokens, 32 q / 8 kv
+    heads, head_dim 128. Sampled query rows of every document (its first
+    tokens, rows across it and its last rows, where 2048 keys are kept) are
+    each compared, all heads, with the oracle's single-query attention over
+    the row's kept keys; every sampled row keeping 16 or more keys is held to
+    max abs 1e-2."""
+    from oracle.attention import decode_attention_row
+    rng = np.random.default_rng(78)
+    L, Hq, Hkv, D, n = 8 * 2048, 32, 8, 128, 2048
+    docs = np.repeat(np.arange(8), n).astype(np.int32)
+    q = wl.randn_bf16(rng, (Hq, L, D))
+    k = wl.randn_bf16(rng, (Hkv, L, D))
+    v = wl.randn_bf16(rng, (Hkv, L, D))
+    scale = D ** -0.5
+    out, bm = _run(dev, q, k, v, docs, 0, scale)
+    got = f64(out)
+    qd, kd, vd = q.double().numpy(), k.double().numpy(), v.double().numpy()
+    within = np.r_[0, 1, 15, 16, rng.integers(17, n - 64, size=6), np.arange(n - 64, n, 16),
+                   n - 1]
+    G = Hq // Hkv
+    errs, kept = [], []
+    for d in range(8):
+        for w_ in within:
+            i = d * n + int(w_)
+            js = np.arange(d * n, i + 1)
+            ref = np.stack([decode_attention_row(qd[h, i], kd[h // G, js], vd[h // G, js],
+                                                 scale)[0] for h in range(Hq)])
+            errs.append(np.abs(got[:, i] - ref))
+            kept.append(len(js))
+    e = np.stack(errs, axis=1)                       # [Hq][rows][D]
+    long_rows = np.array(kept) >= 16
+    assert np.isfinite(got).all()
+    assert e[:, long_rows].max() <= 1e-2, float(e[:, long_rows].max())
+    assert e.mean() <= 1e-3, float(e.mean())
