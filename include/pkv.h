@@ -209,16 +209,20 @@ int qk_norm_rope_append(pkv_bf16 *q, pkv_bf16 *k, const pkv_bf16 *v,
  *
  * Split-KV: the (row, kv head) key ranges are cut into parts of whole
  * 64-key tiles processed by persistent CTAs; a row cut into several parts
- * gets fp32 partial outputs and log-sum-exps in the workspace that a combine
- * kernel merges. num_splits 0 (automatic) picks one part size for the call
- * on the device from the actual lengths so that all SMs get the same amount
- * of work; num_splits S > 0 cuts every row into at most S equal parts.
+ * gets fp32 partial outputs and log-sum-exps in the workspace. num_splits 0
+ * (automatic) lays the tiles of the call on one line from the actual
+ * lengths, on the device, and gives every CTA an equal share of it; the CTA
+ * holding the first part of a cut row merges the later parts (each the first
+ * work of its own CTA) itself, so no second kernel runs. num_splits S > 0
+ * cuts every row into at most S equal parts that a combine kernel merges.
  * The workspace must hold paged_decode_attn_workspace(B, Hq, D, P) bytes
  * (16-byte aligned; may be NULL when that is 0), with P = S for a fixed
  * split count or P = paged_decode_attn_splits(...) for the automatic mode.
- * Every workspace field is written by a call before that call reads it, so
- * the workspace needs no initialisation; calls sharing one workspace must
- * not overlap on the GPU.
+ * It holds partials, which every call writes before reading, and per-part
+ * flags: zero the workspace once before its first use (e.g. cudaMemset).
+ * Every call leaves the flags zero again, except a call that reports
+ * PKV_ERR_TIMEOUT in the error word, after which the workspace must be
+ * zeroed again. Calls sharing one workspace must not overlap on the GPU.
  * q: bf16 [B][Hq][D], out: bf16 [B][Hq][D], caches and table as above.
  * Requires D in {64, 128, 256, 512}, 1 <= Hq/Hkv <= 8, Hq % Hkv == 0,
  * page_size a power of two >= 8, B <= 512, and 16-byte aligned q, out,
@@ -376,12 +380,16 @@ int prefill_attn(const pkv_bf16 *q, const pkv_bf16 *k, const pkv_bf16 *v,
  * as paged_decode_attn minus workspace / workspace_bytes. The split
  * partials go to a fixed 32 MiB scratch array in the library's device
  * image, held by every GPU that loads the library until the process exits;
- * calls whose partials need more (see paged_decode_attn_workspace) fail with
- * PKV_E_BAD_ARG. The first call on a device looks up the scratch address
+ * a call whose partials need more fails with PKV_E_BAD_ARG. The need is
+ * paged_decode_attn_workspace(B, Hq, D, parts) with parts = num_splits
+ * capped at the 64-key tiles of the longest row the table holds (the
+ * automatic count of paged_decode_attn_splits when num_splits is 0), the
+ * same cap paged_decode_attn applies. The first call on a device looks up the scratch address
  * (cudaGetSymbolAddress) with that device current; make it before any
  * stream capture begins. All calls share the scratch: calls whose kernels
- * overlap on the GPU race and must be serialized by the caller. Nothing in
- * the scratch needs clearing between calls. No device memory is allocated.
+ * overlap on the GPU race and must be serialized by the caller. Each call
+ * first clears the scratch's part flags (cudaMemsetAsync on the caller's
+ * stream); the partials need no clearing. No device memory is allocated.
  * ------------------------------------------------------------------- */
 int paged_decode_attn_noalloc(const pkv_bf16 *q, const pkv_bf16 *k_cache,
                               const pkv_bf16 *v_cache, const int32_t *dev_table,

@@ -53,11 +53,14 @@ constexpr int kMaxRows = 512;        // rows per call (row cache kept in smem)
 constexpr int kSpinLimit = 1 << 22;
 // Balanced split cost model, in quarter tiles: a key tile costs kTileCost and
 // starting a (row, kv head) costs kUnitCost more (its query load, table
-// lookups, epilogue and the tail of its partly used last tile). The value
-// is the best of a sweep over 1..16 on the rollout, Llama and Gemma layers
-// (6: rollout attention 29.24 -> 28.98 us against 3).
+// lookups, epilogue and the tail of its partly used last tile). A
+// least-squares fit of per-CTA end times (%globaltimer) on the rollout gave
+// 0.93 us per tile and 0.75 us per unit for the attention kernel, 1.31 us per
+// unit for the fused step (which also rotates the unit's query rows). Both
+// kernels use one value, so that they cut rows at the same places and the
+// fused step stays bit-identical to the separate calls.
 constexpr int kTileCost = 4;
-constexpr int kUnitCost = 6;
+constexpr int kUnitCost = 4;
 
 template <int D>
 struct Cfg {
@@ -75,7 +78,7 @@ struct Cfg {
   static constexpr int OFF_P = OFF_Q + 2 * Q_STAGE;
   static constexpr int OFF_RED = OFF_P + kT * 16;                // 2 x [4][8] f32
   static constexpr int OFF_BAR = OFF_RED + 2 * kCWarps * kMaxG * 4;
-  static constexpr int N_BARS = 4 * NS + 4;
+  static constexpr int N_BARS = 4 * NS + 5;   // + the merge barrier
   static constexpr int OFF_MASK = OFF_BAR + N_BARS * 8;           // 2 x NS u32
   static constexpr int OFF_MISC = OFF_MASK + 2 * NS * 4;          // abort flag
   static constexpr int OFF_DESC = OFF_MISC + 16;                  // Unit [2] (48 B each)
@@ -93,6 +96,11 @@ struct Cfg {
 static_assert(Cfg<64>::CTAS_PER_SM * (Cfg<64>::SMEM + 1024) <= 228 * 1024, "D=64 residency");
 static_assert(Cfg<128>::CTAS_PER_SM * (Cfg<128>::SMEM + 1024) <= 228 * 1024, "D=128 residency");
 static_assert(Cfg<256>::SMEM <= 227 * 1024 && Cfg<512>::SMEM <= 227 * 1024, "smem per CTA");
+// the two Q stages hold one part's partial (o [G][D] and lse [G], fp32) for the merge
+static_assert(2 * Cfg<64>::Q_STAGE >= kMaxG * 64 * 4 + kMaxG * 4 &&
+              2 * Cfg<128>::Q_STAGE >= kMaxG * 128 * 4 + kMaxG * 4 &&
+              2 * Cfg<256>::Q_STAGE >= kMaxG * 256 * 4 + kMaxG * 4 &&
+              2 * Cfg<512>::Q_STAGE >= kMaxG * 512 * 4 + kMaxG * 4, "merge buffer");
 
 // ---------------------------------------------------------------- PTX ----
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -216,7 +224,8 @@ struct Problem {
   int len_bias;       // L = seq_lens[b] + len_bias (1 when seq_lens holds input_pos)
   int n_slots, max_pages, log2_ps, n_pages, window, B, Hq, Hkv, G;
   int fixed_splits;   // > 0: each row cut into at most this many parts; 0: balanced
-  int max_parts;      // partial slots per (row, head) in the workspace
+  int max_parts;      // partial slots per (row, kv head) in the workspace
+  int unit_cost;      // balanced mode: cost of starting a (row, kv head), quarter tiles
 };
 
 struct RowInfo {
@@ -372,6 +381,26 @@ __device__ __forceinline__ int small_quotient_warp(int x, int d, int n, int lane
   return __popc(__ballot_sync(0xffffffffu, lane < n && lane * d <= x)) - 1;
 }
 
+// The shares of the balanced cost line: CTA c owns cost positions
+// [bound(c), bound(c + 1)) with bound(c) = floor(c * num / den), clipped to
+// the line's length. Shares are at least one tile's cost long, so every CTA
+// strictly between the first and the last owner of a (row, head) owns one of
+// its tiles. Equal fractional shares (num = cost, den = grid) are used when
+// the line is long enough, else shares of exactly one tile (num = kTileCost,
+// den = 1).
+struct Share {
+  long long num;
+  int den;
+};
+__device__ __forceinline__ int share_bound(const Share &s, int c, int cost) {
+  const long long v = static_cast<long long>(c) * s.num / s.den;
+  return v < cost ? static_cast<int>(v) : cost;
+}
+// CTA owning cost position x: the largest c with bound(c) <= x.
+__device__ __forceinline__ int share_owner(const Share &s, int x) {
+  return static_cast<int>((static_cast<long long>(x + 1) * s.den + s.num - 1) / s.num) - 1;
+}
+
 // A run of key tiles of one (row, kv head) processed by one CTA. The
 // producer computes each unit once and hands it to the consumers in shared
 // memory with the unit's query rows (b < 0: no more units).
@@ -387,22 +416,25 @@ static_assert(sizeof(Unit) <= 48, "unit descriptor slot");
 
 // Walks this CTA's units. Balanced mode: the (row, kv head, tile) sequence
 // is flattened and laid on a cost line where each tile costs kTileCost and
-// each (row, head) kUnitCost more before its first tile; every CTA owns the
-// tiles whose cost position falls in its equal share [c*qc, (c+1)*qc), a
-// contiguous run of the flattened sequence. A (row, head) that straddles
-// CTAs is finished by the combine kernel. Fixed mode: units are (row, part,
+// each (row, head) unit_cost more before its first tile; the line is cut into
+// one share per CTA, [bound(c), bound(c + 1)), and every CTA owns the tiles
+// whose cost position falls in its share, a contiguous run of the flattened
+// sequence. A (row, head) that straddles CTAs is cut into parts: its first
+// part is the last unit of its CTA and every later part is the first unit of
+// its own CTA, so the first part's CTA finds the later parts' partials ready
+// when it ends and merges them itself. Fixed mode: units are (row, part,
 // head) with each row cut into at most S equal parts, dealt out in equal
-// counts.
+// counts, and merged by the combine kernel.
 struct UnitIter {
   int pos, end;     // balanced: flattened tile index; fixed: unit index
-  int qc;           // balanced: cost per CTA
+  Share sh;         // balanced: the shares of the cost line
   int hb, hg, ht;   // balanced: (row, head, tile) of pos when already known; hb < 0 if not
 };
 
 // Cost position of the first tile of (row b, head g): prc is the prefix of
-// per-row head costs (kTileCost * tiles + kUnitCost for rows with tiles).
+// per-row head costs (kTileCost * tiles + unit_cost for rows with tiles).
 __device__ __forceinline__ int head_cost_start(const Problem &p, const int *prc, int b, int g) {
-  return p.Hkv * prc[b] + g * (prc[b + 1] - prc[b]) + kUnitCost;
+  return p.Hkv * prc[b] + g * (prc[b + 1] - prc[b]) + p.unit_cost;
 }
 
 // The CTA's range: flattened indices of the first tiles whose cost positions
@@ -431,7 +463,7 @@ __device__ __forceinline__ void locate_range(const Problem &p, const int *pre, c
       const int W = prc[b + 1] - prc[b], T = pre[b + 1] - pre[b];
       const int within = x - p.Hkv * prc[b];
       const int g = small_quotient_warp(within, W, p.Hkv, lane), r = within - g * W;
-      const int j = r <= kUnitCost ? 0 : (r - kUnitCost + kTileCost - 1) / kTileCost;
+      const int j = r <= p.unit_cost ? 0 : (r - p.unit_cost + kTileCost - 1) / kTileCost;
       flat = p.Hkv * pre[b] + g * T + j;
       if (k == 0 && j < T) {
         it.hb = b;
@@ -465,12 +497,12 @@ __device__ __forceinline__ bool next_unit(const Problem &p, const int2 *rows, co
     const int tiles = pre[b + 1] - pre[b];
     const int n = min(tiles - t0, it.end - it.pos);
     const int c0 = head_cost_start(p, prc, b, w.g);
-    const int first_cta = c0 / it.qc;
+    const int first_cta = share_owner(it.sh, c0);
     w.b = b;
     w.slot = r.slot;
     w.ta = r.t_first + t0;
     w.tb = w.ta + n;
-    w.parts = (c0 + kTileCost * (tiles - 1)) / it.qc - first_cta + 1;
+    w.parts = share_owner(it.sh, c0 + kTileCost * (tiles - 1)) - first_cta + 1;
     w.part = static_cast<int>(blockIdx.x) - first_cta;   // this CTA owns the unit's tiles
     w.k0 = max(r.lo, w.ta * kT);
     w.k1 = min(r.L, w.tb * kT);
@@ -494,6 +526,37 @@ __device__ __forceinline__ bool next_unit(const Problem &p, const int2 *rows, co
   return true;
 }
 
+// Flags of the later parts of a cut (row, head): part j (1 <= j < parts) sets
+// f[j] to 1 with a gpu-scope release once its partial is in the workspace.
+// The converged producer warp of the first part's CTA waits until it has seen
+// every one set (each lane one flag, relaxed polls; `peek` is the lane's
+// earlier look at its flag in the first batch), then acquires with a fence,
+// resets the flags to 0 for the next call and returns true; false if the wait
+// gives up (after kFlagSpinLimit polls, or when the CTA aborts).
+constexpr int kFlagSpinLimit = 1 << 21;
+__device__ __forceinline__ unsigned ld_relaxed_gpu(const unsigned *a) {
+  unsigned v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ bool wait_parts(unsigned *f, int parts, int lane,
+                                           volatile int *abort_flag, unsigned peek) {
+  for (int j0 = 1; j0 < parts; j0 += 32) {
+    const int j = j0 + lane;
+    bool done = j >= parts || (j0 == 1 && peek != 0u);
+    for (int i = 0; !__all_sync(0xffffffffu, done); ++i) {
+      if (i >= kFlagSpinLimit) return false;
+      if (__shfl_sync(0xffffffffu, (i & 15) == 15 ? *abort_flag : 0, 0)) return false;
+      __nanosleep(32);
+      if (!done) done = ld_relaxed_gpu(f + j) != 0u;
+    }
+  }
+  asm volatile("fence.acq_rel.gpu;" ::: "memory");
+  for (int j = 1 + lane; j < parts; j += 32)
+    asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(f + j), "r"(0u) : "memory");
+  return true;
+}
+
 // ------------------------------------------------------------- kernel ----
 template <int D, bool STEP>
 __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
@@ -504,8 +567,8 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
                        const __nv_bfloat16 *__restrict__ q, const Problem p,
                        float scale_log2, float *__restrict__ o_part,
                        float *__restrict__ lse_part, int *__restrict__ parts_out,
-                       __nv_bfloat16 *__restrict__ out, int32_t *__restrict__ err,
-                       const StepArgs sa) {
+                       unsigned *__restrict__ flags, __nv_bfloat16 *__restrict__ out,
+                       int32_t *__restrict__ err, const StepArgs sa) {
   using Cf = Cfg<D>;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -517,10 +580,10 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
   float *red_max = reinterpret_cast<float *>(sm + Cf::OFF_RED);
   float *red_sum = red_max + kCWarps * kMaxG;
   const uint32_t bar0 = sK + Cf::OFF_BAR;
-  // barrier layout: fullK[NS] emptyK[NS] fullV[NS] emptyV[NS] fullQ[2] emptyQ[2]
+  // barrier layout: fullK[NS] emptyK[NS] fullV[NS] emptyV[NS] fullQ[2] emptyQ[2] merge
   const uint32_t fullK = bar0, emptyK = bar0 + 8 * Cf::NS, fullV = bar0 + 16 * Cf::NS,
                  emptyV = bar0 + 24 * Cf::NS, fullQ = bar0 + 32 * Cf::NS,
-                 emptyQ = fullQ + 16;
+                 emptyQ = fullQ + 16, mergeBar = fullQ + 32;
   uint32_t *kmask = reinterpret_cast<uint32_t *>(sm + Cf::OFF_MASK);
   uint32_t *vmask = kmask + Cf::NS;
   volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + Cf::OFF_MISC);
@@ -541,6 +604,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
       mbar_init(fullQ + 8 * i, 1);
       mbar_init(emptyQ + 8 * i, kCWarps);
     }
+    mbar_init(mergeBar, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     fence_proxy_async();
@@ -575,7 +639,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
     const RowInfo r = row_info(p, b, err, blockIdx.x == 0);
     rows[b] = make_int2(r.n_tiles > 0 ? r.slot : -1, r.L | (r.clamped ? kClampBit : 0));
     pre[b + 1] = p.fixed_splits > 0 ? fixed_parts(r.n_tiles, p.fixed_splits) : r.n_tiles;
-    prc[b + 1] = r.n_tiles > 0 ? kTileCost * r.n_tiles + kUnitCost : 0;
+    prc[b + 1] = r.n_tiles > 0 ? kTileCost * r.n_tiles + p.unit_cost : 0;
   }
   __syncthreads();
   if (warp < 2) {  // inclusive scans of pre[1..B] (warp 0) and prc[1..B] (warp 1)
@@ -605,11 +669,18 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
       const int cost = p.Hkv * prc[p.B];
       // at least one tile per share, so that every CTA between the first and
       // the last owner of a (row, head) owns one of its tiles
-      it0.qc = max(kTileCost, (cost + grid - 1) / grid);
+      if (cost >= kTileCost * grid) {
+        it0.sh.num = cost;
+        it0.sh.den = grid;
+      } else {
+        it0.sh.num = kTileCost;
+        it0.sh.den = 1;
+      }
       it0.pos = it0.end = 0;   // the producer warp finds its range (locate_range)
       it0.hb = -1;
     } else {
-      it0.qc = 1;
+      it0.sh.num = 1;
+      it0.sh.den = 1;
       it0.hb = -1;
       it0.pos = static_cast<int>(1LL * total * blockIdx.x / gridDim.x);
       it0.end = static_cast<int>(1LL * total * (blockIdx.x + 1) / gridDim.x);
@@ -617,9 +688,9 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
     itp = it0;   // the producer's share of the cost line (shared memory only)
     if (warp == kCWarps && p.fixed_splits == 0) {
       const int cost = p.Hkv * prc[p.B];
-      const long long c0 = 1LL * itp.qc * blockIdx.x, c1 = c0 + itp.qc;
-      locate_range(p, pre, prc, static_cast<int>(c0 < cost ? c0 : cost),
-                   static_cast<int>(c1 < cost ? c1 : cost), lane, itp);
+      const int c = static_cast<int>(blockIdx.x);
+      locate_range(p, pre, prc, share_bound(itp.sh, c, cost), share_bound(itp.sh, c + 1, cost),
+                   lane, itp);
     }
     // the consumer warps wait here; the producer warp also looks up its first
     // unit and that unit's pages first, and waits just before its first copy
@@ -627,16 +698,10 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
       pkv_wait_prior_grid();
       pkv_allow_next_grid();
     }
-    if (parts_out && warp < kCWarps) {  // parts per (row, kv head) for the combine
+    if (parts_out && warp < kCWarps) {  // fixed mode: parts per (row, kv head) for the combine
       for (int rh = blockIdx.x + gridDim.x * tid; rh < p.B * p.Hkv; rh += gridDim.x * kCThreads) {
-        const int b = rh / p.Hkv, g = rh - b * p.Hkv;
-        const int n = pre[b + 1] - pre[b];
-        int parts = n;
-        if (p.fixed_splits == 0 && n > 0) {
-          const int c0 = head_cost_start(p, prc, b, g);
-          parts = (c0 + kTileCost * (n - 1)) / it0.qc - c0 / it0.qc + 1;
-        }
-        parts_out[rh] = parts;
+        const int b = rh / p.Hkv;
+        parts_out[rh] = pre[b + 1] - pre[b];
       }
     }
   }
@@ -715,7 +780,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
     UnitIter it = itp;
     Unit w, wn;
     int it_k = 0, it_v = 0, it_q = 0;
-    bool ok = true;
+    bool ok = true, merge_copy = false;
     bool have = next_unit(p, rows, pre, prc, it, w, lane);
     int page_first = have ? box_page(w, lane) : -1;
     pkv_wait_prior_grid();
@@ -723,6 +788,13 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
       bool have_next = false, looked_ahead = false;
       int page_next = -1;
       const int n_boxes = (w.tb - w.ta) * boxes;
+      // The first part of a (row, head) cut across CTAs is this CTA's last
+      // unit: look at the later parts' flags now (relaxed loads, not waited
+      // on) so that their state is known when the unit's tiles are issued.
+      const bool merge_unit = p.fixed_splits == 0 && w.part == 0 && w.parts > 1;
+      unsigned *const fbase = flags + (static_cast<size_t>(w.b) * p.Hkv + w.g) * p.max_parts;
+      const unsigned fpeek =
+          merge_unit && 1 + lane < w.parts ? ld_relaxed_gpu(fbase + 1 + lane) : 0u;
       // query rows of the GQA group, one bulk copy per head into padded rows
       {
         const int qs = it_q & 1;
@@ -849,6 +921,28 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
         have_next = next_unit(p, rows, pre, prc, it, wn, lane);
         page_next = have_next ? box_page(wn, lane) : -1;
       }
+      if (ok && merge_unit) {
+        // Wait for the later parts' partials, then copy part 1's (o, then
+        // lse) into the two Q stages, free once the consumers hold this
+        // unit's query rows; the consumers merge at the unit's end.
+        ok = wait_parts(fbase, w.parts, lane, abort_flag, fpeek);
+        if (ok && lane == 0)
+          ok = mbar_wait(emptyQ + 8 * (it_q & 1), ((it_q >> 1) & 1) ^ 1, abort_flag) &&
+               mbar_wait(emptyQ + 8 * ((it_q + 1) & 1), (((it_q + 1) >> 1) & 1) ^ 1, abort_flag);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (ok) {
+          const size_t r1 = (static_cast<size_t>(w.b) * p.Hkv + w.g) * p.max_parts + 1;
+          float *mbuf = reinterpret_cast<float *>(sm + Cf::OFF_Q);
+          if (lane < p.G) mbuf[p.G * D + lane] = __ldcg(lse_part + r1 * p.G + lane);
+          __syncwarp();
+          if (lane == 0) {
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+            mbar_expect_tx(mergeBar, static_cast<uint32_t>(p.G * D * 4));
+            bulk_load(sQ, o_part + r1 * p.G * D, static_cast<uint32_t>(p.G * D * 4), mergeBar);
+          }
+          merge_copy = true;
+        }
+      }
       w = wn;
       page_first = page_next;
       have = have_next;
@@ -885,6 +979,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
         (void)mbar_wait(fullQ + 8 * s, (last / 2) & 1, &no_abort);
       }
     }
+    if (merge_copy) (void)mbar_wait(mergeBar, 0, &no_abort);
     return;
   }
 
@@ -1000,8 +1095,9 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
         qb[ks][0] = hv ? qrow[(16 * ks + 2 * tig) >> 1] : 0u;
         qb[ks][1] = hv ? qrow[(16 * ks + 8 + 2 * tig) >> 1] : 0u;
       }
-      // the fused step keeps the stage (its k / v rows) until the unit ends
-      if (!STEP) {
+      // a fused-step unit that appends the row's new token keeps the stage
+      // (its k / v rows) until the unit ends; every other unit frees it now
+      if (!STEP || patch < 0) {
         __syncwarp();
         if (lane == 0) mbar_arrive(emptyQ + 8 * qs);
       }
@@ -1160,58 +1256,122 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
       __syncwarp();
       if (lane == 0) mbar_arrive(emptyV + 8 * st);
     }
-    if constexpr (STEP) {   // the unit's Q stage (and its k / v rows) is free
+    if (STEP && patch >= 0) {   // the unit's Q stage (and its k / v rows) is free
       __syncwarp();
       if (lane == 0) mbar_arrive(emptyQ + 8 * qs);
     }
 
     if (failed) continue;
-    // ---- epilogue: direct output for one-part rows, else a partial ----
+    // ---- epilogue ----
+    // A (row, head) done inside one CTA writes its output directly. A later
+    // part of a cut one (every part, in the fixed mode) writes its partial:
+    // o / l and lse = m + log2(l) per head, in the (row, kv head)'s record
+    // for that part. The first part of a cut one (balanced mode) merges the
+    // later parts' partials into its own running state and writes the output.
+    const bool balanced = p.fixed_splits == 0;
+    const bool merge = balanced && w.parts > 1 && w.part == 0;
+    const size_t head0 = static_cast<size_t>(w.b) * p.Hq + static_cast<size_t>(w.g) * p.G;
+    const size_t rec = (static_cast<size_t>(w.b) * p.Hkv + w.g) * p.max_parts;
+    if (w.parts > 1 && !merge) {
+      const float il0 = l_run0 > 0.f ? 1.f / l_run0 : 0.f;
+      const float il1 = l_run1 > 0.f ? 1.f / l_run1 : 0.f;
+      float *op = o_part + (rec + w.part) * p.G * D;
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        const int d = warp * (D / 4) + 16 * mt + gid;
+        if (hv0) {
+          op[h0 * D + d] = o[mt][0] * il0;
+          op[h0 * D + d + 8] = o[mt][2] * il0;
+        }
+        if (hv1) {
+          op[h1 * D + d] = o[mt][1] * il1;
+          op[h1 * D + d + 8] = o[mt][3] * il1;
+        }
+      }
+      if (warp == 0 && gid == 0) {
+        float *lp = lse_part + (rec + w.part) * p.G;
+        if (hv0) lp[h0] = l_run0 > 0.f ? m_run0 + log2f(l_run0) : -INFINITY;
+        if (hv1) lp[h1] = l_run1 > 0.f ? m_run1 + log2f(l_run1) : -INFINITY;
+      }
+      if (balanced) {   // publish the partial to the first part's CTA
+        // the barrier orders every consumer's stores before thread 0's
+        // gpu-scope release (cumulative), which the reader acquires
+        consumer_sync();
+        if (tid == 0)
+          asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(flags + rec + w.part), "r"(1u)
+                       : "memory");
+      }
+      continue;
+    }
+    if (merge) {
+      // The producer has seen every later part's flag and copied part 1's
+      // partial (o [G][D], then lse [G]) into the Q stages; later parts, when
+      // a row is cut more than twice, are read from the workspace.
+      if (!mbar_wait(mergeBar, 0, abort_flag)) {
+        failed = true;
+        *abort_flag = 1;
+        continue;
+      }
+      const float *mbuf = reinterpret_cast<const float *>(sm + Cf::OFF_Q);
+      for (int j = 1; j < w.parts; ++j) {
+        const bool in_smem = j == 1;
+        const float *op = in_smem ? mbuf : o_part + (rec + j) * p.G * D;
+        const float *lp = in_smem ? mbuf + p.G * D : lse_part + (rec + j) * p.G;
+        auto ld = [&](const float *a) { return in_smem ? *a : __ldcg(a); };
+        const float ls0 = hv0 ? ld(lp + h0) : -INFINITY;
+        const float ls1 = hv1 ? ld(lp + h1) : -INFINITY;
+        float v[MT][4];
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+          const int d = warp * (D / 4) + 16 * mt + gid;
+          v[mt][0] = hv0 ? ld(op + h0 * D + d) : 0.f;
+          v[mt][2] = hv0 ? ld(op + h0 * D + d + 8) : 0.f;
+          v[mt][1] = hv1 ? ld(op + h1 * D + d) : 0.f;
+          v[mt][3] = hv1 ? ld(op + h1 * D + d + 8) : 0.f;
+        }
+        const float mn0 = fmaxf(m_run0, ls0), mn1 = fmaxf(m_run1, ls1);
+        const float mu0 = mn0 == -INFINITY ? 0.f : mn0;
+        const float mu1 = mn1 == -INFINITY ? 0.f : mn1;
+        const float a0 = exp2f(m_run0 - mu0), b0 = exp2f(ls0 - mu0);
+        const float a1 = exp2f(m_run1 - mu1), b1 = exp2f(ls1 - mu1);
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+          o[mt][0] = fmaf(o[mt][0], a0, v[mt][0] * b0);
+          o[mt][2] = fmaf(o[mt][2], a0, v[mt][2] * b0);
+          o[mt][1] = fmaf(o[mt][1], a1, v[mt][1] * b1);
+          o[mt][3] = fmaf(o[mt][3], a1, v[mt][3] * b1);
+        }
+        l_run0 = fmaf(l_run0, a0, b0);
+        l_run1 = fmaf(l_run1, a1, b1);
+        m_run0 = mn0;
+        m_run1 = mn1;
+      }
+    }
     const float il0 = l_run0 > 0.f ? 1.f / l_run0 : 0.f;
     const float il1 = l_run1 > 0.f ? 1.f / l_run1 : 0.f;
-    const size_t head0 = static_cast<size_t>(w.b) * p.Hq + static_cast<size_t>(w.g) * p.G;
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) {
       const int d = warp * (D / 4) + 16 * mt + gid;
-      if (w.parts == 1) {
-        if (hv0) {
-          out[(head0 + h0) * D + d] = __float2bfloat16_rn(o[mt][0] * il0);
-          out[(head0 + h0) * D + d + 8] = __float2bfloat16_rn(o[mt][2] * il0);
-        }
-        if (hv1) {
-          out[(head0 + h1) * D + d] = __float2bfloat16_rn(o[mt][1] * il1);
-          out[(head0 + h1) * D + d + 8] = __float2bfloat16_rn(o[mt][3] * il1);
-        }
-      } else {
-        if (hv0) {
-          float *op = o_part + ((head0 + h0) * p.max_parts + w.part) * D;
-          op[d] = o[mt][0] * il0;
-          op[d + 8] = o[mt][2] * il0;
-        }
-        if (hv1) {
-          float *op = o_part + ((head0 + h1) * p.max_parts + w.part) * D;
-          op[d] = o[mt][1] * il1;
-          op[d + 8] = o[mt][3] * il1;
-        }
+      if (hv0) {
+        out[(head0 + h0) * D + d] = __float2bfloat16_rn(o[mt][0] * il0);
+        out[(head0 + h0) * D + d + 8] = __float2bfloat16_rn(o[mt][2] * il0);
       }
-    }
-    if (w.parts > 1 && warp == 0 && gid == 0) {
-      if (hv0)
-        lse_part[(head0 + h0) * p.max_parts + w.part] =
-            l_run0 > 0.f ? m_run0 + log2f(l_run0) : -INFINITY;
-      if (hv1)
-        lse_part[(head0 + h1) * p.max_parts + w.part] =
-            l_run1 > 0.f ? m_run1 + log2f(l_run1) : -INFINITY;
+      if (hv1) {
+        out[(head0 + h1) * D + d] = __float2bfloat16_rn(o[mt][1] * il1);
+        out[(head0 + h1) * D + d + 8] = __float2bfloat16_rn(o[mt][3] * il1);
+      }
     }
   }
 }
 
-// Merge the parts of one (row, head) with weights 2^(lse_c - max), skipping
-// parts without keys (lse = -inf). (Row, head) pairs handled by one CTA were
-// written by the attention kernel itself. One warp per (row, head); lane l
-// merges output columns 4l + 128c. The part count, the log-sum-exps and the
-// first two partials are loaded together, so the common two-part merge needs
-// one round trip to L2 after the attention kernel completes.
+// Fixed split mode: merge the parts of one (row, head) with weights
+// 2^(lse_c - max), skipping parts without keys (lse = -inf). (Row, head)
+// pairs handled by one CTA were written by the attention kernel itself. One
+// warp per (row, head); lane l merges output columns 4l + 128c. The part
+// count, the log-sum-exps and the first two partials are loaded together, so
+// a two-part merge needs one round trip to L2 after the attention kernel
+// completes. Part s of query head hi of (row b, kv head g) sits in record
+// (b * Hkv + g) * max_parts + s: o at [hi][D] of a [G][D] block, lse at [hi].
 template <int D>
 __global__ void combine_kernel(const float *__restrict__ o_part,
                                const float *__restrict__ lse_part,
@@ -1226,24 +1386,26 @@ __global__ void combine_kernel(const float *__restrict__ o_part,
   const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (r >= p.B * p.Hq) return;
-  const int b = r / p.Hq, g = (r - b * p.Hq) / p.G;
-  const float *lse = lse_part + static_cast<size_t>(r) * p.max_parts;
-  const float *op = o_part + static_cast<size_t>(r) * p.max_parts * D;
+  const int b = r / p.Hq, hh = r - b * p.Hq, g = hh / p.G, hi = hh - g * p.G;
+  const size_t rec = (static_cast<size_t>(b) * p.Hkv + g) * p.max_parts;
+  const size_t pstride = static_cast<size_t>(p.G) * D;     // floats between parts
+  const float *lse = lse_part + rec * p.G + hi;              // part s at lse[s * G]
+  const float *op = o_part + rec * pstride + static_cast<size_t>(hi) * D;
   const int parts = __ldcg(parts_in + b * p.Hkv + g);
-  float my_lse = lane < p.max_parts ? __ldcg(lse + lane) : -INFINITY;
+  float my_lse = lane < p.max_parts ? __ldcg(lse + lane * p.G) : -INFINITY;
   float4 v0[CH], v1[CH];   // parts 0 and 1 (max_parts >= 2 whenever this kernel runs)
 #pragma unroll
   for (int c = 0; c < CH; ++c) {
     const int d = 4 * lane + 128 * c;
     if (d < D) {
       v0[c] = __ldcg(reinterpret_cast<const float4 *>(op + d));
-      v1[c] = __ldcg(reinterpret_cast<const float4 *>(op + D + d));
+      v1[c] = __ldcg(reinterpret_cast<const float4 *>(op + pstride + d));
     }
   }
   if (parts <= 1) return;
   if (lane >= parts) my_lse = -INFINITY;
   float m = my_lse;
-  for (int s = 32 + lane; s < parts; s += 32) m = fmaxf(m, __ldcg(lse + s));
+  for (int s = 32 + lane; s < parts; s += 32) m = fmaxf(m, __ldcg(lse + s * p.G));
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
   __nv_bfloat16 *orow = out + static_cast<size_t>(r) * D;
@@ -1255,10 +1417,10 @@ __global__ void combine_kernel(const float *__restrict__ o_part,
     float wsum = 0.f;
     if (m != -INFINITY) {
       for (int s = 0; s < parts; ++s) {
-        const float l = s < 32 ? __shfl_sync(0xffffffffu, my_lse, s) : __ldcg(lse + s);
+        const float l = s < 32 ? __shfl_sync(0xffffffffu, my_lse, s) : __ldcg(lse + s * p.G);
         const float4 v = s == 0   ? v0[c]
                          : s == 1 ? v1[c]
-                                  : __ldcg(reinterpret_cast<const float4 *>(op + static_cast<size_t>(s) * D + d));
+                                  : __ldcg(reinterpret_cast<const float4 *>(op + s * pstride + d));
         const float wgt = l == -INFINITY ? 0.f : exp2f(l - m);
         wsum += wgt;
         acc.x = fmaf(wgt, v.x, acc.x);
@@ -1343,7 +1505,7 @@ template <int D, bool STEP>
 int launch_attn(const CUtensorMap &tmK, const CUtensorMap &tmV, const CUtensorMap &tmK3,
                 const CUtensorMap &tmV3, const pkv_bf16 *q,
                 const Problem &p, float scale_log2, float *o_part, float *lse_part,
-                int *parts, pkv_bf16 *out, int32_t *err, const StepArgs &sa,
+                int *parts, unsigned *flags, pkv_bf16 *out, int32_t *err, const StepArgs &sa,
                 cudaStream_t stream) {
   int st = set_smem_attr<D, STEP>();
   if (st != PKV_OK) return st;
@@ -1353,7 +1515,7 @@ int launch_attn(const CUtensorMap &tmK, const CUtensorMap &tmV, const CUtensorMa
   PKV_CUDA_CHECK(pkv::launch_pdl(decode_attn_kernel<D, STEP>, dim3(grid), dim3(kThreads),
                                  Cfg<D>::SMEM, stream, tmK, tmV, tmK3, tmV3,
                                  reinterpret_cast<const __nv_bfloat16 *>(q), p, scale_log2,
-                                 o_part, lse_part, parts,
+                                 o_part, lse_part, parts, flags,
                                  reinterpret_cast<__nv_bfloat16 *>(out), err, sa));
   return PKV_OK;
 }
@@ -1370,19 +1532,31 @@ int max_parts_for(int max_pages, int page_size, int window, int num_splits) {
 
 }  // namespace
 
-extern "C" {
-
-// Workspace layout: [parts per (row, kv head): B*Hq ints, 256-byte padded]
-// [o_part fp32 B*Hq*P*D][lse_part fp32 B*Hq*P]; every field is written by a
-// call before it is read, so the workspace needs no initialisation.
-size_t parts_bytes(int B, int Hq) {
+static size_t parts_bytes(int B, int Hq) {
   return (static_cast<size_t>(B) * Hq * sizeof(int) + 255) & ~size_t(255);
 }
+
+int pkv::decode_max_parts(int max_pages_per_seq, int page_size, int window, int num_splits) {
+  if (max_pages_per_seq < 1 || page_size < 1 || num_splits < 0) return 0;
+  return max_parts_for(max_pages_per_seq, page_size, window, num_splits);
+}
+
+extern "C" {
+
+// Workspace layout, with P the parts a (row, kv head) may be cut into:
+//   [parts per (row, kv head) for the fixed mode's combine: B*Hq ints, 256-byte padded]
+//   [o_part fp32: B*Hkv*P records of G*D, = B*Hq*P*D]
+//   [lse_part fp32: B*Hkv*P records of G, = B*Hq*P]
+//   [flags u32: one per (row, kv head, part), B*Hq*P words reserved]
+// Partials and counts are written before they are read. The flags must be
+// zero before the first call; every call that completes without
+// PKV_ERR_TIMEOUT leaves them zero again.
 
 size_t paged_decode_attn_workspace(int B, int Hq, int D, int num_splits) {
   if (num_splits <= 1 || B <= 0 || Hq <= 0 || D <= 0) return 0;
   const size_t rows = static_cast<size_t>(B) * Hq * num_splits;
-  return parts_bytes(B, Hq) + rows * D * sizeof(float) + rows * sizeof(float);
+  return parts_bytes(B, Hq) + rows * D * sizeof(float) + rows * sizeof(float) +
+         rows * sizeof(unsigned);
 }
 
 int paged_decode_attn_splits(int B, int Hkv, int D, int max_pages_per_seq,
@@ -1394,6 +1568,15 @@ int paged_decode_attn_splits(int B, int Hkv, int D, int max_pages_per_seq,
 }
 
 }  // extern "C"
+
+void pkv::decode_flags_region(int B, int Hq, int D, int parts, size_t *offset, size_t *bytes) {
+  *offset = *bytes = 0;
+  if (paged_decode_attn_workspace(B, Hq, D, parts) == 0) return;
+  const size_t rows = static_cast<size_t>(B) * Hq * parts;
+  *offset = parts_bytes(B, Hq) + rows * D * sizeof(float) + rows * sizeof(float);
+  *bytes = rows * sizeof(unsigned);
+}
+
 
 namespace {
 
@@ -1456,10 +1639,12 @@ int decode_common(const char *fn, const pkv_bf16 *q, const pkv_bf16 *k_cache,
   }
   int *parts = nullptr;
   float *o_part = nullptr, *lse_part = nullptr;
+  unsigned *flags = nullptr;
   if (need > 0) {
     parts = static_cast<int *>(workspace);
     o_part = reinterpret_cast<float *>(static_cast<char *>(workspace) + parts_bytes(B, Hq));
     lse_part = o_part + static_cast<size_t>(B) * Hq * max_parts * D;
+    flags = reinterpret_cast<unsigned *>(lse_part + static_cast<size_t>(B) * Hq * max_parts);
   }
   const int box_rows = page_size < kT ? page_size : kT;
   CUtensorMap tmK, tmV, tmK3, tmV3;
@@ -1495,15 +1680,20 @@ int decode_common(const char *fn, const pkv_bf16 *q, const pkv_bf16 *k_cache,
   // with at most one part per row no partial is ever written
   p.fixed_splits = max_parts == 1 ? 1 : num_splits;
   p.max_parts = max_parts;
+  p.unit_cost = kUnitCost;
+  // the balanced mode merges cut rows inside the attention kernel; only the
+  // fixed mode needs the per-row part counts and the combine kernel
+  const bool combine = p.fixed_splits > 0 && max_parts > 1;
+  if (!combine) parts = nullptr;
   const float scale_log2 = scale * 1.4426950408889634f;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const StepArgs none = {};
   const StepArgs &a = sa ? *sa : none;
 #define PKV_LAUNCH(DD)                                                                        \
-  st = sa ? launch_attn<DD, true>(tmK, tmV, tmK3, tmV3, q, p, scale_log2, o_part, lse_part, parts, out,   \
-                                  err_word, a, s)                                             \
-          : launch_attn<DD, false>(tmK, tmV, tmK3, tmV3, q, p, scale_log2, o_part, lse_part, parts, out,  \
-                                   err_word, a, s)
+  st = sa ? launch_attn<DD, true>(tmK, tmV, tmK3, tmV3, q, p, scale_log2, o_part, lse_part,    \
+                                  parts, flags, out, err_word, a, s)                          \
+          : launch_attn<DD, false>(tmK, tmV, tmK3, tmV3, q, p, scale_log2, o_part, lse_part,   \
+                                   parts, flags, out, err_word, a, s)
   switch (D) {
     case 64: PKV_LAUNCH(64); break;
     case 128: PKV_LAUNCH(128); break;
@@ -1512,7 +1702,7 @@ int decode_common(const char *fn, const pkv_bf16 *q, const pkv_bf16 *k_cache,
   }
 #undef PKV_LAUNCH
   if (st != PKV_OK) return st;
-  if (max_parts > 1) {
+  if (combine) {
     const int rows_bh = B * Hq;
     const int wpb = 4;
     auto *kern = D == 64    ? combine_kernel<64>

@@ -11,11 +11,12 @@
 //
 // The scratch is a file-scope __device__ array of kNoallocScratchBytes. Every
 // GPU that loads the library holds that much device memory until the process
-// exits. All calls share it and it keeps the last call's contents; nothing in
-// it needs to start at zero (every partial result is written before it is
-// read). Two calls whose kernels overlap on the GPU (for instance on two
-// streams, or from two threads) race on the scratch and corrupt each other's
-// results: serialize them.
+// exits. All calls share it and it keeps the last call's contents. The split
+// partials are written before they are read; the per-part flags must start
+// at zero, so every call clears them first (one cudaMemsetAsync on the
+// caller's stream, no allocation). Two calls whose kernels overlap on the GPU
+// (for instance on two streams, or from two threads) race on the scratch and
+// corrupt each other's results: serialize them.
 //
 // The first call on each device looks the array's device address up with
 // cudaGetSymbolAddress while that device is current, and caches it; make that
@@ -70,22 +71,29 @@ int paged_decode_attn_noalloc(const pkv_bf16 *q, const pkv_bf16 *k_cache,
                               int B, int Hq, int Hkv, int D, int num_splits,
                               pkv_bf16 *out, int32_t *err_word, void *stream) {
   if (num_splits < 0) return pkv::fail(PKV_E_BAD_ARG, "paged_decode_attn_noalloc: num_splits < 0");
-  // most parts a row can be cut into: the fixed count, or the automatic bound
-  int splits = num_splits;
-  if (splits == 0) {
-    int st = paged_decode_attn_splits(B, Hkv, D, max_pages_per_seq, page_size, window, &splits);
-    if (st != PKV_OK) return st;
-  }
-  const size_t need = paged_decode_attn_workspace(B, Hq, D, splits);
+  if (max_pages_per_seq < 1 || page_size < 1)
+    return pkv::fail(PKV_E_BAD_ARG, "paged_decode_attn_noalloc: bad size argument");
+  // the parts paged_decode_attn will actually cut a row into: num_splits
+  // capped at the tiles of the longest row the table can hold (the same cap
+  // it applies), so a large num_splits on short rows needs little scratch
+  const int parts = pkv::decode_max_parts(max_pages_per_seq, page_size, window, num_splits);
+  const size_t need = paged_decode_attn_workspace(B, Hq, D, parts);
   if (need > kNoallocScratchBytes)
     return pkv::fail(PKV_E_BAD_ARG,
-                     "paged_decode_attn_noalloc: %d splits x %d rows x %d heads x D=%d need "
+                     "paged_decode_attn_noalloc: %d parts x %d rows x %d heads x D=%d need "
                      "%zu bytes of scratch, more than the fixed %zu; use paged_decode_attn "
                      "with a caller workspace, or fewer splits",
-                     splits, B, Hq, D, need, kNoallocScratchBytes);
+                     parts, B, Hq, D, need, kNoallocScratchBytes);
   void *scratch = nullptr;
   int st = scratch_address(&scratch);
   if (st != PKV_OK) return st;
+  // the part flags must be zero when a call starts; a call leaves them zero
+  // unless it gave up on a wait, so clear them every time (no allocation)
+  size_t off = 0, bytes = 0;
+  pkv::decode_flags_region(B, Hq, D, parts, &off, &bytes);
+  if (bytes > 0)
+    PKV_CUDA_CHECK(cudaMemsetAsync(static_cast<char *>(scratch) + off, 0, bytes,
+                                   static_cast<cudaStream_t>(stream)));
   return paged_decode_attn(q, k_cache, v_cache, dev_table, n_slots, max_pages_per_seq,
                            page_size, n_pages, batch_idx, seq_lens, window, scale, B, Hq, Hkv,
                            D, num_splits, scratch, kNoallocScratchBytes, out, err_word, stream);

@@ -21,6 +21,14 @@ int ok();
 // Number of SMs of the current device (cached per device; 0 if unknown).
 int sm_count();
 
+// Most parts paged_decode_attn cuts one (row, head) into for these arguments
+// (num_splits 0 = automatic), the count its workspace is sized for with
+// paged_decode_attn_workspace; 0 if the arguments are out of range.
+int decode_max_parts(int max_pages_per_seq, int page_size, int window, int num_splits);
+// Byte offset and size of the part flags inside a workspace sized by
+// paged_decode_attn_workspace(B, Hq, D, parts) (both 0 when it is empty).
+void decode_flags_region(int B, int Hq, int D, int parts, size_t *offset, size_t *bytes);
+
 // Document-causal prefill attention on tcgen05 (prefill_tc.cu), D in {64, 128};
 // arguments already validated by the public entry point.
 template <int D>

@@ -58,7 +58,9 @@ class AttnWorkspace:
     """Split mode and workspace for one (B, Hq, Hkv, D, table, window) shape.
 
     num_splits 0 is the automatic, length-balanced mode; the workspace is
-    sized for the most parts a row can be cut into in that mode."""
+    sized for the most parts a row can be cut into in that mode. It starts
+    zeroed: the automatic mode's part flags must be zero before the first
+    call (each call leaves them zero)."""
 
     def __init__(self, B, Hq, Hkv, D, max_pages_per_seq, page_size, window, device,
                  num_splits: int = 0):
@@ -66,7 +68,7 @@ class AttnWorkspace:
         self.max_parts = num_splits or paged_decode_attn_splits(B, Hkv, D, max_pages_per_seq,
                                                                 page_size, window)
         n = paged_decode_attn_workspace(B, Hq, D, self.max_parts)
-        self.buf = torch.empty(n, dtype=torch.uint8, device=device) if n else None
+        self.buf = torch.zeros(n, dtype=torch.uint8, device=device) if n else None
 
 
 def decode_layer_step(spec: LayerSpec, pt: PageTable, k_cache, v_cache, q, k, v, batch_idx,

@@ -57,12 +57,45 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls(dev):
         assert_attn_close(f64(got), ref)
 
 
-def test_noalloc_rejects_partials_beyond_its_scratch(dev):
-    case = PagedCase(np.random.default_rng(43), 2, 8, 1, 512, 64, [100, 100])
+def test_noalloc_accepts_split_counts_beyond_the_rows_tiles(dev):
+    # num_splits is capped at the tiles of the longest row the table holds
+    # (here 2 pages of 64 keys, so 2 parts), as paged_decode_attn caps it: a
+    # huge split count needs only a few KB of scratch and gives the same result
+    case = PagedCase(np.random.default_rng(44), 3, 16, 2, 128, 64, [100, 7, 128])
+    scale = 1.0 / math.sqrt(case.D)
+    for _ in range(2):
+        got, err = _noalloc(case, dev, 0, scale, 2100)
+        assert pkv.pkv_read_error_word(err) == 0
+        want, _ = run_attn(pkv, case, dev, 0, scale, 2100)
+        assert_attn_close(f64(got), f64(want))
+        ref, _ = case.oracle(0, scale)
+        assert_attn_close(f64(got), ref)
+
+
+@pytest.mark.parametrize("splits", [0, 33])
+def test_noalloc_rejects_partials_beyond_its_scratch(dev, splits):
+    # 64 rows x 8 heads x D=512 with a table of 40 pages of 64 keys: the
+    # automatic mode may cut a row into 40 parts, 64*8*40*(512+1)*4 bytes
+    # (42 MB); a fixed 33 parts need 64*8*33*513*4 bytes (34.7 MB). Both are
+    # beyond the 32 MiB scratch; the call is refused before any launch.
+    case = PagedCase(np.random.default_rng(43), 64, 8, 1, 512, 64, [10] * 64, max_pages=40)
     d = case.device(dev)
-    out = torch.empty((2, 8, 512), dtype=torch.bfloat16, device=dev)
-    # 2 rows x 8 heads x 2100 splits x (512 + 1) x 4 bytes > 32 MiB
+    out = torch.empty((64, 8, 512), dtype=torch.bfloat16, device=dev)
     with pytest.raises(pkv.BadArgError, match="scratch"):
         pkv.paged_decode_attn_noalloc(d["q"], d["kc"], d["vc"], d["table"], case.n_slots,
                                       case.max_pages, case.ps, case.P, d["bidx"], d["lens"], 0,
-                                      0.04, 2100, out)
+                                      0.04, splits, out)
+
+
+def test_noalloc_accepts_the_largest_split_count_that_fits(dev):
+    # the same table with 31 fixed parts: 64*8*31*513*4 bytes plus the part
+    # counts, just under 32 MiB, so the call runs and matches paged_decode_attn
+    case = PagedCase(np.random.default_rng(45), 64, 8, 1, 512, 64,
+                     np.random.default_rng(46).integers(1, 300, size=64), max_pages=40)
+    assert pkv.paged_decode_attn_workspace(64, 8, 512, 31) <= 32 << 20
+    assert pkv.paged_decode_attn_workspace(64, 8, 512, 32) > 32 << 20
+    scale = 1.0 / math.sqrt(case.D)
+    got, err = _noalloc(case, dev, 0, scale, 31)
+    assert pkv.pkv_read_error_word(err) == 0
+    want, _ = run_attn(pkv, case, dev, 0, scale, 31)
+    assert_attn_close(f64(got), f64(want))
