@@ -85,10 +85,8 @@ struct Cfg {
   static constexpr int OFF_ROWS = OFF_DESC + 2 * 48;              // int2 [kMaxRows]
   static constexpr int OFF_PRE = OFF_ROWS + kMaxRows * 8;         // int [kMaxRows + 1]
   static constexpr int OFF_PRC = OFF_PRE + (kMaxRows + 1) * 4;    // int [kMaxRows + 1]
-  // fused step only: rotation factors of the unit's row (f32 cos[D/2],
-  // sin[D/2]) and the norm gains (bf16 [D] each)
-  static constexpr int OFF_FAC = (OFF_PRC + (kMaxRows + 1) * 4 + 15) & ~15;
-  static constexpr int OFF_GAM = OFF_FAC + 4 * D;
+  // fused step only: the norm gains (bf16 [D] each)
+  static constexpr int OFF_GAM = (OFF_PRC + (kMaxRows + 1) * 4 + 15) & ~15;
   static constexpr int SMEM = OFF_GAM + 4 * D + 1024;  // + alignment
   static constexpr int CTAS_PER_SM = D <= 128 ? 2 : 1;
 };
@@ -112,6 +110,11 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
 __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
                "r"(bytes)
+               : "memory");
+}
+// Raises the transaction count of the current phase without arriving.
+__device__ __forceinline__ void mbar_expect_tx_only(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes)
                : "memory");
 }
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
@@ -931,15 +934,18 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
                mbar_wait(emptyQ + 8 * ((it_q + 1) & 1), (((it_q + 1) >> 1) & 1) ^ 1, abort_flag);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (ok) {
+          // the o copy and the lse loads travel together; the phase completes
+          // once the copy has landed and lane 0 has arrived after the stores
           const size_t r1 = (static_cast<size_t>(w.b) * p.Hkv + w.g) * p.max_parts + 1;
           float *mbuf = reinterpret_cast<float *>(sm + Cf::OFF_Q);
-          if (lane < p.G) mbuf[p.G * D + lane] = __ldcg(lse_part + r1 * p.G + lane);
-          __syncwarp();
           if (lane == 0) {
             asm volatile("fence.proxy.async.global;" ::: "memory");
-            mbar_expect_tx(mergeBar, static_cast<uint32_t>(p.G * D * 4));
+            mbar_expect_tx_only(mergeBar, static_cast<uint32_t>(p.G * D * 4));
             bulk_load(sQ, o_part + r1 * p.G * D, static_cast<uint32_t>(p.G * D * 4), mergeBar);
           }
+          if (lane < p.G) mbuf[p.G * D + lane] = __ldcg(lse_part + r1 * p.G + lane);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(mergeBar);
           merge_copy = true;
         }
       }
@@ -991,6 +997,10 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
   constexpr int MT = D / 64;  // 16-row m-tiles of this warp's D/4 slice
   int it = 0, it_q = 0;
   bool failed = false;
+  // fused step: this lane's rotation factors and the row they belong to
+  constexpr int PAIRS = (D / 2 + 31) / 32;
+  float cf[PAIRS], sf[PAIRS];
+  int fac_b = -1;
 
   while (true) {
     uint32_t qb[KS][2];
@@ -1012,34 +1022,37 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
     }
     {
       if constexpr (STEP) {
-        // Rotate the raw query rows in place with the row's rotation factors
-        // (computed once, one pair per thread). The unit that holds the row's
-        // last tile also rotates the new k in place, writes k and v to their
-        // cache row (the kv_append of the chain) and later patches both into
-        // that tile, whose TMA copy may predate the write.
-        constexpr int PAIRS = (D / 2 + 31) / 32;
+        // Rotate the raw query rows in place. Lane l of every warp rotates
+        // the pairs (l + 32 j, l + 32 j + D/2) of its rows, so each lane needs
+        // only its own pairs' factors: computed in registers, once per row
+        // (consecutive units of one row reuse them). The unit that holds the
+        // row's last tile also rotates the new k in place, writes k and v to
+        // their cache row (the kv_append of the chain) and later patches both
+        // into that tile, whose TMA copy may predate the write.
         const int c_b = rows[w.b].y;
         const int L_b = c_b & ~kClampBit;
         const int app_b = w.app;
         const int pos_b = c_b < 0 ? __ldg(p.seq_lens + w.b) : L_b - 1;
-        const float fpos = static_cast<float>(pos_b);
-        float *fac = reinterpret_cast<float *>(sm + Cf::OFF_FAC);
-        for (int i = tid; i < D / 2; i += kCThreads) {
-          float cs, sn;
-          pkv_rope_factor(i, D, fpos, sa.log2_theta, sa.rot_pairs, cs, sn);
-          fac[i] = cs;
-          fac[D / 2 + i] = sn;
+        if (w.b != fac_b) {
+          const float fpos = static_cast<float>(pos_b);
+#pragma unroll
+          for (int j = 0; j < PAIRS; ++j) {
+            const int i = lane + 32 * j;
+            if (i < D / 2) pkv_rope_factor(i, D, fpos, sa.log2_theta, sa.rot_pairs, cf[j], sf[j]);
+          }
+          fac_b = w.b;
         }
-        consumer_sync();
         const __nv_bfloat16 *gq =
             sa.gamma_q ? reinterpret_cast<const __nv_bfloat16 *>(sm + Cf::OFF_GAM) : nullptr;
-        auto table_factor = [&](int i, float &cs, float &sn) {
-          cs = fac[i];
-          sn = fac[D / 2 + i];
-        };
         auto rotate_row = [&](__nv_bfloat16 *x, const __nv_bfloat16 *g, float (&lo)[PAIRS],
                               float (&hi)[PAIRS]) {
-          pkv_norm_rope_core<PAIRS>(x, g, sa.eps, D, lane, table_factor, lo, hi);
+          pkv_norm_rope_core<PAIRS>(
+              x, g, sa.eps, D, lane,
+              [&](int j, int, float &cs, float &sn) {
+                cs = cf[j];
+                sn = sf[j];
+              },
+              lo, hi);
 #pragma unroll
           for (int j = 0; j < PAIRS; ++j) {
             const int i = lane + 32 * j;

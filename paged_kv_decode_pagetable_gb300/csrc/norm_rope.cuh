@@ -13,8 +13,9 @@
 // out with _rn intrinsics (no contraction left to the compiler), and the
 // rotation factors (cos phi_i, sin phi_i) are a pure function of (i, D, pos,
 // theta) computed by pkv_rope_factor alone, so the standalone qk_norm_rope
-// kernel (factors inline) and the fused decode step (factors computed once
-// per row into shared memory) produce the same bits for the same input.
+// kernel (factors inline) and the fused decode step (each lane's factors
+// computed once per row and kept in registers) produce the same bits for the
+// same input.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -34,8 +35,9 @@ __device__ __forceinline__ void pkv_rope_factor(int i, int D, float pos, float l
   sincosf(__fmul_rn(pos, inv_freq), &sn, &cs);
 }
 
-// Norm + rotation with the factors supplied by factor(i, cs, sn). PAIRS >=
-// ceil(D / 64): register slots per lane. x and gamma may point to global or
+// Norm + rotation with the factors supplied by factor(j, i, cs, sn) for the
+// lane's j-th pair i = lane + 32 j. PAIRS >= ceil(D / 64): register slots per
+// lane. x and gamma may point to global or
 // shared memory; gamma == nullptr skips the norm.
 template <int PAIRS, typename Factor>
 __device__ __forceinline__ void pkv_norm_rope_core(const __nv_bfloat16 *x,
@@ -70,7 +72,7 @@ __device__ __forceinline__ void pkv_norm_rope_core(const __nv_bfloat16 *x,
         r2 = __fmul_rn(__fmul_rn(r2, inv_rms), __bfloat162float(g[i + half]));
       }
       float cs, sn;
-      factor(i, cs, sn);
+      factor(j, i, cs, sn);
       lo[j] = __fsub_rn(__fmul_rn(r1, cs), __fmul_rn(r2, sn));
       hi[j] = __fadd_rn(__fmul_rn(r2, cs), __fmul_rn(r1, sn));
     }
@@ -86,7 +88,7 @@ __device__ __forceinline__ void pkv_norm_rope_lane(const __nv_bfloat16 *x,
                                                    float (&hi)[PAIRS]) {
   pkv_norm_rope_core<PAIRS>(
       x, g, eps, D, lane,
-      [&](int i, float &cs, float &sn) {
+      [&](int, int i, float &cs, float &sn) {
         pkv_rope_factor(i, D, pos, log2_theta, rot_pairs, cs, sn);
       },
       lo, hi);
