@@ -61,6 +61,10 @@ constexpr int kSpinLimit = 1 << 22;
 // fused step stays bit-identical to the separate calls.
 constexpr int kTileCost = 4;
 constexpr int kUnitCost = 4;
+// Shortest share of the cost line a CTA gets (at least one tile's cost): a
+// call too small to give every CTA this much leaves the last CTAs idle
+// rather than cutting rows into many short parts.
+constexpr int kMinShare = kTileCost;
 
 template <int D>
 struct Cfg {
@@ -389,8 +393,8 @@ __device__ __forceinline__ int small_quotient_warp(int x, int d, int n, int lane
 // the line's length. Shares are at least one tile's cost long, so every CTA
 // strictly between the first and the last owner of a (row, head) owns one of
 // its tiles. Equal fractional shares (num = cost, den = grid) are used when
-// the line is long enough, else shares of exactly one tile (num = kTileCost,
-// den = 1).
+// the line is long enough, else shares of kMinShare (num = kMinShare,
+// den = 1), leaving the CTAs past the line's end idle.
 struct Share {
   long long num;
   int den;
@@ -672,11 +676,11 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
       const int cost = p.Hkv * prc[p.B];
       // at least one tile per share, so that every CTA between the first and
       // the last owner of a (row, head) owns one of its tiles
-      if (cost >= kTileCost * grid) {
+      if (cost >= kMinShare * grid) {
         it0.sh.num = cost;
         it0.sh.den = grid;
       } else {
-        it0.sh.num = kTileCost;
+        it0.sh.num = kMinShare;
         it0.sh.den = 1;
       }
       it0.pos = it0.end = 0;   // the producer warp finds its range (locate_range)
@@ -792,12 +796,14 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
       int page_next = -1;
       const int n_boxes = (w.tb - w.ta) * boxes;
       // The first part of a (row, head) cut across CTAs is this CTA's last
-      // unit: look at the later parts' flags now (relaxed loads, not waited
-      // on) so that their state is known when the unit's tiles are issued.
+      // unit: look at the later parts' flags (relaxed loads, not waited on)
+      // when the unit starts and again once all but its last tile are
+      // issued, so that their state is known when the last tile is.
       const bool merge_unit = p.fixed_splits == 0 && w.part == 0 && w.parts > 1;
       unsigned *const fbase = flags + (static_cast<size_t>(w.b) * p.Hkv + w.g) * p.max_parts;
-      const unsigned fpeek =
-          merge_unit && 1 + lane < w.parts ? ld_relaxed_gpu(fbase + 1 + lane) : 0u;
+      const bool peeks = merge_unit && 1 + lane < w.parts;
+      unsigned fpeek = peeks ? ld_relaxed_gpu(fbase + 1 + lane) : 0u;
+      const int unit_tiles = w.tb - w.ta;
       // query rows of the GQA group, one bulk copy per head into padded rows
       {
         const int qs = it_q & 1;
@@ -913,6 +919,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
             }
           }
           ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (peeks && base / boxes + tt == unit_tiles - 2) fpeek = ld_relaxed_gpu(fbase + 1 + lane);
           if (!looked_ahead) {  // next unit's table lookups, once this one is moving
             looked_ahead = true;
             have_next = next_unit(p, rows, pre, prc, it, wn, lane);
@@ -1325,23 +1332,8 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
         *abort_flag = 1;
         continue;
       }
-      const float *mbuf = reinterpret_cast<const float *>(sm + Cf::OFF_Q);
-      for (int j = 1; j < w.parts; ++j) {
-        const bool in_smem = j == 1;
-        const float *op = in_smem ? mbuf : o_part + (rec + j) * p.G * D;
-        const float *lp = in_smem ? mbuf + p.G * D : lse_part + (rec + j) * p.G;
-        auto ld = [&](const float *a) { return in_smem ? *a : __ldcg(a); };
-        const float ls0 = hv0 ? ld(lp + h0) : -INFINITY;
-        const float ls1 = hv1 ? ld(lp + h1) : -INFINITY;
-        float v[MT][4];
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt) {
-          const int d = warp * (D / 4) + 16 * mt + gid;
-          v[mt][0] = hv0 ? ld(op + h0 * D + d) : 0.f;
-          v[mt][2] = hv0 ? ld(op + h0 * D + d + 8) : 0.f;
-          v[mt][1] = hv1 ? ld(op + h1 * D + d) : 0.f;
-          v[mt][3] = hv1 ? ld(op + h1 * D + d + 8) : 0.f;
-        }
+      // fold one part (normalised o, lse) into the running (m, l, unnormalised o)
+      auto merge_in = [&](float ls0, float ls1, const float (&v)[MT][4]) {
         const float mn0 = fmaxf(m_run0, ls0), mn1 = fmaxf(m_run1, ls1);
         const float mu0 = mn0 == -INFINITY ? 0.f : mn0;
         const float mu1 = mn1 == -INFINITY ? 0.f : mn1;
@@ -1358,6 +1350,45 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
         l_run1 = fmaf(l_run1, a1, b1);
         m_run0 = mn0;
         m_run1 = mn1;
+      };
+      {   // part 1, from the Q stages
+        const float *mbuf = reinterpret_cast<const float *>(sm + Cf::OFF_Q);
+        const float *lp = mbuf + p.G * D;
+        float v[MT][4];
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+          const int d = warp * (D / 4) + 16 * mt + gid;
+          v[mt][0] = hv0 ? mbuf[h0 * D + d] : 0.f;
+          v[mt][2] = hv0 ? mbuf[h0 * D + d + 8] : 0.f;
+          v[mt][1] = hv1 ? mbuf[h1 * D + d] : 0.f;
+          v[mt][3] = hv1 ? mbuf[h1 * D + d + 8] : 0.f;
+        }
+        merge_in(hv0 ? lp[h0] : -INFINITY, hv1 ? lp[h1] : -INFINITY, v);
+      }
+      // parts 2.. (rows cut more than twice), from the workspace, JB parts per
+      // round trip to L2
+      constexpr int JB = D <= 128 ? 4 : D == 256 ? 2 : 1;
+      for (int j0 = 2; j0 < w.parts; j0 += JB) {
+        float v[JB][MT][4], ls[JB][2];
+#pragma unroll
+        for (int jj = 0; jj < JB; ++jj) {
+          const int j = j0 + jj;
+          const bool jv = j < w.parts;
+          const float *op = o_part + (rec + j) * p.G * D;
+          const float *lp = lse_part + (rec + j) * p.G;
+          ls[jj][0] = jv && hv0 ? __ldcg(lp + h0) : -INFINITY;
+          ls[jj][1] = jv && hv1 ? __ldcg(lp + h1) : -INFINITY;
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt) {
+            const int d = warp * (D / 4) + 16 * mt + gid;
+            v[jj][mt][0] = jv && hv0 ? __ldcg(op + h0 * D + d) : 0.f;
+            v[jj][mt][2] = jv && hv0 ? __ldcg(op + h0 * D + d + 8) : 0.f;
+            v[jj][mt][1] = jv && hv1 ? __ldcg(op + h1 * D + d) : 0.f;
+            v[jj][mt][3] = jv && hv1 ? __ldcg(op + h1 * D + d + 8) : 0.f;
+          }
+        }
+#pragma unroll
+        for (int jj = 0; jj < JB; ++jj) merge_in(ls[jj][0], ls[jj][1], v[jj]);
       }
     }
     const float il0 = l_run0 > 0.f ? 1.f / l_run0 : 0.f;
