@@ -636,7 +636,10 @@ def run_ours(args, world, rank, local):
     t_max = reduce_max(t_step_ms, world)
     value = reduce_sum(timed_bytes, world) / (t_max * 1e-3) / 1e9
     attn_gbs = timed_bytes / (t_attn_ms * 1e-3) / 1e9
-    launches_per_step = (3 if args.chain else 1) + (1 if ws.max_parts > 1 else 0)
+    # the combine kernel runs only with a fixed split count; the automatic mode
+    # merges cut rows inside the attention kernel
+    combine = bool(ws.splits) and ws.max_parts > 1
+    launches_per_step = (3 if args.chain else 1) + (1 if combine else 0)
 
     # ---- end to end through the public API: pinned host in, output back ----
     n_e2e = min(args.e2e_steps, K)
@@ -675,7 +678,8 @@ def run_ours(args, world, rank, local):
                        "parallelism": f"replicas x{world}"},
             "roofline": {"bound": "hbm", "achieved": attn_gbs, "peak": peak, "unit": "GB/s",
                          "frac": attn_gbs / peak, "peak_kind": peak_kind,
-                         "kernel": f"decode_attn_kernel<{D}, false> + combine_kernel<{D}>",
+                         "kernel": f"decode_attn_kernel<{D}, false>"
+                                   + (f" + combine_kernel<{D}>" if combine else ""),
                          "traffic": profile_traffic(f"{args.workload}_decode_attn_{D}",
                                                     timed_bytes / K)},
             "cpu_baseline": cpu,
