@@ -74,7 +74,9 @@ def parse_args():
     ap.add_argument("--layers", type=int, default=0,
                     help="layer caches to cycle (0: enough for 4x L2)")
     ap.add_argument("--workload", default="rollout",
-                    choices=sorted(list(WORKLOAD_CHOICES) + ["prefill", "prefill-long"]),
+                    choices=sorted(list(WORKLOAD_CHOICES) + ["prefill", "prefill-long",
+                                                             "prefill-gemma-sliding",
+                                                             "prefill-gemma-full"]),
                     help="rollout (the headline line) or one of the static decode layers")
     return ap.parse_args()
 
@@ -784,26 +786,42 @@ def prefill_docs(long: bool = False, n_docs: int = 64, seed_salt: int = 31):
     return np.repeat(np.arange(n_docs), lens).astype(np.int32), lens
 
 
-def prefill_flops(lens, Hq: int, D: int) -> float:
-    """QK^T and PV over the kept (causal, same-document) pairs: 4 D Hq per pair."""
+def prefill_flops(lens, Hq: int, D: int, window: int = 0) -> float:
+    """QK^T and PV over the kept (causal, same-document, within the window)
+    pairs: 4 D Hq per pair. A document of n tokens keeps n(n+1)/2 pairs, or
+    with a window W < n: W(W+1)/2 + (n - W) W."""
     lens = np.asarray(lens, dtype=np.float64)
-    return float(4.0 * D * Hq * np.sum(lens * (lens + 1) / 2))
+    full = lens * (lens + 1) / 2
+    if window > 0:
+        W = float(window)
+        full = np.where(lens > W, W * (W + 1) / 2 + (lens - W) * W, full)
+    return float(4.0 * D * Hq * np.sum(full))
+
+
+# prefill workloads: name -> (q heads, kv heads, head_dim, window, long documents)
+PREFILL_CHOICES = {
+    "prefill": (32, 8, 128, 0, False),
+    "prefill-long": (32, 8, 128, 0, True),
+    "prefill-gemma-sliding": (8, 1, 256, 512, False),
+    "prefill-gemma-full": (8, 1, 512, 0, False),
+}
 
 
 def run_prefill(args, world, rank, local):
     """Document-causal prefill attention (prefill_attn) on 64 packed prompts
-    with Qwen3-4B heads (32 q / 8 kv, head_dim 128); tensor-core bound. A
-    step is one layer's attention call; the block mask (prefill_block_mask)
-    depends only on the documents, is built once per batch for all layers,
-    and is timed on its own."""
+    (or 8 documents of 2048 tokens), with Qwen3-4B heads (32 q / 8 kv,
+    head_dim 128) or the Gemma-4 E2B layers (8 q / 1 kv; sliding: head_dim 256,
+    window 512; full: head_dim 512); tensor-core bound. A step is one layer's
+    attention call; the block mask (prefill_block_mask) depends only on the
+    documents and the window, is built once per batch for all layers, and is
+    timed on its own."""
     import paged_kv_decode_pagetable_gb300 as pkv
     if not torch.cuda.is_available():
         raise SystemExit("bench.py needs a CUDA GPU (the product path has no CPU fallback)")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     pkv.load_library()
-    Hq, Hkv, D = 32, 8, 128
-    long = args.workload == "prefill-long"
+    Hq, Hkv, D, window, long = PREFILL_CHOICES[args.workload]
     docs, lens = prefill_docs(long)
     L = len(docs)
     g = torch.Generator(device=dev)
@@ -817,7 +835,7 @@ def run_prefill(args, world, rank, local):
     scale = D ** -0.5
     W, K = args.warmup, min(args.steps, 200)
 
-    bm = pkv.prefill_block_mask(d_docs)
+    bm = pkv.prefill_block_mask(d_docs, window)
 
     def call(t):
         q, k, v = sets[t % 2]
@@ -848,7 +866,7 @@ def run_prefill(args, world, rank, local):
     mgraph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(mgraph):
         for _ in range(K):
-            pkv.prefill_block_mask(d_docs)
+            pkv.prefill_block_mask(d_docs, window)
     mgraph.replay()
     torch.cuda.synchronize()
     e0.record(stream)
@@ -856,7 +874,7 @@ def run_prefill(args, world, rank, local):
     e1.record(stream)
     torch.cuda.synchronize()
     mask_us = e0.elapsed_time(e1) * 1e3 / K
-    flops = prefill_flops(lens, Hq, D)
+    flops = prefill_flops(lens, Hq, D, window)
     n_blocks = int(bm.kv_num_blocks.sum().item() + bm.full_kv_num_blocks.sum().item())
     value = reduce_sum(flops * K, world) / (ms * 1e-3) / 1e12
     peaks, peak_kind = measured_peaks()
@@ -871,9 +889,9 @@ def run_prefill(args, world, rank, local):
         ks = sets[0][1][:, :end].float().cpu().numpy()
         vs = sets[0][2][:, :end].float().cpu().numpy()
         t0 = time.perf_counter()
-        oracle.prefill_attention(qs, ks, vs, docs[:end], scale)
+        oracle.prefill_attention(qs, ks, vs, docs[:end], scale, window=window)
         sec = time.perf_counter() - t0
-        cpu = {"value": prefill_flops(lens[:n], Hq, D) / sec / 1e12, "unit": "TFLOP/s",
+        cpu = {"value": prefill_flops(lens[:n], Hq, D, window) / sec / 1e12, "unit": "TFLOP/s",
                "cores": 1, "kind": "oracle",
                "sample": f"the first {n} documents ({end} tokens), float64 NumPy, {sec:.1f} s"}
     if rank == 0:
@@ -885,7 +903,8 @@ def run_prefill(args, world, rank, local):
             "config": {"workload": (f"packed prefill: 8 documents of 2048 tokens ({L} tokens), "
                                     if long else
                                     f"packed prefill: 64 prompts U[100,400] ({L} tokens), ")
-                                   + "32 q / 8 kv heads, head_dim 128",
+                                   + f"{Hq} q / {Hkv} kv heads, head_dim {D}"
+                                   + (f", window {window}" if window else ""),
                        "global_batch": len(lens) * world, "tokens": L, "flops_per_call": flops,
                        "visited_blocks_per_head": n_blocks,
                        "block_flops_per_call": 4.0 * 64 * 64 * D * Hq * n_blocks,
@@ -894,7 +913,9 @@ def run_prefill(args, world, rank, local):
                        "parallelism": f"replicas x{world}"},
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
                          "unit": "TFLOP/s", "frac": achieved / peak, "peak_kind": peak_kind,
-                         "kernel": "prefill_tc_kernel<128> (tcgen05)", "traffic": None},
+                         "kernel": (f"prefill_tc_kernel<{D}>" if D <= 128
+                                    else f"prefill_wide_kernel<{D}>") + " (tcgen05)",
+                         "traffic": None},
             "cpu_baseline": cpu, "gpu_launches": K, "clocks": clocks}), flush=True)
 
 
@@ -904,7 +925,7 @@ def main():
     try:
         if args.impl == "reference":
             run_reference(args, world, rank)
-        elif args.workload in ("prefill", "prefill-long"):
+        elif args.workload in PREFILL_CHOICES:
             run_prefill(args, world, rank, local)
         else:
             run_ours(args, world, rank, local)

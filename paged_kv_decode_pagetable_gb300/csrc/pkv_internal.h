@@ -36,6 +36,23 @@ int launch_prefill_tc(const pkv_bf16 *q, const pkv_bf16 *k, const pkv_bf16 *v,
                       const int32_t *docs, const int32_t *kv_num, const int32_t *kv_idx,
                       const int32_t *full_num, const int32_t *full_idx, int L, int Hq, int Hkv,
                       int window, float scale, pkv_bf16 *out, cudaStream_t s);
+// The same for D in {256, 512} (prefill_tc_wide.cu).
+template <int D>
+int launch_prefill_wide(const pkv_bf16 *q, const pkv_bf16 *k, const pkv_bf16 *v,
+                        const int32_t *docs, const int32_t *kv_num, const int32_t *kv_idx,
+                        const int32_t *full_num, const int32_t *full_idx, int L, int Hq, int Hkv,
+                        int window, float scale, pkv_bf16 *out, cudaStream_t s);
+}  // namespace pkv
+
+struct CUtensorMap_st;
+namespace pkv {
+// Tensor maps of the prefill kernels (prefill_tc.cu): a 3-D map {column,
+// token, head} over a [heads][L][D] bf16 tensor with [box_rows][64] boxes and
+// 128-byte swizzle (tokens past L read zeros), and a 1-D map over the int32
+// document ids in 64-id boxes (ids past L read zeros).
+int prefill_head_map(CUtensorMap_st *tm, const void *base, int heads, int L, int D,
+                     int box_rows);
+int prefill_docs_map(CUtensorMap_st *tm, const int32_t *docs, int L);
 
 inline bool aligned16(const void *p) {
   return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;

@@ -163,14 +163,15 @@ extern "C" int prefill_attn(const pkv_bf16 *q, const pkv_bf16 *k, const pkv_bf16
                             const int32_t *kv_indices, const int32_t *full_kv_num_blocks,
                             const int32_t *full_kv_indices, int L, int Hq, int Hkv, int D,
                             int window, float scale, pkv_bf16 *out, void *stream) {
-  if (D != 64 && D != 128)
-    return pkv::fail(PKV_E_BAD_ARG, "prefill_attn: D must be 64 or 128");
+  if (D != 64 && D != 128 && D != 256 && D != 512)
+    return pkv::fail(PKV_E_BAD_ARG, "prefill_attn: D must be 64, 128, 256 or 512");
   if (Hkv < 1 || Hq < Hkv || Hq % Hkv)
     return pkv::fail(PKV_E_BAD_ARG, "prefill_attn: need Hq %% Hkv == 0");
   if (L < 0 || L > 0x7fffffff - kBM || Hq > 65535 || window < 0)
     return pkv::fail(PKV_E_BAD_ARG, "prefill_attn: bad size or window");
-  // work items of 128 query rows and one head are counted in 32 bits
-  if (1LL * ((L + 2 * kBM - 1) / (2 * kBM)) * Hq > 0x7fffffffLL)
+  // work items of 128 query rows, one head and (D = 512) one output half are
+  // counted in 32 bits
+  if (1LL * ((L + 2 * kBM - 1) / (2 * kBM)) * Hq * (D == 512 ? 2 : 1) > 0x7fffffffLL)
     return pkv::fail(PKV_E_BAD_ARG, "prefill_attn: L x Hq too large");
   if (!(scale > 0.f) || !std::isfinite(scale))
     return pkv::fail(PKV_E_BAD_ARG, "prefill_attn: scale must be finite and > 0");
@@ -182,13 +183,14 @@ extern "C" int prefill_attn(const pkv_bf16 *q, const pkv_bf16 *k, const pkv_bf16
       !pkv::aligned16(docs))
     return pkv::fail(PKV_E_BAD_ARG, "prefill_attn: tensors and docs must be 16-byte aligned");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const int st =
-      D == 64 ? pkv::launch_prefill_tc<64>(q, k, v, docs, kv_num_blocks, kv_indices,
-                                           full_kv_num_blocks, full_kv_indices, L, Hq, Hkv,
-                                           window, scale, out, s)
-              : pkv::launch_prefill_tc<128>(q, k, v, docs, kv_num_blocks, kv_indices,
-                                            full_kv_num_blocks, full_kv_indices, L, Hq, Hkv,
-                                            window, scale, out, s);
+#define PKV_PREFILL(FN, DD)                                                                  \
+  pkv::FN<DD>(q, k, v, docs, kv_num_blocks, kv_indices, full_kv_num_blocks, full_kv_indices, L, \
+              Hq, Hkv, window, scale, out, s)
+  const int st = D == 64    ? PKV_PREFILL(launch_prefill_tc, 64)
+                 : D == 128 ? PKV_PREFILL(launch_prefill_tc, 128)
+                 : D == 256 ? PKV_PREFILL(launch_prefill_wide, 256)
+                            : PKV_PREFILL(launch_prefill_wide, 512);
+#undef PKV_PREFILL
   if (st != PKV_OK) return st;
   return pkv::ok();
 }

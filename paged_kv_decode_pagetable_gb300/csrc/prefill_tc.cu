@@ -39,10 +39,11 @@
 #include <mutex>
 
 #include "pkv_internal.h"
+#include "tcgen05.cuh"
 
 namespace {
 
-constexpr int kQR = 128;      // query rows per work item
+constexpr int kQR = kTcM;     // query rows per work item
 constexpr int kKB = 64;       // keys per tile (the block mask's block)
 constexpr int kNS = 3;        // K/V ring stages
 constexpr int kSplit = 4;                  // softmax warps per TMEM lane group
@@ -50,7 +51,6 @@ constexpr int kSoftWarps = 4 * kSplit;     // each: 32 rows x 16 keys of a tile
 constexpr int kKW = 64 / kSplit;           // keys per softmax warp
 constexpr int kProdWarp = kSoftWarps, kMmaWarp = kSoftWarps + 1;
 constexpr int kTCThreads = (kSoftWarps + 2) * 32;
-constexpr int kSpin = 1 << 22;
 constexpr float kLazyLog2 = 8.f;   // rescale O only when a row maximum grows past 2^8
 
 // tile descriptor flags; kNeed0 / kNeed1: the block is listed for the
@@ -87,138 +87,6 @@ struct TC {
   static_assert(OFF_SD % 128 == 0, "TMA destination alignment");
   static_assert(SMEM <= 232448 / CTAS_PER_SM, "shared memory per SM");
 };
-
-// ---- PTX wrappers ----------------------------------------------------------
-__device__ __forceinline__ uint32_t t_smem(const void *p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ void t_bar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
-}
-__device__ __forceinline__ void t_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ void t_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-               : "memory");
-}
-// waits for completion number k (0, 1, ...) of the barrier's phases; false
-// if it gave up (the abort flag is then raised for everyone)
-__device__ __forceinline__ bool t_wait(uint32_t bar, int k, volatile int *abort_flag) {
-  const uint32_t parity = static_cast<uint32_t>(k) & 1u;
-  for (int i = 0; i < kSpin; ++i) {
-    uint32_t done;
-    asm volatile(
-        "{\n.reg .pred q;\nmbarrier.try_wait.parity.shared::cta.b64 q, [%1], %2;\n"
-        "selp.u32 %0, 1, 0, q;\n}\n"
-        : "=r"(done)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    if (done) return true;
-    if ((i & 63) == 63 && *abort_flag) return false;
-  }
-  *abort_flag = 1;
-  return false;
-}
-// the same, by every lane of a warp, with one result for the warp (so the
-// warp-collective TMEM accesses that follow are never reached by part of it)
-__device__ __forceinline__ bool t_wait_warp(uint32_t bar, int k, volatile int *abort_flag) {
-  return __all_sync(0xffffffffu, t_wait(bar, k, abort_flag));
-}
-// bounded wait that ignores the abort flag (used to drain the tensor core
-// before the TMEM is released)
-__device__ __forceinline__ void t_wait_drain(uint32_t bar) {
-  for (int i = 0; i < kSpin; ++i) {
-    uint32_t done;
-    asm volatile(
-        "{\n.reg .pred q;\nmbarrier.try_wait.parity.shared::cta.b64 q, [%1], 0;\n"
-        "selp.u32 %0, 1, 0, q;\n}\n"
-        : "=r"(done)
-        : "r"(bar)
-        : "memory");
-    if (done) return;
-  }
-}
-__device__ __forceinline__ void t_tma_1d(uint32_t dst, const CUtensorMap *tm, int x, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.1d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2}], [%3];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(bar)
-      : "memory");
-}
-__device__ __forceinline__ void t_tma_3d(uint32_t dst, const CUtensorMap *tm, int x, int y, int z,
-                                         uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(z), "r"(bar)
-      : "memory");
-}
-// shared-memory matrix descriptor: SW128 atoms, version 1
-__device__ __forceinline__ uint64_t t_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-  return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu) |
-         (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
-         (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (static_cast<uint64_t>(1) << 46) |
-         (static_cast<uint64_t>(2) << 61);
-}
-// instruction descriptor, kind::f16: f32 accumulator, bf16 A and B, A
-// K-major, B K-major (b_mn = 0) or MN-major (b_mn = 1), M = 128
-__host__ __device__ constexpr uint32_t t_idesc(int N, int b_mn) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(b_mn) << 16) |
-         (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(kQR >> 4) << 24);
-}
-__device__ __forceinline__ void t_mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
-                                      uint32_t accumulate) {
-  asm volatile(
-      "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
-      "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
-}
-__device__ __forceinline__ void t_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                   bar)
-               : "memory");
-}
-__device__ __forceinline__ void t_fence_before() {
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void t_fence_after() {
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void t_ld16(uint32_t taddr, uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
-}
-__device__ __forceinline__ void t_st16(uint32_t taddr, const uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
-      "r"(r[15]));
-}
-__device__ __forceinline__ void t_wait_ld() {
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void t_wait_st() {
-  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
-// 2^x on the MUFU unit (the PTX approximate instruction, subnormal results
-// flushed to zero: they are below what the bf16 P can hold anyway)
-__device__ __forceinline__ float t_ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-__device__ __forceinline__ uint32_t t_pack(float lo, float hi) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t *>(&v);
-}
 
 struct Item {
   int row0, h;
@@ -718,8 +586,11 @@ EncodeTiledFn tc_encode_fn() {
   return fn;
 }
 
+}  // namespace
+
+namespace pkv {
 // 1-D map over the int32 document ids, 64-id boxes; ids past L read zeros
-int docs_map(CUtensorMap *tm, const int32_t *docs, int L) {
+int prefill_docs_map(CUtensorMap *tm, const int32_t *docs, int L) {
   EncodeTiledFn fn = tc_encode_fn();
   if (!fn) return pkv::fail(PKV_E_CUDA, "cuTensorMapEncodeTiled unavailable");
   cuuint64_t dims[1] = {static_cast<cuuint64_t>(L)};
@@ -736,7 +607,7 @@ int docs_map(CUtensorMap *tm, const int32_t *docs, int L) {
 
 // 3-D map {column, token, head} over a [heads][L][D] bf16 tensor with
 // [box_rows][64] boxes, 128-byte swizzle; tokens past L read zeros
-int head_map(CUtensorMap *tm, const void *base, int heads, int L, int D, int box_rows) {
+int prefill_head_map(CUtensorMap *tm, const void *base, int heads, int L, int D, int box_rows) {
   EncodeTiledFn fn = tc_encode_fn();
   if (!fn) return pkv::fail(PKV_E_CUDA, "cuTensorMapEncodeTiled unavailable");
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(L),
@@ -752,7 +623,7 @@ int head_map(CUtensorMap *tm, const void *base, int heads, int L, int D, int box
   return PKV_OK;
 }
 
-}  // namespace
+}  // namespace pkv
 
 // Launch of the tcgen05 prefill kernel (declared in pkv_internal.h); the
 // public entry point prefill_attn validates the arguments first.
@@ -777,10 +648,10 @@ int launch_prefill_tc(const pkv_bf16 *q, const pkv_bf16 *k, const pkv_bf16 *v,
     }
   }
   CUtensorMap tmQ, tmK, tmV, tmD;
-  int st = head_map(&tmQ, q, Hq, L, D, kQR);
-  if (st == PKV_OK) st = head_map(&tmK, k, Hkv, L, D, kKB);
-  if (st == PKV_OK) st = head_map(&tmV, v, Hkv, L, D, kKB);
-  if (st == PKV_OK) st = docs_map(&tmD, docs, L);
+  int st = prefill_head_map(&tmQ, q, Hq, L, D, kQR);
+  if (st == PKV_OK) st = prefill_head_map(&tmK, k, Hkv, L, D, kKB);
+  if (st == PKV_OK) st = prefill_head_map(&tmV, v, Hkv, L, D, kKB);
+  if (st == PKV_OK) st = prefill_docs_map(&tmD, docs, L);
   if (st != PKV_OK) return st;
   const int n = (L + kKB - 1) / kKB;
   const long long items = 1LL * ((n + 1) / 2) * Hq;

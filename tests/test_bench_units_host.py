@@ -68,3 +68,14 @@ def test_rollout_lengths_equal_the_allocator_driven_schedule():
     _, _, _, lens_pt = bench.rollout_metadata(w, w.steps)
     assert lens.shape == (512, 64) and np.array_equal(lens, lens_pt)
     assert lens.min() >= 101 and lens.max() <= 1024
+
+
+def test_prefill_flops_with_a_window_equal_kept_pairs_of_the_mask():
+    """The sliding-window count (W(W+1)/2 + (n - W) W kept pairs for a document
+    of n > W tokens) equals the oracle mask's kept pairs, for documents both
+    shorter and longer than the window."""
+    lens = np.array([5, 30, 31, 90, 7])
+    docs = np.repeat(np.arange(len(lens)), lens).astype(np.int32)
+    for window in (1, 8, 31, 64):
+        kept = int(oracle.keep_matrix(docs, window).sum())
+        assert bench.prefill_flops(lens, 8, 256, window) == 4.0 * 256 * 8 * kept, window

@@ -7,6 +7,9 @@ more than 128 key blocks (the builder's second pass).
 
 The block mask is integer work: equal to the oracle's, entry for entry.
 
+Head dims 64 and 128 run on prefill_tc.cu's kernel, 256 and 512 (the Gemma-4
+widths) on prefill_tc_wide.cu's.
+
 Attention bar: the decode path's, max abs 1e-2 and mean abs 1e-3, on every
 query row that keeps at least 16 keys, and the mean over all rows. Rows with
 fewer kept keys (a document's first tokens) may miss 1e-2 without any fault:
@@ -106,7 +109,12 @@ def _kept(docs, window=0):
     (64, 8, 1, 128, "one", 0), (1, 2, 1, 64, "one", 0), (65, 4, 2, 128, "interleaved", 0),
     (777, 16, 4, 128, "contiguous", 0), (200, 6, 3, 64, "contiguous", 0),
     (300, 4, 1, 128, "one", 100), (500, 4, 2, 64, "contiguous", 64),
-    (257, 4, 2, 128, "interleaved", 7), (640, 8, 2, 128, "many", 0)])
+    (257, 4, 2, 128, "interleaved", 7), (640, 8, 2, 128, "many", 0),
+    # the Gemma-4 widths: sliding layers D=256 (window 512), full layers D=512
+    (300, 8, 1, 256, "contiguous", 0), (257, 4, 2, 256, "interleaved", 0),
+    (200, 8, 1, 256, "one", 64), (700, 8, 1, 256, "many", 512), (1, 2, 1, 256, "one", 0),
+    (300, 8, 1, 512, "contiguous", 0), (65, 4, 1, 512, "interleaved", 0),
+    (1, 2, 1, 512, "one", 0), (500, 8, 1, 512, "many", 0), (257, 2, 2, 512, "interleaved", 37)])
 def test_prefill_attention_parity(dev, L, Hq, Hkv, D, kind, window):
     rng = np.random.default_rng(L * 10 + D + Hq + window)
     q = wl.randn_bf16(rng, (Hq, L, D))
@@ -179,7 +187,7 @@ def test_prefill_bad_arguments(dev):
     docs = torch.zeros(8, dtype=torch.int32, device=dev)
     bm = pkv.prefill_block_mask(docs)
     q = torch.zeros((2, 8, 96), dtype=torch.bfloat16, device=dev)
-    with pytest.raises(pkv.BadArgError):       # D = 96 unsupported
+    with pytest.raises(pkv.BadArgError):       # D = 96 unsupported (64, 128, 256, 512 are)
         pkv.prefill_attn(q, q, q, bm, 0.1, q.clone())
     q = torch.zeros((3, 8, 64), dtype=torch.bfloat16, device=dev)
     k = torch.zeros((2, 8, 64), dtype=torch.bfloat16, device=dev)
@@ -192,7 +200,7 @@ def test_prefill_bad_arguments(dev):
         pkv.prefill_attn(q, q, q, bm, 0.1, q.clone())
 
 
-@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("D", [64, 128, 256, 512])
 def test_prefill_rising_scores_rescale_every_tile(dev, D):
     """Scores that climb by about 16 (log2 units) per 64-key tile: every row's
     maximum outgrows the kept one on each new tile, so the kernel rescales
@@ -249,3 +257,28 @@ def test_prefill_long_documents_sampled_rows(dev):
     assert np.isfinite(got).all()
     assert e[:, long_rows].max() <= 1e-2, float(e[:, long_rows].max())
     assert e.mean() <= 1e-3, float(e.mean())
+
+
+@pytest.mark.parametrize("D,window", [(256, 512), (512, 0)])
+def test_prefill_gemma_layers_sampled_documents(dev, D, window):
+    """The Gemma-4 E2B prefill launches: 64 packed prompts of U[100, 400]
+    tokens, 8 q heads / 1 kv head, the sliding layer (D=256, window 512) and
+    the full layer (D=512). Whole documents are checked against the oracle run
+    on that document alone: the first, one in the middle and the last."""
+    rng = np.random.default_rng(79 + D)
+    lens = wl.uniform_lengths(rng, 64, 100, 400)
+    docs = np.repeat(np.arange(64), lens).astype(np.int32)
+    L, Hq, Hkv = len(docs), 8, 1
+    q = wl.randn_bf16(rng, (Hq, L, D))
+    k = wl.randn_bf16(rng, (Hkv, L, D))
+    v = wl.randn_bf16(rng, (Hkv, L, D))
+    scale = D ** -0.5
+    out, bm = _run(dev, q, k, v, docs, window, scale)
+    _check_mask(bm, docs, window)
+    got = f64(out)
+    starts = np.r_[0, np.cumsum(lens)]
+    for d in (0, 31, 63):
+        sl = slice(int(starts[d]), int(starts[d + 1]))
+        ref = oracle.prefill_attention(q[:, sl].double().numpy(), k[:, sl].double().numpy(),
+                                       v[:, sl].double().numpy(), docs[sl], scale, window=window)
+        _compare(got[:, sl], ref, v, _kept(docs[sl], window))
