@@ -359,12 +359,15 @@ int prefill_block_mask(const int32_t *docs, int L, int window,
  * block listed as full that is not makes its pairs count as kept; list
  * entries outside [0, n) are skipped, so no list can make a read go out of
  * bounds; the lists are expected ascending, as prefill_block_mask writes
- * them). A row with no visited key gets zeros. Requires D in {64, 128},
- * Hq % Hkv == 0, Hq <= 65535, ceil(L / 128) * Hq < 2^31, 16-byte aligned q,
- * k, v, out and docs, scale finite and > 0. One kernel (tcgen05 MMAs with TMEM accumulators, one
- * persistent CTA per SM over work items of 128 query rows and one head); no
- * workspace. Errors: PKV_E_BAD_ARG for the above or a NULL pointer,
- * PKV_E_CUDA on a launch failure. */
+ * them). A row with no visited key gets zeros. Requires D in {64, 128,
+ * 256, 512} (256 and 512: the Gemma-4 sliding and full layers), Hq % Hkv ==
+ * 0, Hq <= 65535, ceil(L / 128) * Hq (twice that at D = 512) < 2^31,
+ * 16-byte aligned q, k, v, out and docs, scale finite and > 0. One kernel
+ * (tcgen05 MMAs with TMEM accumulators, one persistent CTA per SM over work
+ * items of 128 query rows and one head; at D = 256 and 512 the scores are
+ * accumulated over D in 64-column chunks and an item writes one 256-column
+ * half of the output); no workspace. Errors: PKV_E_BAD_ARG for the above or
+ * a NULL pointer, PKV_E_CUDA on a launch failure. */
 int prefill_attn(const pkv_bf16 *q, const pkv_bf16 *k, const pkv_bf16 *v,
                  const int32_t *docs, const int32_t *kv_num_blocks,
                  const int32_t *kv_indices, const int32_t *full_kv_num_blocks,
