@@ -15,7 +15,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libpkv.so")
 SOURCES = ["common.cu", "pagetable.cpp", "kv_append.cu", "qk_norm_rope.cu",
            "decode_attn.cu", "decode_attn_noalloc.cu", "prefill_attn.cu", "prefill_tc.cu",
-           "prefill_tc_wide.cu"]
+           "prefill_tc_wide.cu", "block_mask_convert.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
          "-I", os.path.join(ROOT, "include")]
