@@ -46,6 +46,7 @@ namespace {
 constexpr int kQR = kTcM;     // query rows per work item
 constexpr int kKB = 64;       // keys per tile (the block mask's block)
 constexpr int kNS = 3;        // K/V ring stages
+constexpr int kNQ = 2;        // Q tile buffers: the next item's Q loads while this one runs
 constexpr int kSplit = 4;                  // softmax warps per TMEM lane group
 constexpr int kSoftWarps = 4 * kSplit;     // each: 32 rows x 16 keys of a tile
 constexpr int kKW = 64 / kSplit;           // keys per softmax warp
@@ -67,17 +68,17 @@ struct TC {
   static constexpr int KV_BYTES = ATOMS * KV_ATOM;
   static constexpr int P_BYTES = kQR * kKB * 2;
   static constexpr int OFF_Q = 0;
-  static constexpr int OFF_K = OFF_Q + Q_BYTES;
+  static constexpr int OFF_K = OFF_Q + kNQ * Q_BYTES;
   static constexpr int OFF_V = OFF_K + kNS * KV_BYTES;
   static constexpr int OFF_P = OFF_V + kNS * KV_BYTES;
   static constexpr int OFF_SD = OFF_P + 2 * P_BYTES;          // int [kNS][64] key documents
   static constexpr int OFF_XCH = OFF_SD + kNS * kKB * 4;       // float [2][kSplit][128 rows]
   static constexpr int OFF_META = OFF_XCH + 2 * kSplit * kQR * 4;  // int4 [kNS]
   static constexpr int OFF_BAR = OFF_META + kNS * 16;
-  // qfull, qempty, kvfull[NS], kvempty[NS], sfull[2], sfree[2], pfull[2], pvdone[2],
-  // ofree[2] (per O buffer, so that no waiter can fall two phases behind),
-  // drain, xbar[4] (the softmax groups' exchanges)
-  static constexpr int N_BAR = 2 + 2 * kNS + 2 + 2 + 2 + 2 + 2 + 1 + 4;
+  // qfull[NQ], qempty[NQ], kvfull[NS], kvempty[NS], sfull[2], sfree[2], pfull[2],
+  // pvdone[2], ofree[2] (per O buffer, so that no waiter can fall two phases
+  // behind), drain, xbar[4] (the softmax groups' exchanges)
+  static constexpr int N_BAR = 2 * kNQ + 2 * kNS + 2 + 2 + 2 + 2 + 2 + 1 + 4;
   static constexpr int OFF_MISC = OFF_BAR + N_BAR * 8;       // tmem address, abort flag
   static constexpr int SMEM = OFF_MISC + 16 + 1024;          // + slack to align to 1024
   static constexpr int TMEM_COLS = 512;   // S[2] (2 x 64) + O[2] (2 x 128): items alternate O
@@ -122,7 +123,7 @@ __global__ void __launch_bounds__(kTCThreads, TC<D>::CTAS_PER_SM)
                  sD = t_smem(sm + C::OFF_SD);
   int4 *meta = reinterpret_cast<int4 *>(sm + C::OFF_META);
   const uint32_t bar0 = t_smem(sm + C::OFF_BAR);
-  const uint32_t qfull = bar0, qempty = bar0 + 8, kvfull = bar0 + 16,
+  const uint32_t qfull = bar0, qempty = bar0 + 8 * kNQ, kvfull = bar0 + 16 * kNQ,
                  kvempty = kvfull + 8 * kNS, sfull = kvempty + 8 * kNS, sfree = sfull + 16,
                  pfull = sfree + 16, pvdone = pfull + 16, ofree = pvdone + 16, drain = ofree + 16,
                  xbar = drain + 8;
@@ -130,8 +131,10 @@ __global__ void __launch_bounds__(kTCThreads, TC<D>::CTAS_PER_SM)
   volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + C::OFF_MISC + 4);
 
   if (tid == 0) {
-    t_bar_init(qfull, 1);
-    t_bar_init(qempty, 1);
+    for (int i = 0; i < kNQ; ++i) {
+      t_bar_init(qfull + 8 * i, 1);
+      t_bar_init(qempty + 8 * i, 1);
+    }
     for (int i = 0; i < kNS; ++i) {
       t_bar_init(kvfull + 8 * i, 1);
       t_bar_init(kvempty + 8 * i, 1);
@@ -173,10 +176,13 @@ __global__ void __launch_bounds__(kTCThreads, TC<D>::CTAS_PER_SM)
       for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++it) {
         const Item w = item_of(item, n2, Hq);
         const int hk = w.h / G;
-        if (it > 0 && !t_wait(qempty, it - 1, abort_flag)) break;
-        t_expect_tx(qfull, C::Q_BYTES);
+        const int qs = it % kNQ;
+        if (it >= kNQ && !t_wait(qempty + 8 * qs, it / kNQ - 1, abort_flag)) break;
+        t_expect_tx(qfull + 8 * qs, C::Q_BYTES);
 #pragma unroll
-        for (int a = 0; a < C::ATOMS; ++a) t_tma_3d(sQ + a * C::Q_ATOM, &tmQ, 64 * a, w.row0, w.h, qfull);
+        for (int a = 0; a < C::ATOMS; ++a)
+          t_tma_3d(sQ + qs * C::Q_BYTES + a * C::Q_ATOM, &tmQ, 64 * a, w.row0, w.h,
+                   qfull + 8 * qs);
         // the union of the two query blocks' lists, ascending
         const int qb0 = w.row0 / kKB, qb1 = qb0 + 1;
         const bool has1 = qb1 < nblk;
@@ -268,7 +274,9 @@ __global__ void __launch_bounds__(kTCThreads, TC<D>::CTAS_PER_SM)
         return true;
       };
       for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++it) {
-        if (!t_wait(qfull, it, abort_flag)) break;
+        const int qs = it % kNQ;
+        if (!t_wait(qfull + 8 * qs, it / kNQ, abort_flag)) break;
+        const uint32_t sQi = sQ + qs * C::Q_BYTES;
         int flags = 0;
         do {
           const int s = g % kNS, b = g & 1;
@@ -284,13 +292,13 @@ __global__ void __launch_bounds__(kTCThreads, TC<D>::CTAS_PER_SM)
           t_fence_after();
 #pragma unroll
           for (int k = 0; k < D / 16; ++k) {
-            const uint64_t a = t_desc(sQ + (k >> 2) * C::Q_ATOM + (k & 3) * 32, 16, 1024);
+            const uint64_t a = t_desc(sQi + (k >> 2) * C::Q_ATOM + (k & 3) * 32, 16, 1024);
             const uint64_t bd =
                 t_desc(sK + s * C::KV_BYTES + (k >> 2) * C::KV_ATOM + (k & 3) * 32, 16, 1024);
             t_mma(tmem + C::S_COL + b * kKB, a, bd, idS, k > 0 ? 1u : 0u);
           }
           t_commit(sfull + 8 * b);
-          if (flags & kLast) t_commit(qempty);
+          if (flags & kLast) t_commit(qempty + 8 * qs);
           // P V one tile behind S (across items too: the next item's first S
           // goes in before the previous item's last P V)
           if (pv_pending && !do_pv(g - 1, prev_flags)) {
