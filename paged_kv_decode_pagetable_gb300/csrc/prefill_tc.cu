@@ -89,16 +89,27 @@ struct TC {
   static_assert(SMEM <= 232448 / CTAS_PER_SM, "shared memory per SM");
 };
 
+// A work item fills the 128 rows of the MMA in one of two ways.
+//   paired (Hq / Hkv even): one 64-row query block for two query heads h and
+//     h + 1 of one kv group, which share the key blocks and the K / V tiles
+//     (tile rows 0-63: head h, rows 64-127: head h + 1);
+//   unpaired: two consecutive 64-row query blocks of one head (tile row r is
+//     query row0 + r); the key blocks visited are the union of the two
+//     blocks' lists, some of them needed by one half only.
+// Pairing visits each query block's own list once per head pair; on short
+// documents the union of two blocks' lists is nearly twice as long.
 struct Item {
   int row0, h;
 };
-// work item i of n_items, the last query tiles first; items of one query
-// tile are consecutive over the heads
-__device__ __forceinline__ Item item_of(int i, int n2, int Hq) {
+// work item i: the last query blocks first; items of one query block (pair)
+// are consecutive over the heads
+__device__ __forceinline__ Item item_of(int i, int nq, int Hq, bool pair) {
   Item it;
-  const int ct = n2 - 1 - i / Hq;
-  it.row0 = ct * kQR;
-  it.h = i - (i / Hq) * Hq;
+  const int per = pair ? Hq / 2 : Hq;
+  const int ct = nq - 1 - i / per;
+  const int r = i - (i / per) * per;
+  it.row0 = ct * (pair ? kKB : kQR);
+  it.h = pair ? 2 * r : r;
   return it;
 }
 
@@ -111,7 +122,8 @@ __global__ void __launch_bounds__(kTCThreads, TC<D>::CTAS_PER_SM)
                       const int32_t *__restrict__ kv_num, const int32_t *__restrict__ kv_idx,
                       const int32_t *__restrict__ full_num,
                       const int32_t *__restrict__ full_idx, int nblk, int L, int Hq, int G,
-                      int window, float scale_log2, __nv_bfloat16 *__restrict__ out) {
+                      int window, float scale_log2, int pair_heads,
+                      __nv_bfloat16 *__restrict__ out) {
   using C = TC<D>;
   extern __shared__ uint8_t tc_raw[];
   // 1024-byte aligned base, by offsetting the shared array itself (an integer
@@ -165,8 +177,9 @@ __global__ void __launch_bounds__(kTCThreads, TC<D>::CTAS_PER_SM)
   pkv_wait_prior_grid();
   pkv_allow_next_grid();
 
-  const int n2 = (nblk + 1) / 2;
-  const int n_items = n2 * Hq;
+  const bool pair = pair_heads != 0;
+  const int nq = pair ? nblk : (nblk + 1) / 2;   // row tiles of the items
+  const int n_items = nq * (pair ? Hq / 2 : Hq);
 
   if (warp == kProdWarp) {
     // ============================ producer ============================
@@ -174,17 +187,21 @@ __global__ void __launch_bounds__(kTCThreads, TC<D>::CTAS_PER_SM)
       int g = 0, it = 0;
       bool ok = true;
       for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++it) {
-        const Item w = item_of(item, n2, Hq);
-        const int hk = w.h / G;
+        const Item w = item_of(item, nq, Hq, pair);
+        const int hk = w.h / G;   // = (h + 1) / G when paired (G even, h even)
         const int qs = it % kNQ;
         if (it >= kNQ && !t_wait(qempty + 8 * qs, it / kNQ - 1, abort_flag)) break;
         t_expect_tx(qfull + 8 * qs, C::Q_BYTES);
+        // the tile's two 64-row halves (rows past L read zeros)
 #pragma unroll
-        for (int a = 0; a < C::ATOMS; ++a)
-          t_tma_3d(sQ + qs * C::Q_BYTES + a * C::Q_ATOM, &tmQ, 64 * a, w.row0, w.h,
-                   qfull + 8 * qs);
-        // the union of the two query blocks' lists, ascending
-        const int qb0 = w.row0 / kKB, qb1 = qb0 + 1;
+        for (int a = 0; a < C::ATOMS; ++a) {
+          const uint32_t dst = sQ + qs * C::Q_BYTES + a * C::Q_ATOM;
+          t_tma_3d(dst, &tmQ, 64 * a, w.row0, w.h, qfull + 8 * qs);
+          t_tma_3d(dst + kKB * 128, &tmQ, 64 * a, pair ? w.row0 : w.row0 + kKB,
+                   pair ? w.h + 1 : w.h, qfull + 8 * qs);
+        }
+        // the union of the two halves' lists, ascending (paired: one list)
+        const int qb0 = w.row0 / kKB, qb1 = pair ? qb0 : qb0 + 1;
         const bool has1 = qb1 < nblk;
         const int32_t *lf0 = full_idx + static_cast<size_t>(qb0) * nblk;
         const int32_t *lp0 = kv_idx + static_cast<size_t>(qb0) * nblk;
@@ -379,9 +396,10 @@ __global__ void __launch_bounds__(kTCThreads, TC<D>::CTAS_PER_SM)
     bool ok = true;
     for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
       ++it;
-      const Item w = item_of(item, n2, Hq);
+      const Item w = item_of(item, nq, Hq, pair);
       const uint32_t ocol_it = C::O_COL + C::O_STRIDE * (it & 1) + OH * hf;
-      const int qi = w.row0 + row;
+      const int qi = pair ? w.row0 + (row & (kKB - 1)) : w.row0 + row;
+      const int hrow = pair ? w.h + (row >> 6) : w.h;   // this row's query head
       const bool valid = qi < L;
       const int dq = valid ? docs[qi] : 0;
       float m = -INFINITY, l = 0.f;   // l: this half's share of the row sum
@@ -549,7 +567,7 @@ __global__ void __launch_bounds__(kTCThreads, TC<D>::CTAS_PER_SM)
           ep_g = g;
           ep_it = it;
           ep_qi = qi;
-          ep_h = w.h;
+          ep_h = hrow;
           ep_il = lt > 0.f ? 1.f / lt : 0.f;
         }
         ++g;
@@ -558,10 +576,11 @@ __global__ void __launch_bounds__(kTCThreads, TC<D>::CTAS_PER_SM)
     if (ok && ep && !epilogue()) ok = false;
     if (!ok || *abort_flag) {   // a wait gave up: mark this CTA's rows as failed
       for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
-        const Item w = item_of(item, n2, Hq);
-        const int qi = w.row0 + row;
+        const Item w = item_of(item, nq, Hq, pair);
+        const int qi = pair ? w.row0 + (row & (kKB - 1)) : w.row0 + row;
         if (qi >= L) continue;
-        __nv_bfloat16 *orow = out + (static_cast<size_t>(w.h) * L + qi) * D + OH * hf;
+        const int hrow = pair ? w.h + (row >> 6) : w.h;
+        __nv_bfloat16 *orow = out + (static_cast<size_t>(hrow) * L + qi) * D + OH * hf;
         for (int c = 0; c < OH; ++c) orow[c] = __float2bfloat16_rn(NAN);
       }
     }
@@ -656,18 +675,20 @@ int launch_prefill_tc(const pkv_bf16 *q, const pkv_bf16 *k, const pkv_bf16 *v,
     }
   }
   CUtensorMap tmQ, tmK, tmV, tmD;
-  int st = prefill_head_map(&tmQ, q, Hq, L, D, kQR);
+  int st = prefill_head_map(&tmQ, q, Hq, L, D, kKB);   // two 64-row boxes per item
   if (st == PKV_OK) st = prefill_head_map(&tmK, k, Hkv, L, D, kKB);
   if (st == PKV_OK) st = prefill_head_map(&tmV, v, Hkv, L, D, kKB);
   if (st == PKV_OK) st = prefill_docs_map(&tmD, docs, L);
   if (st != PKV_OK) return st;
   const int n = (L + kKB - 1) / kKB;
-  const long long items = 1LL * ((n + 1) / 2) * Hq;
+  const int G = Hq / Hkv;
+  const bool pair = G % 2 == 0;
+  const long long items = pair ? 1LL * n * (Hq / 2) : 1LL * ((n + 1) / 2) * Hq;
   const long long cap = 1LL * TC<D>::CTAS_PER_SM * pkv::sm_count();
   const int grid = static_cast<int>(items < cap ? items : cap);
   PKV_CUDA_CHECK(pkv::launch_pdl(prefill_tc_kernel<D>, dim3(grid), dim3(kTCThreads), TC<D>::SMEM,
                                  s, tmQ, tmK, tmV, tmD, docs, kv_num, kv_idx, full_num, full_idx, n, L,
-                                 Hq, Hq / Hkv, window, scale * 1.4426950408889634f,
+                                 Hq, G, window, scale * 1.4426950408889634f, pair ? 1 : 0,
                                  reinterpret_cast<__nv_bfloat16 *>(out)));
   return PKV_OK;
 }

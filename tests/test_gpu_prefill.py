@@ -8,7 +8,9 @@ more than 128 key blocks (the builder's second pass).
 The block mask is integer work: equal to the oracle's, entry for entry.
 
 Head dims 64 and 128 run on prefill_tc.cu's kernel, 256 and 512 (the Gemma-4
-widths) on prefill_tc_wide.cu's.
+widths) on prefill_tc_wide.cu's. With an even number of query heads per kv
+head a work item holds one query block of two heads; otherwise two query
+blocks of one head: both are covered.
 
 Attention bar: the decode path's, max abs 1e-2 and mean abs 1e-3, on every
 query row that keeps at least 16 keys, and the mean over all rows. Rows with
@@ -110,6 +112,8 @@ def _kept(docs, window=0):
     (777, 16, 4, 128, "contiguous", 0), (200, 6, 3, 64, "contiguous", 0),
     (300, 4, 1, 128, "one", 100), (500, 4, 2, 64, "contiguous", 64),
     (257, 4, 2, 128, "interleaved", 7), (640, 8, 2, 128, "many", 0),
+    # odd query heads per kv head: items of two query blocks of one head
+    (300, 6, 2, 128, "contiguous", 0), (333, 3, 1, 64, "many", 0), (400, 3, 3, 128, "many", 90),
     # the Gemma-4 widths: sliding layers D=256 (window 512), full layers D=512
     (300, 8, 1, 256, "contiguous", 0), (257, 4, 2, 256, "interleaved", 0),
     (200, 8, 1, 256, "one", 64), (700, 8, 1, 256, "many", 512), (1, 2, 1, 256, "one", 0),
