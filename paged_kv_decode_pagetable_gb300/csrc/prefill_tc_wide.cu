@@ -79,19 +79,24 @@ struct TW {
   static_assert(SMEM <= 232448, "shared memory per CTA");
 };
 
+// The 128 rows of an item: paired (Hq / Hkv even) one 64-row query block of
+// query heads h and h + 1 (rows 0-63 / 64-127), which share the key blocks
+// and the K / V tiles; unpaired two consecutive 64-row query blocks of head h
+// (the union of their key lists is visited).
 struct WItem {
   int row0, h, oc;
 };
-// work item i: the last query tiles first; the items of one query tile are
-// consecutive over (head, output half)
-__device__ __forceinline__ WItem witem_of(int i, int n2, int Hq, int noc) {
+// work item i: the last query blocks first; the items of one query block
+// (pair) are consecutive over (head, output half)
+__device__ __forceinline__ WItem witem_of(int i, int nq, int Hq, int noc, bool pair) {
   WItem it;
-  const int per = Hq * noc;
-  const int ct = n2 - 1 - i / per;
+  const int per = (pair ? Hq / 2 : Hq) * noc;
+  const int ct = nq - 1 - i / per;
   const int r = i - (i / per) * per;
-  it.row0 = ct * wQR;
-  it.h = r / noc;
-  it.oc = r - it.h * noc;
+  it.row0 = ct * (pair ? wKB : wQR);
+  const int hi = r / noc;
+  it.h = pair ? 2 * hi : hi;
+  it.oc = r - hi * noc;
   return it;
 }
 
@@ -104,7 +109,8 @@ __global__ void __launch_bounds__(wThreads, 1)
                         const int32_t *__restrict__ kv_num, const int32_t *__restrict__ kv_idx,
                         const int32_t *__restrict__ full_num,
                         const int32_t *__restrict__ full_idx, int nblk, int L, int Hq, int G,
-                        int window, float scale_log2, __nv_bfloat16 *__restrict__ out) {
+                        int window, float scale_log2, int pair_heads,
+                        __nv_bfloat16 *__restrict__ out) {
   using C = TW<D>;
   extern __shared__ uint8_t tw_raw[];
   uint8_t *sm = tw_raw + ((1024u - (t_smem(tw_raw) & 1023u)) & 1023u);
@@ -155,8 +161,9 @@ __global__ void __launch_bounds__(wThreads, 1)
   pkv_wait_prior_grid();
   pkv_allow_next_grid();
 
-  const int n2 = (nblk + 1) / 2;
-  const int n_items = n2 * Hq * C::NOC;
+  const bool pair = pair_heads != 0;
+  const int nq = pair ? nblk : (nblk + 1) / 2;   // row tiles of the items
+  const int n_items = nq * (pair ? Hq / 2 : Hq) * C::NOC;
 
   if (warp == wProdWarp) {
     // ============================ producer ============================
@@ -164,10 +171,10 @@ __global__ void __launch_bounds__(wThreads, 1)
       int gq = 0, gv = 0;
       bool ok = true;
       for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
-        const WItem w = witem_of(item, n2, Hq, C::NOC);
-        const int hk = w.h / G;
-        // the union of the two query blocks' lists, ascending
-        const int qb0 = w.row0 / wKB, qb1 = qb0 + 1;
+        const WItem w = witem_of(item, nq, Hq, C::NOC, pair);
+        const int hk = w.h / G;   // = (h + 1) / G when paired
+        // the union of the two halves' lists, ascending (paired: one list)
+        const int qb0 = w.row0 / wKB, qb1 = pair ? qb0 : qb0 + 1;
         const bool has1 = qb1 < nblk;
         const int32_t *lf0 = full_idx + static_cast<size_t>(qb0) * nblk;
         const int32_t *lp0 = kv_idx + static_cast<size_t>(qb0) * nblk;
@@ -194,7 +201,10 @@ __global__ void __launch_bounds__(wThreads, 1)
             if (gq >= wNSQ && !t_wait(qkempty + 8 * s, gq / wNSQ - 1, abort_flag)) return false;
             const uint32_t dst = sQK + s * C::QK_STAGE;
             t_expect_tx(qkfull + 8 * s, C::QK_STAGE);
-            t_tma_3d(dst, &tmQ, 64 * c, w.row0, w.h, qkfull + 8 * s);   // rows past L: zeros
+            // the chunk's two 64-row halves (rows past L read zeros)
+            t_tma_3d(dst, &tmQ, 64 * c, w.row0, w.h, qkfull + 8 * s);
+            t_tma_3d(dst + wKB * 128, &tmQ, 64 * c, pair ? w.row0 : w.row0 + wKB,
+                     pair ? w.h + 1 : w.h, qkfull + 8 * s);
             t_tma_3d(dst + C::Q_CH, &tmK, 64 * c, kb * wKB, hk, qkfull + 8 * s);
             ++gq;
           }
@@ -372,8 +382,9 @@ __global__ void __launch_bounds__(wThreads, 1)
     bool ok = true;
     for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
       ++it;
-      const WItem w = witem_of(item, n2, Hq, C::NOC);
-      const int qi = w.row0 + row;
+      const WItem w = witem_of(item, nq, Hq, C::NOC, pair);
+      const int qi = pair ? w.row0 + (row & (wKB - 1)) : w.row0 + row;
+      const int hrow = pair ? w.h + (row >> 6) : w.h;   // this row's query head
       const bool valid = qi < L;
       const int dq = valid ? docs[qi] : 0;
       float m = -INFINITY, l = 0.f;
@@ -531,7 +542,7 @@ __global__ void __launch_bounds__(wThreads, 1)
           ep_g = g;
           ep_it = it;
           ep_qi = qi;
-          ep_h = w.h;
+          ep_h = hrow;
           ep_oc = w.oc;
           ep_il = lt > 0.f ? 1.f / lt : 0.f;
         }
@@ -541,10 +552,11 @@ __global__ void __launch_bounds__(wThreads, 1)
     if (ok && ep && !epilogue()) ok = false;
     if (!ok || *abort_flag) {   // a wait gave up: mark this CTA's rows as failed
       for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
-        const WItem w = witem_of(item, n2, Hq, C::NOC);
-        const int qi = w.row0 + row;
+        const WItem w = witem_of(item, nq, Hq, C::NOC, pair);
+        const int qi = pair ? w.row0 + (row & (wKB - 1)) : w.row0 + row;
         if (qi >= L) continue;
-        __nv_bfloat16 *orow = out + (static_cast<size_t>(w.h) * L + qi) * D + w.oc * wDO + OH * hf;
+        const int hrow = pair ? w.h + (row >> 6) : w.h;
+        __nv_bfloat16 *orow = out + (static_cast<size_t>(hrow) * L + qi) * D + w.oc * wDO + OH * hf;
         for (int c = 0; c < OH; ++c) orow[c] = __float2bfloat16_rn(NAN);
       }
     }
@@ -580,19 +592,22 @@ int launch_prefill_wide(const pkv_bf16 *q, const pkv_bf16 *k, const pkv_bf16 *v,
     }
   }
   CUtensorMap tmQ, tmK, tmV, tmD;
-  int st = prefill_head_map(&tmQ, q, Hq, L, D, wQR);
+  int st = prefill_head_map(&tmQ, q, Hq, L, D, wKB);   // two 64-row boxes per chunk
   if (st == PKV_OK) st = prefill_head_map(&tmK, k, Hkv, L, D, wKB);
   if (st == PKV_OK) st = prefill_head_map(&tmV, v, Hkv, L, D, wKB);
   if (st == PKV_OK) st = prefill_docs_map(&tmD, docs, L);
   if (st != PKV_OK) return st;
   const int n = (L + wKB - 1) / wKB;
-  const long long items = 1LL * ((n + 1) / 2) * Hq * TW<D>::NOC;
+  const int G = Hq / Hkv;
+  const bool pair = G % 2 == 0;
+  const long long items =
+      (pair ? 1LL * n * (Hq / 2) : 1LL * ((n + 1) / 2) * Hq) * TW<D>::NOC;
   const long long cap = pkv::sm_count();
   const int grid = static_cast<int>(items < cap ? items : cap);
   PKV_CUDA_CHECK(pkv::launch_pdl(prefill_wide_kernel<D>, dim3(grid), dim3(wThreads),
                                  TW<D>::SMEM, s, tmQ, tmK, tmV, tmD, docs, kv_num, kv_idx,
-                                 full_num, full_idx, n, L, Hq, Hq / Hkv, window,
-                                 scale * 1.4426950408889634f,
+                                 full_num, full_idx, n, L, Hq, G, window,
+                                 scale * 1.4426950408889634f, pair ? 1 : 0,
                                  reinterpret_cast<__nv_bfloat16 *>(out)));
   return PKV_OK;
 }

@@ -118,7 +118,8 @@ def _kept(docs, window=0):
     (300, 8, 1, 256, "contiguous", 0), (257, 4, 2, 256, "interleaved", 0),
     (200, 8, 1, 256, "one", 64), (700, 8, 1, 256, "many", 512), (1, 2, 1, 256, "one", 0),
     (300, 8, 1, 512, "contiguous", 0), (65, 4, 1, 512, "interleaved", 0),
-    (1, 2, 1, 512, "one", 0), (500, 8, 1, 512, "many", 0), (257, 2, 2, 512, "interleaved", 37)])
+    (1, 2, 1, 512, "one", 0), (500, 8, 1, 512, "many", 0), (257, 2, 2, 512, "interleaved", 37),
+    (300, 6, 2, 256, "many", 0), (200, 3, 1, 512, "contiguous", 50)])
 def test_prefill_attention_parity(dev, L, Hq, Hkv, D, kind, window):
     rng = np.random.default_rng(L * 10 + D + Hq + window)
     q = wl.randn_bf16(rng, (Hq, L, D))
