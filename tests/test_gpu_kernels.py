@@ -223,6 +223,11 @@ ATTN_CASES = [
     (512, 16, 2, 16, [95, 300], 0, 4),
     (64, 7, 1, 256, [1, 300, 257], 0, 0),
     (128, 40, 8, 64, [333, 64], 65, 0),
+    # one long row and few kv heads: the automatic mode cuts a (row, head) into
+    # up to 128 parts (more than a warp's worth of flags, several merge batches)
+    (128, 8, 1, 64, [8192], 0, 0),
+    (64, 4, 2, 64, [5000, 3], 0, 0),
+    (512, 8, 1, 64, [4096], 1500, 0),
 ]
 
 
