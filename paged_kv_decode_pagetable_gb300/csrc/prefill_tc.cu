@@ -422,11 +422,14 @@ __global__ void __launch_bounds__(kTCThreads, TC<D>::CTAS_PER_SM)
         t_fence_after();
         float sv[kKW];
         {
-          uint32_t r[16];
-          t_ld16(trow + C::S_COL + b * kKB + kKW * hf, r);
+          uint32_t r[kKW];
+#pragma unroll
+          for (int c = 0; c < kKW / 16; ++c)
+            t_ld16(trow + C::S_COL + b * kKB + kKW * hf + 16 * c,
+                   *reinterpret_cast<uint32_t(*)[16]>(r + 16 * c));
           t_wait_ld();
 #pragma unroll
-          for (int j = 0; j < 16; ++j) sv[j] = __uint_as_float(r[j]);
+          for (int j = 0; j < kKW; ++j) sv[j] = __uint_as_float(r[j]);
         }
         t_fence_before();   // S buffer b may be overwritten from here
         __syncwarp();
