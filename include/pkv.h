@@ -218,9 +218,10 @@ int qk_norm_rope_append(pkv_bf16 *q, pkv_bf16 *k, const pkv_bf16 *v,
  * The workspace must hold paged_decode_attn_workspace(B, Hq, D, P) bytes
  * (16-byte aligned; may be NULL when that is 0), with P = S for a fixed
  * split count or P = paged_decode_attn_splits(...) for the automatic mode.
- * It holds partials, which every call writes before reading, and per-part
- * flags: zero the workspace once before its first use (e.g. cudaMemset).
- * Every call leaves the flags zero again, except a call that reports
+ * It holds the partials, each word of which tells by itself whether it has
+ * been written in this call (a reader waits for it and clears it after
+ * use): zero the workspace once before its first use (e.g. cudaMemset).
+ * Every call leaves it zero again, except a call that reports
  * PKV_ERR_TIMEOUT in the error word, after which the workspace must be
  * zeroed again. Calls sharing one workspace must not overlap on the GPU.
  * q: bf16 [B][Hq][D], out: bf16 [B][Hq][D], caches and table as above.
@@ -390,9 +391,12 @@ int prefill_attn(const pkv_bf16 *q, const pkv_bf16 *k, const pkv_bf16 *v,
  * same cap paged_decode_attn applies. The first call on a device looks up the scratch address
  * (cudaGetSymbolAddress) with that device current; make it before any
  * stream capture begins. All calls share the scratch: calls whose kernels
- * overlap on the GPU race and must be serialized by the caller. Each call
- * first clears the scratch's part flags (cudaMemsetAsync on the caller's
- * stream); the partials need no clearing. No device memory is allocated.
+ * overlap on the GPU race and must be serialized by the caller. The
+ * scratch starts zeroed and every completed call leaves it zero; each call
+ * first launches a small kernel on the caller's stream that clears it only
+ * when *err_word holds PKV_ERR_TIMEOUT (a call that gave up on a wait can
+ * leave partials behind; with err_word NULL nothing is checked). No device
+ * memory is allocated.
  * ------------------------------------------------------------------- */
 int paged_decode_attn_noalloc(const pkv_bf16 *q, const pkv_bf16 *k_cache,
                               const pkv_bf16 *v_cache, const int32_t *dev_table,

@@ -8,12 +8,15 @@
 //
 // Design (GB300):
 //   * work: the key tiles (64 keys) of every (row, kv head). In the default
-//     (balanced) mode the (row, kv head, tile) sequence is flattened from
-//     the actual lengths and every persistent CTA takes the same number of
-//     consecutive tiles; a fixed split count (each row cut into S equal
-//     parts) is also accepted. A (row, head) finished inside one CTA writes
-//     the output directly; one that straddles CTAs leaves fp32 partials +
-//     log2-sum-exp that a combine kernel merges;
+//     (balanced) mode the (row, kv head, tile) sequence is laid on a cost
+//     line from the actual lengths and every persistent CTA takes an equal
+//     share of it; a fixed split count (each row cut into S equal parts) is
+//     also accepted. A (row, head) finished inside one CTA writes the output
+//     directly; one that straddles CTAs leaves fp32 partials + log2-sum-exp
+//     that the CTA holding its first part merges (a combine kernel, with a
+//     fixed split count). Each partial word is stored as the complement of
+//     its bits, so a zero word is one not yet written: the reader polls the
+//     data itself (no flag, no release fence) and clears it after use;
 //   * persistent CTAs (a fixed grid of SMs x CTAs/SM), each with one
 //     producer warp and four consumer warps. The producer streams, across
 //     all of the CTA's work without pausing, the query rows (cp.async.bulk)
@@ -82,7 +85,7 @@ struct Cfg {
   static constexpr int OFF_P = OFF_Q + 2 * Q_STAGE;
   static constexpr int OFF_RED = OFF_P + kT * 16;                // 2 x [4][8] f32
   static constexpr int OFF_BAR = OFF_RED + 2 * kCWarps * kMaxG * 4;
-  static constexpr int N_BARS = 4 * NS + 5;   // + the merge barrier
+  static constexpr int N_BARS = 4 * NS + 4;
   static constexpr int OFF_MASK = OFF_BAR + N_BARS * 8;           // 2 x NS u32
   static constexpr int OFF_MISC = OFF_MASK + 2 * NS * 4;          // abort flag
   static constexpr int OFF_DESC = OFF_MISC + 16;                  // Unit [2] (48 B each)
@@ -98,11 +101,6 @@ struct Cfg {
 static_assert(Cfg<64>::CTAS_PER_SM * (Cfg<64>::SMEM + 1024) <= 228 * 1024, "D=64 residency");
 static_assert(Cfg<128>::CTAS_PER_SM * (Cfg<128>::SMEM + 1024) <= 228 * 1024, "D=128 residency");
 static_assert(Cfg<256>::SMEM <= 227 * 1024 && Cfg<512>::SMEM <= 227 * 1024, "smem per CTA");
-// the two Q stages hold one part's partial (o [G][D] and lse [G], fp32) for the merge
-static_assert(2 * Cfg<64>::Q_STAGE >= kMaxG * 64 * 4 + kMaxG * 4 &&
-              2 * Cfg<128>::Q_STAGE >= kMaxG * 128 * 4 + kMaxG * 4 &&
-              2 * Cfg<256>::Q_STAGE >= kMaxG * 256 * 4 + kMaxG * 4 &&
-              2 * Cfg<512>::Q_STAGE >= kMaxG * 512 * 4 + kMaxG * 4, "merge buffer");
 
 // ---------------------------------------------------------------- PTX ----
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -533,35 +531,104 @@ __device__ __forceinline__ bool next_unit(const Problem &p, const int2 *rows, co
   return true;
 }
 
-// Flags of the later parts of a cut (row, head): part j (1 <= j < parts) sets
-// f[j] to 1 with a gpu-scope release once its partial is in the workspace.
-// The converged producer warp of the first part's CTA waits until it has seen
-// every one set (each lane one flag, relaxed polls; `peek` is the lane's
-// earlier look at its flag in the first batch), then acquires with a fence,
-// resets the flags to 0 for the next call and returns true; false if the wait
-// gives up (after kFlagSpinLimit polls, or when the CTA aborts).
-constexpr int kFlagSpinLimit = 1 << 21;
-__device__ __forceinline__ unsigned ld_relaxed_gpu(const unsigned *a) {
-  unsigned v;
+// Partials of cut (row, head)s carry their own validity. A part stores each
+// fp32 word of its partial (normalised o, lse) as the bitwise complement of
+// the float's bits, so a stored word is never 0 (its float would have the
+// bits 0xffffffff, a NaN that arithmetic never yields; such a NaN is stored
+// as the canonical one), and the workspace holds 0 wherever nothing of this
+// call has been written yet. The reader polls the words themselves with
+// relaxed gpu-scope loads until none is 0, decodes them and writes 0 back,
+// so a completed call leaves the partial area zero for the next one. No
+// flag, fence or release is needed: each word is its own message.
+constexpr int kPollLimit = 1 << 21;
+__device__ __forceinline__ uint32_t part_enc(float v) {
+  const uint32_t u = __float_as_uint(v);
+  return ~(u == 0xffffffffu ? 0x7fffffffu : u);
+}
+__device__ __forceinline__ float part_dec(uint32_t w) { return __uint_as_float(~w); }
+__device__ __forceinline__ uint32_t ld_relaxed_gpu(const float *a) {
+  uint32_t v;
   asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(a) : "memory");
   return v;
 }
-__device__ __forceinline__ bool wait_parts(unsigned *f, int parts, int lane,
-                                           volatile int *abort_flag, unsigned peek) {
-  for (int j0 = 1; j0 < parts; j0 += 32) {
-    const int j = j0 + lane;
-    bool done = j >= parts || (j0 == 1 && peek != 0u);
-    for (int i = 0; !__all_sync(0xffffffffu, done); ++i) {
-      if (i >= kFlagSpinLimit) return false;
-      if (__shfl_sync(0xffffffffu, (i & 15) == 15 ? *abort_flag : 0, 0)) return false;
-      __nanosleep(32);
-      if (!done) done = ld_relaxed_gpu(f + j) != 0u;
+__device__ __forceinline__ void st_relaxed_gpu(float *a, uint32_t v) {
+  asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(a), "r"(v) : "memory");
+}
+// The words of one (row, kv head)'s partial records that a consumer thread
+// owns: for part j, o[k] of m-tile mt (query heads h0 / h1, columns
+// dbase + 16 mt (+ 8)) and the lse of h0 / h1, in the thread's MMA fragment
+// order.
+struct PartView {
+  float *o, *lse;      // the record of part 0
+  int G, D, h0, h1, dbase;
+  bool hv0, hv1;
+  __device__ __forceinline__ bool valid(int k) const { return (k & 1) ? hv1 : hv0; }
+  __device__ __forceinline__ float *ow(int j, int mt, int k) const {
+    return o + static_cast<size_t>(j) * G * D + ((k & 1) ? h1 : h0) * D + dbase + 16 * mt +
+           ((k & 2) ? 8 : 0);
+  }
+  __device__ __forceinline__ float *lw(int j, int k) const {
+    return lse + static_cast<size_t>(j) * G + (k ? h1 : h0);
+  }
+};
+// Loads parts j0 .. j0 + NB - 1; absent parts and heads get the encoding of
+// (o = 0, lse = -inf), which merges as nothing and is never waited on.
+template <int NB, int MT>
+__device__ __forceinline__ void part_load(const PartView &v, int j0, int parts,
+                                          uint32_t (&w)[NB][MT][4], uint32_t (&l)[NB][2]) {
+#pragma unroll
+  for (int jj = 0; jj < NB; ++jj) {
+    const bool jv = j0 + jj < parts;
+#pragma unroll
+    for (int k = 0; k < 2; ++k)
+      l[jj][k] = jv && v.valid(k) ? ld_relaxed_gpu(v.lw(j0 + jj, k)) : part_enc(-INFINITY);
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        w[jj][mt][k] = jv && v.valid(k) ? ld_relaxed_gpu(v.ow(j0 + jj, mt, k)) : part_enc(0.f);
+  }
+}
+// Waits until no loaded word is 0 (the part has not written it yet),
+// re-loading only those; false if it gives up (kPollLimit polls, or the CTA
+// aborts).
+template <int NB, int MT>
+__device__ __forceinline__ bool part_wait(const PartView &v, int j0, uint32_t (&w)[NB][MT][4],
+                                          uint32_t (&l)[NB][2], volatile int *abort_flag) {
+  for (int i = 0;; ++i) {
+    bool ready = true;
+#pragma unroll
+    for (int jj = 0; jj < NB; ++jj) {
+      ready = ready && l[jj][0] != 0u && l[jj][1] != 0u;
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) ready = ready && w[jj][mt][k] != 0u;
+    }
+    if (ready) return true;
+    if (i >= kPollLimit || *abort_flag) return false;
+    __nanosleep(64);
+#pragma unroll
+    for (int jj = 0; jj < NB; ++jj) {
+#pragma unroll
+      for (int k = 0; k < 2; ++k)
+        if (l[jj][k] == 0u) l[jj][k] = ld_relaxed_gpu(v.lw(j0 + jj, k));
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          if (w[jj][mt][k] == 0u) w[jj][mt][k] = ld_relaxed_gpu(v.ow(j0 + jj, mt, k));
     }
   }
-  asm volatile("fence.acq_rel.gpu;" ::: "memory");
-  for (int j = 1 + lane; j < parts; j += 32)
-    asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(f + j), "r"(0u) : "memory");
-  return true;
+}
+// Clears part j's o words of this thread (each has this one reader).
+template <int MT>
+__device__ __forceinline__ void part_clear(const PartView &v, int j) {
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      if (v.valid(k)) st_relaxed_gpu(v.ow(j, mt, k), 0u);
 }
 
 // ------------------------------------------------------------- kernel ----
@@ -574,7 +641,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
                        const __nv_bfloat16 *__restrict__ q, const Problem p,
                        float scale_log2, float *__restrict__ o_part,
                        float *__restrict__ lse_part, int *__restrict__ parts_out,
-                       unsigned *__restrict__ flags, __nv_bfloat16 *__restrict__ out,
+                       __nv_bfloat16 *__restrict__ out,
                        int32_t *__restrict__ err, const StepArgs sa) {
   using Cf = Cfg<D>;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -587,10 +654,10 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
   float *red_max = reinterpret_cast<float *>(sm + Cf::OFF_RED);
   float *red_sum = red_max + kCWarps * kMaxG;
   const uint32_t bar0 = sK + Cf::OFF_BAR;
-  // barrier layout: fullK[NS] emptyK[NS] fullV[NS] emptyV[NS] fullQ[2] emptyQ[2] merge
+  // barrier layout: fullK[NS] emptyK[NS] fullV[NS] emptyV[NS] fullQ[2] emptyQ[2]
   const uint32_t fullK = bar0, emptyK = bar0 + 8 * Cf::NS, fullV = bar0 + 16 * Cf::NS,
                  emptyV = bar0 + 24 * Cf::NS, fullQ = bar0 + 32 * Cf::NS,
-                 emptyQ = fullQ + 16, mergeBar = fullQ + 32;
+                 emptyQ = fullQ + 16;
   uint32_t *kmask = reinterpret_cast<uint32_t *>(sm + Cf::OFF_MASK);
   uint32_t *vmask = kmask + Cf::NS;
   volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + Cf::OFF_MISC);
@@ -611,7 +678,6 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
       mbar_init(fullQ + 8 * i, 1);
       mbar_init(emptyQ + 8 * i, kCWarps);
     }
-    mbar_init(mergeBar, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     fence_proxy_async();
@@ -787,7 +853,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
     UnitIter it = itp;
     Unit w, wn;
     int it_k = 0, it_v = 0, it_q = 0;
-    bool ok = true, merge_copy = false;
+    bool ok = true;
     bool have = next_unit(p, rows, pre, prc, it, w, lane);
     int page_first = have ? box_page(w, lane) : -1;
     pkv_wait_prior_grid();
@@ -795,15 +861,6 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
       bool have_next = false, looked_ahead = false;
       int page_next = -1;
       const int n_boxes = (w.tb - w.ta) * boxes;
-      // The first part of a (row, head) cut across CTAs is this CTA's last
-      // unit: look at the later parts' flags (relaxed loads, not waited on)
-      // when the unit starts and again once all but its last tile are
-      // issued, so that their state is known when the last tile is.
-      const bool merge_unit = p.fixed_splits == 0 && w.part == 0 && w.parts > 1;
-      unsigned *const fbase = flags + (static_cast<size_t>(w.b) * p.Hkv + w.g) * p.max_parts;
-      const bool peeks = merge_unit && 1 + lane < w.parts;
-      unsigned fpeek = peeks ? ld_relaxed_gpu(fbase + 1 + lane) : 0u;
-      const int unit_tiles = w.tb - w.ta;
       // query rows of the GQA group, one bulk copy per head into padded rows
       {
         const int qs = it_q & 1;
@@ -919,7 +976,6 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
             }
           }
           ok = __shfl_sync(0xffffffffu, ok, 0);
-          if (peeks && base / boxes + tt == unit_tiles - 2) fpeek = ld_relaxed_gpu(fbase + 1 + lane);
           if (!looked_ahead) {  // next unit's table lookups, once this one is moving
             looked_ahead = true;
             have_next = next_unit(p, rows, pre, prc, it, wn, lane);
@@ -930,31 +986,6 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
       if (!looked_ahead) {
         have_next = next_unit(p, rows, pre, prc, it, wn, lane);
         page_next = have_next ? box_page(wn, lane) : -1;
-      }
-      if (ok && merge_unit) {
-        // Wait for the later parts' partials, then copy part 1's (o, then
-        // lse) into the two Q stages, free once the consumers hold this
-        // unit's query rows; the consumers merge at the unit's end.
-        ok = wait_parts(fbase, w.parts, lane, abort_flag, fpeek);
-        if (ok && lane == 0)
-          ok = mbar_wait(emptyQ + 8 * (it_q & 1), ((it_q >> 1) & 1) ^ 1, abort_flag) &&
-               mbar_wait(emptyQ + 8 * ((it_q + 1) & 1), (((it_q + 1) >> 1) & 1) ^ 1, abort_flag);
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (ok) {
-          // the o copy and the lse loads travel together; the phase completes
-          // once the copy has landed and lane 0 has arrived after the stores
-          const size_t r1 = (static_cast<size_t>(w.b) * p.Hkv + w.g) * p.max_parts + 1;
-          float *mbuf = reinterpret_cast<float *>(sm + Cf::OFF_Q);
-          if (lane == 0) {
-            asm volatile("fence.proxy.async.global;" ::: "memory");
-            mbar_expect_tx_only(mergeBar, static_cast<uint32_t>(p.G * D * 4));
-            bulk_load(sQ, o_part + r1 * p.G * D, static_cast<uint32_t>(p.G * D * 4), mergeBar);
-          }
-          if (lane < p.G) mbuf[p.G * D + lane] = __ldcg(lse_part + r1 * p.G + lane);
-          __syncwarp();
-          if (lane == 0) mbar_arrive(mergeBar);
-          merge_copy = true;
-        }
       }
       w = wn;
       page_first = page_next;
@@ -992,7 +1023,6 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
         (void)mbar_wait(fullQ + 8 * s, (last / 2) & 1, &no_abort);
       }
     }
-    if (merge_copy) (void)mbar_wait(mergeBar, 0, &no_abort);
     return;
   }
 
@@ -1128,7 +1158,31 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
     for (int mt = 0; mt < MT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
     float m_run0 = -INFINITY, m_run1 = -INFINITY, l_run0 = 0.f, l_run1 = 0.f;
 
+    // The first part of a (row, head) cut across CTAs (balanced mode) is its
+    // CTA's last unit and merges the later parts at its end. The first PF
+    // later parts are loaded when the unit's last tile starts, so that
+    // partials already written arrive with that tile; the rest follow at the
+    // end, JB per round trip to L2.
+    constexpr int JB = D <= 128 ? 4 : D == 256 ? 2 : 1;
+    constexpr int PF = 1;
+    const bool merge = p.fixed_splits == 0 && w.parts > 1 && w.part == 0;
+    PartView pv;
+    {
+      const size_t rec = (static_cast<size_t>(w.b) * p.Hkv + w.g) * p.max_parts;
+      pv.o = o_part + rec * p.G * D;
+      pv.lse = lse_part + rec * p.G;
+      pv.G = p.G;
+      pv.D = D;
+      pv.h0 = h0;
+      pv.h1 = h1;
+      pv.hv0 = hv0;
+      pv.hv1 = hv1;
+      pv.dbase = warp * (D / 4) + gid;
+    }
+    uint32_t wp[PF][MT][4], lp[PF][2];   // words of parts 1 .. PF
+
     for (int t = w.ta; t < w.tb; ++t, ++it) {
+      if (merge && t == w.tb - 1) part_load<PF, MT>(pv, 1, w.parts, wp, lp);
       const int st = it % Cf::NS;
       const uint32_t par = (it / Cf::NS) & 1;
       if (!mbar_wait(fullK + 8 * st, par, abort_flag)) {
@@ -1285,55 +1339,33 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
     // ---- epilogue ----
     // A (row, head) done inside one CTA writes its output directly. A later
     // part of a cut one (every part, in the fixed mode) writes its partial:
-    // o / l and lse = m + log2(l) per head, in the (row, kv head)'s record
-    // for that part. The first part of a cut one (balanced mode) merges the
-    // later parts' partials into its own running state and writes the output.
-    const bool balanced = p.fixed_splits == 0;
-    const bool merge = balanced && w.parts > 1 && w.part == 0;
+    // o / l and lse = m + log2(l) per head, encoded, in the (row, kv head)'s
+    // record for that part, and goes on at once. The first part of a cut one
+    // (balanced mode) merges the later parts' partials into its own running
+    // state and writes the output.
     const size_t head0 = static_cast<size_t>(w.b) * p.Hq + static_cast<size_t>(w.g) * p.G;
-    const size_t rec = (static_cast<size_t>(w.b) * p.Hkv + w.g) * p.max_parts;
     if (w.parts > 1 && !merge) {
       const float il0 = l_run0 > 0.f ? 1.f / l_run0 : 0.f;
       const float il1 = l_run1 > 0.f ? 1.f / l_run1 : 0.f;
-      float *op = o_part + (rec + w.part) * p.G * D;
 #pragma unroll
-      for (int mt = 0; mt < MT; ++mt) {
-        const int d = warp * (D / 4) + 16 * mt + gid;
-        if (hv0) {
-          op[h0 * D + d] = o[mt][0] * il0;
-          op[h0 * D + d + 8] = o[mt][2] * il0;
-        }
-        if (hv1) {
-          op[h1 * D + d] = o[mt][1] * il1;
-          op[h1 * D + d + 8] = o[mt][3] * il1;
-        }
-      }
+      for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          if (pv.valid(k))
+            st_relaxed_gpu(pv.ow(w.part, mt, k), part_enc(o[mt][k] * ((k & 1) ? il1 : il0)));
       if (warp == 0 && gid == 0) {
-        float *lp = lse_part + (rec + w.part) * p.G;
-        if (hv0) lp[h0] = l_run0 > 0.f ? m_run0 + log2f(l_run0) : -INFINITY;
-        if (hv1) lp[h1] = l_run1 > 0.f ? m_run1 + log2f(l_run1) : -INFINITY;
-      }
-      if (balanced) {   // publish the partial to the first part's CTA
-        // the barrier orders every consumer's stores before thread 0's
-        // gpu-scope release (cumulative), which the reader acquires
-        consumer_sync();
-        if (tid == 0)
-          asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(flags + rec + w.part), "r"(1u)
-                       : "memory");
+        if (hv0)
+          st_relaxed_gpu(pv.lw(w.part, 0),
+                         part_enc(l_run0 > 0.f ? m_run0 + log2f(l_run0) : -INFINITY));
+        if (hv1)
+          st_relaxed_gpu(pv.lw(w.part, 1),
+                         part_enc(l_run1 > 0.f ? m_run1 + log2f(l_run1) : -INFINITY));
       }
       continue;
     }
     if (merge) {
-      // The producer has seen every later part's flag and copied part 1's
-      // partial (o [G][D], then lse [G]) into the Q stages; later parts, when
-      // a row is cut more than twice, are read from the workspace.
-      if (!mbar_wait(mergeBar, 0, abort_flag)) {
-        failed = true;
-        *abort_flag = 1;
-        continue;
-      }
       // fold one part (normalised o, lse) into the running (m, l, unnormalised o)
-      auto merge_in = [&](float ls0, float ls1, const float (&v)[MT][4]) {
+      auto merge_in = [&](float ls0, float ls1, const uint32_t (&v)[MT][4]) {
         const float mn0 = fmaxf(m_run0, ls0), mn1 = fmaxf(m_run1, ls1);
         const float mu0 = mn0 == -INFINITY ? 0.f : mn0;
         const float mu1 = mn1 == -INFINITY ? 0.f : mn1;
@@ -1341,54 +1373,52 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
         const float a1 = exp2f(m_run1 - mu1), b1 = exp2f(ls1 - mu1);
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
-          o[mt][0] = fmaf(o[mt][0], a0, v[mt][0] * b0);
-          o[mt][2] = fmaf(o[mt][2], a0, v[mt][2] * b0);
-          o[mt][1] = fmaf(o[mt][1], a1, v[mt][1] * b1);
-          o[mt][3] = fmaf(o[mt][3], a1, v[mt][3] * b1);
+          o[mt][0] = fmaf(o[mt][0], a0, part_dec(v[mt][0]) * b0);
+          o[mt][2] = fmaf(o[mt][2], a0, part_dec(v[mt][2]) * b0);
+          o[mt][1] = fmaf(o[mt][1], a1, part_dec(v[mt][1]) * b1);
+          o[mt][3] = fmaf(o[mt][3], a1, part_dec(v[mt][3]) * b1);
         }
         l_run0 = fmaf(l_run0, a0, b0);
         l_run1 = fmaf(l_run1, a1, b1);
         m_run0 = mn0;
         m_run1 = mn1;
       };
-      {   // part 1, from the Q stages
-        const float *mbuf = reinterpret_cast<const float *>(sm + Cf::OFF_Q);
-        const float *lp = mbuf + p.G * D;
-        float v[MT][4];
+      auto give_up = [&]() {
+        failed = true;
+        *abort_flag = 1;
+        if (err) atomicOr(err, PKV_ERR_TIMEOUT);
+      };
+      if (part_wait<PF, MT>(pv, 1, wp, lp, abort_flag)) {
 #pragma unroll
-        for (int mt = 0; mt < MT; ++mt) {
-          const int d = warp * (D / 4) + 16 * mt + gid;
-          v[mt][0] = hv0 ? mbuf[h0 * D + d] : 0.f;
-          v[mt][2] = hv0 ? mbuf[h0 * D + d + 8] : 0.f;
-          v[mt][1] = hv1 ? mbuf[h1 * D + d] : 0.f;
-          v[mt][3] = hv1 ? mbuf[h1 * D + d + 8] : 0.f;
+        for (int jj = 0; jj < PF; ++jj) {
+          merge_in(part_dec(lp[jj][0]), part_dec(lp[jj][1]), wp[jj]);
+          if (1 + jj < w.parts) part_clear<MT>(pv, 1 + jj);
         }
-        merge_in(hv0 ? lp[h0] : -INFINITY, hv1 ? lp[h1] : -INFINITY, v);
+      } else {
+        give_up();
       }
-      // parts 2.. (rows cut more than twice), from the workspace, JB parts per
-      // round trip to L2
-      constexpr int JB = D <= 128 ? 4 : D == 256 ? 2 : 1;
-      for (int j0 = 2; j0 < w.parts; j0 += JB) {
-        float v[JB][MT][4], ls[JB][2];
+      for (int j0 = 1 + PF; j0 < w.parts && !failed; j0 += JB) {
+        uint32_t wb[JB][MT][4], lb[JB][2];
+        part_load<JB, MT>(pv, j0, w.parts, wb, lb);
+        if (!part_wait<JB, MT>(pv, j0, wb, lb, abort_flag)) {
+          give_up();
+          break;
+        }
 #pragma unroll
         for (int jj = 0; jj < JB; ++jj) {
-          const int j = j0 + jj;
-          const bool jv = j < w.parts;
-          const float *op = o_part + (rec + j) * p.G * D;
-          const float *lp = lse_part + (rec + j) * p.G;
-          ls[jj][0] = jv && hv0 ? __ldcg(lp + h0) : -INFINITY;
-          ls[jj][1] = jv && hv1 ? __ldcg(lp + h1) : -INFINITY;
-#pragma unroll
-          for (int mt = 0; mt < MT; ++mt) {
-            const int d = warp * (D / 4) + 16 * mt + gid;
-            v[jj][mt][0] = jv && hv0 ? __ldcg(op + h0 * D + d) : 0.f;
-            v[jj][mt][2] = jv && hv0 ? __ldcg(op + h0 * D + d + 8) : 0.f;
-            v[jj][mt][1] = jv && hv1 ? __ldcg(op + h1 * D + d) : 0.f;
-            v[jj][mt][3] = jv && hv1 ? __ldcg(op + h1 * D + d + 8) : 0.f;
-          }
+          merge_in(part_dec(lb[jj][0]), part_dec(lb[jj][1]), wb[jj]);
+          if (j0 + jj < w.parts) part_clear<MT>(pv, j0 + jj);
         }
-#pragma unroll
-        for (int jj = 0; jj < JB; ++jj) merge_in(ls[jj][0], ls[jj][1], v[jj]);
+      }
+      // every consumer thread of a head has read its lse words: clear them
+      // (the merge unit is the CTA's last, so this barrier costs no overlap)
+      consumer_sync();
+      if (failed) continue;
+      if (warp == 0 && gid == 0) {
+        for (int j = 1; j < w.parts; ++j) {
+          if (hv0) st_relaxed_gpu(pv.lw(j, 0), 0u);
+          if (hv1) st_relaxed_gpu(pv.lw(j, 1), 0u);
+        }
       }
     }
     const float il0 = l_run0 > 0.f ? 1.f / l_run0 : 0.f;
@@ -1415,10 +1445,15 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
 // count, the log-sum-exps and the first two partials are loaded together, so
 // a two-part merge needs one round trip to L2 after the attention kernel
 // completes. Part s of query head hi of (row b, kv head g) sits in record
-// (b * Hkv + g) * max_parts + s: o at [hi][D] of a [G][D] block, lse at [hi].
+// (b * Hkv + g) * max_parts + s: o at [hi][D] of a [G][D] block, lse at [hi],
+// every word encoded (part_enc); the merge clears the words it read, so the
+// partial area is zero again for the next call.
+__device__ __forceinline__ float4 part_dec4(float4 v) {
+  return make_float4(part_dec(__float_as_uint(v.x)), part_dec(__float_as_uint(v.y)),
+                     part_dec(__float_as_uint(v.z)), part_dec(__float_as_uint(v.w)));
+}
 template <int D>
-__global__ void combine_kernel(const float *__restrict__ o_part,
-                               const float *__restrict__ lse_part,
+__global__ void combine_kernel(float *__restrict__ o_part, float *__restrict__ lse_part,
                                const int *__restrict__ parts_in, const Problem p,
                                __nv_bfloat16 *__restrict__ out) {
   constexpr int CH = (D + 127) / 128;   // float4 column chunks per lane
@@ -1433,52 +1468,76 @@ __global__ void combine_kernel(const float *__restrict__ o_part,
   const int b = r / p.Hq, hh = r - b * p.Hq, g = hh / p.G, hi = hh - g * p.G;
   const size_t rec = (static_cast<size_t>(b) * p.Hkv + g) * p.max_parts;
   const size_t pstride = static_cast<size_t>(p.G) * D;     // floats between parts
-  const float *lse = lse_part + rec * p.G + hi;              // part s at lse[s * G]
-  const float *op = o_part + rec * pstride + static_cast<size_t>(hi) * D;
+  float *lse = lse_part + rec * p.G + hi;                    // part s at lse[s * G]
+  float *op = o_part + rec * pstride + static_cast<size_t>(hi) * D;
   const int parts = __ldcg(parts_in + b * p.Hkv + g);
-  float my_lse = lane < p.max_parts ? __ldcg(lse + lane * p.G) : -INFINITY;
+  float my_lse = lane < p.max_parts ? part_dec(__float_as_uint(__ldcg(lse + lane * p.G)))
+                                    : -INFINITY;
   float4 v0[CH], v1[CH];   // parts 0 and 1 (max_parts >= 2 whenever this kernel runs)
 #pragma unroll
   for (int c = 0; c < CH; ++c) {
     const int d = 4 * lane + 128 * c;
     if (d < D) {
-      v0[c] = __ldcg(reinterpret_cast<const float4 *>(op + d));
-      v1[c] = __ldcg(reinterpret_cast<const float4 *>(op + pstride + d));
+      v0[c] = part_dec4(__ldcg(reinterpret_cast<const float4 *>(op + d)));
+      v1[c] = part_dec4(__ldcg(reinterpret_cast<const float4 *>(op + pstride + d)));
     }
   }
   if (parts <= 1) return;
   if (lane >= parts) my_lse = -INFINITY;
   float m = my_lse;
-  for (int s = 32 + lane; s < parts; s += 32) m = fmaxf(m, __ldcg(lse + s * p.G));
+  for (int s = 32 + lane; s < parts; s += 32)
+    m = fmaxf(m, part_dec(__float_as_uint(__ldcg(lse + s * p.G))));
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
   __nv_bfloat16 *orow = out + static_cast<size_t>(r) * D;
+  const float4 zero4 = make_float4(0.f, 0.f, 0.f, 0.f);
+  // every lane runs every iteration (the shuffles name the whole warp); at
+  // D = 64 lanes 16-31 own no column and only skip the memory accesses
 #pragma unroll
   for (int c = 0; c < CH; ++c) {
     const int d = 4 * lane + 128 * c;
-    if (d >= D) continue;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    const bool dv = d < D;
+    float4 acc = zero4;
     float wsum = 0.f;
-    if (m != -INFINITY) {
-      for (int s = 0; s < parts; ++s) {
-        const float l = s < 32 ? __shfl_sync(0xffffffffu, my_lse, s) : __ldcg(lse + s * p.G);
-        const float4 v = s == 0   ? v0[c]
-                         : s == 1 ? v1[c]
-                                  : __ldcg(reinterpret_cast<const float4 *>(op + s * pstride + d));
-        const float wgt = l == -INFINITY ? 0.f : exp2f(l - m);
-        wsum += wgt;
-        acc.x = fmaf(wgt, v.x, acc.x);
-        acc.y = fmaf(wgt, v.y, acc.y);
-        acc.z = fmaf(wgt, v.z, acc.z);
-        acc.w = fmaf(wgt, v.w, acc.w);
-      }
+    for (int s = 0; s < parts; ++s) {
+      const float l = s < 32 ? __shfl_sync(0xffffffffu, my_lse, s)
+                             : part_dec(__float_as_uint(__ldcg(lse + s * p.G)));
+      if (!dv) continue;
+      const float4 v =
+          s == 0   ? v0[c]
+          : s == 1 ? v1[c]
+                   : part_dec4(__ldcg(reinterpret_cast<const float4 *>(op + s * pstride + d)));
+      // each lane reads its own columns: clear them now
+      *reinterpret_cast<float4 *>(op + s * pstride + d) = zero4;
+      if (m == -INFINITY) continue;
+      const float wgt = l == -INFINITY ? 0.f : exp2f(l - m);
+      wsum += wgt;
+      acc.x = fmaf(wgt, v.x, acc.x);
+      acc.y = fmaf(wgt, v.y, acc.y);
+      acc.z = fmaf(wgt, v.z, acc.z);
+      acc.w = fmaf(wgt, v.w, acc.w);
     }
+    if (!dv) continue;
     const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
     uint2 packed;
     packed.x = pack_bf16(acc.x * inv, acc.y * inv);
     packed.y = pack_bf16(acc.z * inv, acc.w * inv);
     *reinterpret_cast<uint2 *>(orow + d) = packed;
   }
+  // every lane has read every lse word it needs
+  __syncwarp();
+  for (int s = lane; s < parts; s += 32) lse[s * p.G] = 0.f;
+}
+
+// Clears the partial area of a workspace when the error word reports a wait
+// that gave up (such a call may leave written, unread partials behind).
+__global__ void scrub_after_timeout_kernel(uint32_t *__restrict__ base, size_t words,
+                                           const int32_t *__restrict__ err) {
+  if (!(__ldcg(err) & PKV_ERR_TIMEOUT)) return;
+  const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+  for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < words;
+       i += stride)
+    base[i] = 0u;
 }
 
 // ------------------------------------------------------------- host ----
@@ -1549,7 +1608,7 @@ template <int D, bool STEP>
 int launch_attn(const CUtensorMap &tmK, const CUtensorMap &tmV, const CUtensorMap &tmK3,
                 const CUtensorMap &tmV3, const pkv_bf16 *q,
                 const Problem &p, float scale_log2, float *o_part, float *lse_part,
-                int *parts, unsigned *flags, pkv_bf16 *out, int32_t *err, const StepArgs &sa,
+                int *parts, pkv_bf16 *out, int32_t *err, const StepArgs &sa,
                 cudaStream_t stream) {
   int st = set_smem_attr<D, STEP>();
   if (st != PKV_OK) return st;
@@ -1559,7 +1618,7 @@ int launch_attn(const CUtensorMap &tmK, const CUtensorMap &tmV, const CUtensorMa
   PKV_CUDA_CHECK(pkv::launch_pdl(decode_attn_kernel<D, STEP>, dim3(grid), dim3(kThreads),
                                  Cfg<D>::SMEM, stream, tmK, tmV, tmK3, tmV3,
                                  reinterpret_cast<const __nv_bfloat16 *>(q), p, scale_log2,
-                                 o_part, lse_part, parts, flags,
+                                 o_part, lse_part, parts,
                                  reinterpret_cast<__nv_bfloat16 *>(out), err, sa));
   return PKV_OK;
 }
@@ -1589,18 +1648,16 @@ extern "C" {
 
 // Workspace layout, with P the parts a (row, kv head) may be cut into:
 //   [parts per (row, kv head) for the fixed mode's combine: B*Hq ints, 256-byte padded]
-//   [o_part fp32: B*Hkv*P records of G*D, = B*Hq*P*D]
-//   [lse_part fp32: B*Hkv*P records of G, = B*Hq*P]
-//   [flags u32: one per (row, kv head, part), B*Hq*P words reserved]
-// Partials and counts are written before they are read. The flags must be
-// zero before the first call; every call that completes without
+//   [o_part: B*Hkv*P records of G*D words, = B*Hq*P*D]
+//   [lse_part: B*Hkv*P records of G words, = B*Hq*P]
+// Counts are written before they are read. The partial words (part_enc)
+// must be zero before the first call; every call that completes without
 // PKV_ERR_TIMEOUT leaves them zero again.
 
 size_t paged_decode_attn_workspace(int B, int Hq, int D, int num_splits) {
   if (num_splits <= 1 || B <= 0 || Hq <= 0 || D <= 0) return 0;
   const size_t rows = static_cast<size_t>(B) * Hq * num_splits;
-  return parts_bytes(B, Hq) + rows * D * sizeof(float) + rows * sizeof(float) +
-         rows * sizeof(unsigned);
+  return parts_bytes(B, Hq) + rows * D * sizeof(float) + rows * sizeof(float);
 }
 
 int paged_decode_attn_splits(int B, int Hkv, int D, int max_pages_per_seq,
@@ -1613,12 +1670,19 @@ int paged_decode_attn_splits(int B, int Hkv, int D, int max_pages_per_seq,
 
 }  // extern "C"
 
-void pkv::decode_flags_region(int B, int Hq, int D, int parts, size_t *offset, size_t *bytes) {
-  *offset = *bytes = 0;
-  if (paged_decode_attn_workspace(B, Hq, D, parts) == 0) return;
+int pkv::decode_scrub_after_timeout(void *workspace, int B, int Hq, int D, int parts,
+                                   const int32_t *err_word, cudaStream_t stream) {
+  if (!workspace || !err_word || paged_decode_attn_workspace(B, Hq, D, parts) == 0)
+    return PKV_OK;
   const size_t rows = static_cast<size_t>(B) * Hq * parts;
-  *offset = parts_bytes(B, Hq) + rows * D * sizeof(float) + rows * sizeof(float);
-  *bytes = rows * sizeof(unsigned);
+  const size_t words = rows * D + rows;   // o_part, then lse_part
+  uint32_t *base =
+      reinterpret_cast<uint32_t *>(static_cast<char *>(workspace) + parts_bytes(B, Hq));
+  const int sms = pkv::sm_count();
+  if (sms <= 0) return pkv::fail(PKV_E_CUDA, "paged_decode_attn: no SM count");
+  scrub_after_timeout_kernel<<<sms, 256, 0, stream>>>(base, words, err_word);
+  PKV_CUDA_CHECK(cudaGetLastError());
+  return PKV_OK;
 }
 
 
@@ -1683,12 +1747,10 @@ int decode_common(const char *fn, const pkv_bf16 *q, const pkv_bf16 *k_cache,
   }
   int *parts = nullptr;
   float *o_part = nullptr, *lse_part = nullptr;
-  unsigned *flags = nullptr;
   if (need > 0) {
     parts = static_cast<int *>(workspace);
     o_part = reinterpret_cast<float *>(static_cast<char *>(workspace) + parts_bytes(B, Hq));
     lse_part = o_part + static_cast<size_t>(B) * Hq * max_parts * D;
-    flags = reinterpret_cast<unsigned *>(lse_part + static_cast<size_t>(B) * Hq * max_parts);
   }
   const int box_rows = page_size < kT ? page_size : kT;
   CUtensorMap tmK, tmV, tmK3, tmV3;
@@ -1735,9 +1797,9 @@ int decode_common(const char *fn, const pkv_bf16 *q, const pkv_bf16 *k_cache,
   const StepArgs &a = sa ? *sa : none;
 #define PKV_LAUNCH(DD)                                                                        \
   st = sa ? launch_attn<DD, true>(tmK, tmV, tmK3, tmV3, q, p, scale_log2, o_part, lse_part,    \
-                                  parts, flags, out, err_word, a, s)                          \
+                                  parts, out, err_word, a, s)                                 \
           : launch_attn<DD, false>(tmK, tmV, tmK3, tmV3, q, p, scale_log2, o_part, lse_part,   \
-                                   parts, flags, out, err_word, a, s)
+                                   parts, out, err_word, a, s)
   switch (D) {
     case 64: PKV_LAUNCH(64); break;
     case 128: PKV_LAUNCH(128); break;
@@ -1754,8 +1816,7 @@ int decode_common(const char *fn, const pkv_bf16 *q, const pkv_bf16 *k_cache,
                  : D == 256 ? combine_kernel<256>
                             : combine_kernel<512>;
     PKV_CUDA_CHECK(pkv::launch_pdl(kern, dim3((rows_bh + wpb - 1) / wpb), dim3(wpb * 32), 0, s,
-                                   static_cast<const float *>(o_part),
-                                   static_cast<const float *>(lse_part),
+                                   o_part, lse_part,
                                    static_cast<const int *>(parts), p,
                                    reinterpret_cast<__nv_bfloat16 *>(out)));
   }

@@ -11,12 +11,15 @@
 //
 // The scratch is a file-scope __device__ array of kNoallocScratchBytes. Every
 // GPU that loads the library holds that much device memory until the process
-// exits. All calls share it and it keeps the last call's contents. The split
-// partials are written before they are read; the per-part flags must start
-// at zero, so every call clears them first (one cudaMemsetAsync on the
-// caller's stream, no allocation). Two calls whose kernels overlap on the GPU
-// (for instance on two streams, or from two threads) race on the scratch and
-// corrupt each other's results: serialize them.
+// exits. All calls share it. The split partials must be zero when a call
+// starts (the array starts zeroed, and every call that completes leaves them
+// zero); a call that gave up on a wait (PKV_ERR_TIMEOUT) can leave some
+// behind, so every call first launches a small kernel on the caller's stream
+// that clears them when the error word holds PKV_ERR_TIMEOUT and otherwise
+// returns at once (no allocation; with err_word NULL nothing is checked).
+// Two calls whose kernels overlap on the GPU (for instance on two streams,
+// or from two threads) race on the scratch and corrupt each other's
+// results: serialize them.
 //
 // The first call on each device looks the array's device address up with
 // cudaGetSymbolAddress while that device is current, and caches it; make that
@@ -87,13 +90,11 @@ int paged_decode_attn_noalloc(const pkv_bf16 *q, const pkv_bf16 *k_cache,
   void *scratch = nullptr;
   int st = scratch_address(&scratch);
   if (st != PKV_OK) return st;
-  // the part flags must be zero when a call starts; a call leaves them zero
-  // unless it gave up on a wait, so clear them every time (no allocation)
-  size_t off = 0, bytes = 0;
-  pkv::decode_flags_region(B, Hq, D, parts, &off, &bytes);
-  if (bytes > 0)
-    PKV_CUDA_CHECK(cudaMemsetAsync(static_cast<char *>(scratch) + off, 0, bytes,
-                                   static_cast<cudaStream_t>(stream)));
+  // the partials must be zero when a call starts; only a call that gave up
+  // on a wait leaves some behind
+  st = pkv::decode_scrub_after_timeout(scratch, B, Hq, D, parts, err_word,
+                                       static_cast<cudaStream_t>(stream));
+  if (st != PKV_OK) return st;
   return paged_decode_attn(q, k_cache, v_cache, dev_table, n_slots, max_pages_per_seq,
                            page_size, n_pages, batch_idx, seq_lens, window, scale, B, Hq, Hkv,
                            D, num_splits, scratch, kNoallocScratchBytes, out, err_word, stream);

@@ -25,9 +25,13 @@ int sm_count();
 // (num_splits 0 = automatic), the count its workspace is sized for with
 // paged_decode_attn_workspace; 0 if the arguments are out of range.
 int decode_max_parts(int max_pages_per_seq, int page_size, int window, int num_splits);
-// Byte offset and size of the part flags inside a workspace sized by
-// paged_decode_attn_workspace(B, Hq, D, parts) (both 0 when it is empty).
-void decode_flags_region(int B, int Hq, int D, int parts, size_t *offset, size_t *bytes);
+// Launches a kernel on `stream` that zeroes the split partials of a
+// workspace sized by paged_decode_attn_workspace(B, Hq, D, parts) when
+// *err_word reports PKV_ERR_TIMEOUT (a call that gave up on a wait can leave
+// unread partials behind); it does nothing otherwise, or when there is no
+// error word or no partial area.
+int decode_scrub_after_timeout(void *workspace, int B, int Hq, int D, int parts,
+                               const int32_t *err_word, cudaStream_t stream);
 
 // Document-causal prefill attention on tcgen05 (prefill_tc.cu), D in {64, 128};
 // arguments already validated by the public entry point.

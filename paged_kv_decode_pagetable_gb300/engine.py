@@ -59,8 +59,8 @@ class AttnWorkspace:
 
     num_splits 0 is the automatic, length-balanced mode; the workspace is
     sized for the most parts a row can be cut into in that mode. It starts
-    zeroed: the automatic mode's part flags must be zero before the first
-    call (each call leaves them zero)."""
+    zeroed: a zero partial word is one not yet written in the current call
+    (each call clears what it read, leaving the workspace zero)."""
 
     def __init__(self, B, Hq, Hkv, D, max_pages_per_seq, page_size, window, device,
                  num_splits: int = 0):

@@ -259,6 +259,31 @@ def test_splits_agree_and_many_splits(dev):
         assert d.max() <= 2.0 ** -8 and d.mean() <= 1e-4, (d.max(), d.mean())
 
 
+def test_workspace_reused_across_modes_is_left_zero(dev):
+    """Cut rows leave their partials in the workspace as self-validating words
+    (zero = not yet written) that the reader clears: one workspace serves
+    automatic and fixed-split calls in any order, and after every completed
+    call its partial area is zero again."""
+    rng = np.random.default_rng(15)
+    B, Hq, Hkv, D, ps = 5, 32, 8, 128, 64
+    case = PagedCase(rng, B, Hq, Hkv, D, ps, [3000, 17, 640, 1900, 129])
+    ref, _ = case.oracle(0, 0.0884)
+    d = case.device(dev)
+    p_auto = pkv.paged_decode_attn_splits(B, Hkv, D, case.max_pages, ps, 0)
+    n = max(pkv.paged_decode_attn_workspace(B, Hq, D, P) for P in (p_auto, 5, 2))
+    ws = torch.zeros(n, dtype=torch.uint8, device=dev)
+    counts = (B * Hq * 4 + 255) // 256 * 256       # the fixed mode's part counts come first
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    for S in (0, 5, 0, 2, 0, 0):
+        out = torch.full((B, Hq, D), float("nan"), dtype=torch.bfloat16, device=dev)
+        pkv.paged_decode_attn(d["q"], d["kc"], d["vc"], d["table"], case.n_slots, case.max_pages,
+                              ps, case.P, d["bidx"], d["lens"], 0, 0.0884, S, ws, out, err)
+        torch.cuda.synchronize()
+        assert pkv.pkv_read_error_word(err) == 0
+        assert_attn_close(f64(out), ref)
+        assert int(torch.count_nonzero(ws[counts:])) == 0, S
+
+
 def test_empty_rows_and_noop_slot_give_zeros(dev):
     rng = np.random.default_rng(6)
     case = PagedCase(rng, 4, 8, 2, 128, 16, [50, 50, 50, 50])
