@@ -6,30 +6,33 @@
 // sliding variant of the Gemma-4 script): query i keeps key j iff j <= i,
 // docs[j] == docs[i] and, with W > 0, i - j < W.
 //
-// Design: a persistent kernel, one CTA per SM, walking work
-// items of (128 query rows = two 64-row query blocks, query head).
-//   warp 16 (producer, one lane): per item, the Q tile by TMA (3-D map
-//     {column, token, head}: rows past L read zeros), then the union of the
-//     two query blocks' key-block lists (merged on the fly, ascending), each
-//     key block's K and V tiles and its 64 document ids by TMA into a
-//     3-stage ring, with a small descriptor (block; full / first / last
-//     flags; which of the two query blocks list it) in the stage.
-//   warp 17 (MMA, one lane): S = Q K^T into one of two TMEM buffers
-//     (M = 128, N = 64, K-major SW128 operands), then, one tile behind,
-//     O += P V into one of two TMEM O buffers (items alternate; P K-major
-//     from shared memory, V MN-major).
-//   warps 0-15 (softmax): warps w, w + 4, w + 8, w + 12 share the 32 query
-//     rows of TMEM lanes 32(w%4)..32(w%4)+31, one row per thread, and split
-//     the 64 keys of a tile and the D columns of O in quarters. S from TMEM,
-//     branch-free masks on partial blocks, the row maximum combined through
-//     shared memory, online softmax in the exp2 domain with lazy rescaling
-//     (O in TMEM is rescaled only when a row's maximum grows by more than
-//     2^8), P as bf16 into a swizzled shared buffer for the next MMA (zeros
-//     for the rows of a query block that does not list the key block), and
-//     an item's O / l to global memory after the next item's first tile.
-// Every wait on an mbarrier is bounded; a wait that gives up sets an abort
-// flag, every role leaves its loop, and the rows of unfinished items are
-// written as NaN, so a fault never passes silently.
+// Design: a persistent kernel, one CTA per SM. A work item is two 128-row
+// query tiles ("sub-items") of one kv head and the same query rows, one for
+// each of two softmax groups: both use every K / V tile the item loads, so
+// one group's waits and exchanges overlap the other group's work, and the
+// tiles are loaded once for both.
+//   warp 16 (producer, one lane): per item, the two Q tiles by TMA (3-D map
+//     {column, token, head}: rows past L read zeros) into the groups' Q
+//     buffers, then the union of the item's two query blocks' key-block
+//     lists (merged on the fly, ascending), each key block's K and V tiles
+//     and its 64 document ids by TMA into a 3-stage ring, with a small
+//     descriptor (block; full / first / last flags; which query block lists
+//     it) in the stage.
+//   warp 17 (MMA, one lane): per tile, S = Q K^T for both groups into their
+//     own TMEM S buffers (two each; M = 128, N = 64, K-major SW128 operands),
+//     then, one tile behind (at once for an item's last tile), O += P V for
+//     both groups into their TMEM O (P K-major from the group's shared
+//     buffer, V MN-major).
+//   warps 0-7 / 8-15 (softmax groups 0 / 1): warps w and w + 4 of a group
+//     share the 32 query rows of TMEM lanes 32(w%4)..32(w%4)+31, one row per
+//     thread, and split the 64 keys of a tile and the D columns of O in
+//     halves. S from TMEM, branch-free masks on partial blocks, the row
+//     maximum combined through shared memory, online softmax in the exp2
+//     domain with lazy rescaling (O in TMEM is rescaled only when a row's
+//     maximum grows by more than 2^8), P as bf16 into the group's swizzled
+//     shared buffer (zeros for the rows of a query block that does not list
+//     the key block), and the sub-item's O / l to global memory after its
+//     last P V.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -45,11 +48,12 @@ namespace {
 
 constexpr int kQR = kTcM;     // query rows per work item
 constexpr int kKB = 64;       // keys per tile (the block mask's block)
-constexpr int kNS = 3;        // K/V ring stages
-constexpr int kNQ = 2;        // Q tile buffers: the next item's Q loads while this one runs
-constexpr int kSplit = 4;                  // softmax warps per TMEM lane group
-constexpr int kSoftWarps = 4 * kSplit;     // each: 32 rows x 16 keys of a tile
-constexpr int kKW = 64 / kSplit;           // keys per softmax warp
+constexpr int kNS = 3;        // K/V ring stages, shared by the two groups
+constexpr int kGroups = 2;    // softmax groups: the CTA's items alternate between them
+constexpr int kSplit = 2;                         // warps of a group per TMEM lane group
+constexpr int kGroupWarps = 4 * kSplit;           // each: 32 rows x 32 keys of a tile
+constexpr int kSoftWarps = kGroups * kGroupWarps;
+constexpr int kKW = 64 / kSplit;                  // keys per softmax warp
 constexpr int kProdWarp = kSoftWarps, kMmaWarp = kSoftWarps + 1;
 constexpr int kTCThreads = (kSoftWarps + 2) * 32;
 constexpr float kLazyLog2 = 8.f;   // rescale O only when a row maximum grows past 2^8
@@ -67,29 +71,31 @@ struct TC {
   static constexpr int Q_BYTES = ATOMS * Q_ATOM;
   static constexpr int KV_BYTES = ATOMS * KV_ATOM;
   static constexpr int P_BYTES = kQR * kKB * 2;
-  static constexpr int OFF_Q = 0;
-  static constexpr int OFF_K = OFF_Q + kNQ * Q_BYTES;
+  static constexpr int OFF_Q = 0;                             // [kGroups] Q tiles
+  static constexpr int OFF_K = OFF_Q + kGroups * Q_BYTES;      // (group x: Q buffer x)
   static constexpr int OFF_V = OFF_K + kNS * KV_BYTES;
-  static constexpr int OFF_P = OFF_V + kNS * KV_BYTES;
-  static constexpr int OFF_SD = OFF_P + 2 * P_BYTES;          // int [kNS][64] key documents
-  static constexpr int OFF_XCH = OFF_SD + kNS * kKB * 4;       // float [2][kSplit][128 rows]
-  static constexpr int OFF_META = OFF_XCH + 2 * kSplit * kQR * 4;  // int4 [kNS]
+  static constexpr int OFF_P = OFF_V + kNS * KV_BYTES;        // [kGroups] P tiles
+  static constexpr int OFF_SD = OFF_P + kGroups * P_BYTES;    // int [kNS][64] key documents
+  static constexpr int OFF_XCH = OFF_SD + kNS * kKB * 4;      // float [kGroups][2][kSplit][128]
+  static constexpr int OFF_META = OFF_XCH + kGroups * 2 * kSplit * kQR * 4;  // int4 [kNS]
   static constexpr int OFF_BAR = OFF_META + kNS * 16;
-  // qfull[NQ], qempty[NQ], kvfull[NS], kvempty[NS], sfull[2], sfree[2], pfull[2],
-  // pvdone[2], ofree[2] (per O buffer, so that no waiter can fall two phases
-  // behind), drain, xbar[4] (the softmax groups' exchanges)
-  static constexpr int N_BAR = 2 * kNQ + 2 * kNS + 2 + 2 + 2 + 2 + 2 + 1 + 4;
+  // shared: qfull, qempty, kvfull[NS], kvempty[NS], drain; per group:
+  // sfull[2], sfree[2], pfull, pvdone, ofree (per item, so that no waiter
+  // can fall two phases behind), xbar[4] (the lane groups' exchanges)
+  static constexpr int GB = 11;
+  static constexpr int N_BAR = 2 + 2 * kNS + 1 + kGroups * GB;
   static constexpr int OFF_MISC = OFF_BAR + N_BAR * 8;       // tmem address, abort flag
   static constexpr int SMEM = OFF_MISC + 16 + 1024;          // + slack to align to 1024
-  static constexpr int TMEM_COLS = 512;   // S[2] (2 x 64) + O[2] (2 x 128): items alternate O
-  static constexpr int S_COL = 0, O_COL = 128, O_STRIDE = 128;
+  // per group: S[2] (2 x 64 columns) then O (D <= 128 columns)
+  static constexpr int TMEM_COLS = 512, GROUP_COLS = 256, S_COL = 0, O_COL = 128;
   static constexpr int CTAS_PER_SM = 1;
   static_assert(OFF_P % 1024 == 0 && OFF_K % 1024 == 0 && OFF_V % 1024 == 0, "atom alignment");
   static_assert(OFF_SD % 128 == 0, "TMA destination alignment");
+  static_assert(O_COL + D <= GROUP_COLS && kGroups * GROUP_COLS <= TMEM_COLS, "TMEM columns");
   static_assert(SMEM <= 232448 / CTAS_PER_SM, "shared memory per SM");
 };
 
-// A work item fills the 128 rows of the MMA in one of two ways.
+// A sub-item fills the 128 rows of the MMA in one of two ways.
 //   paired (Hq / Hkv even): one 64-row query block for two query heads h and
 //     h + 1 of one kv group, which share the key blocks and the K / V tiles
 //     (tile rows 0-63: head h, rows 64-127: head h + 1);
@@ -98,19 +104,34 @@ struct TC {
 //     blocks' lists, some of them needed by one half only.
 // Pairing visits each query block's own list once per head pair; on short
 // documents the union of two blocks' lists is nearly twice as long.
+// A work item is two sub-items of one kv head with the same rows (so the
+// same key blocks): heads h0 (group 0) and h1 (group 1). When the kv group
+// has an odd number of sub-items, its last item's second sub-item repeats
+// the first one and is not written.
 struct Item {
-  int row0, h;
+  int row0, hk, h0, h1;
+  bool two;
 };
-// work item i: the last query blocks first; items of one query block (pair)
-// are consecutive over the heads
-__device__ __forceinline__ Item item_of(int i, int nq, int Hq, bool pair) {
-  Item it;
-  const int per = pair ? Hq / 2 : Hq;
+// work item i: the last row tiles first; the items of one row tile are
+// consecutive over the kv heads
+__device__ __forceinline__ Item item_of(int i, int nq, int Hkv, int G, bool pair) {
+  const int subs = pair ? G / 2 : G;   // sub-items per kv head and row tile
+  const int sups = (subs + 1) / 2;     // items per kv head and row tile
+  const int per = Hkv * sups;
   const int ct = nq - 1 - i / per;
   const int r = i - (i / per) * per;
+  const int hk = r / sups, sp = r - hk * sups;
+  const int s0 = 2 * sp, s1 = 2 * sp + 1;
+  Item it;
   it.row0 = ct * (pair ? kKB : kQR);
-  it.h = pair ? 2 * r : r;
+  it.hk = hk;
+  it.two = s1 < subs;
+  it.h0 = hk * G + (pair ? 2 * s0 : s0);
+  it.h1 = it.two ? hk * G + (pair ? 2 * s1 : s1) : it.h0;
   return it;
+}
+__host__ __device__ constexpr int items_per_tile(int Hkv, int G, bool pair) {
+  return Hkv * (((pair ? G / 2 : G) + 1) / 2);
 }
 
 template <int D>
@@ -135,32 +156,36 @@ __global__ void __launch_bounds__(kTCThreads, TC<D>::CTAS_PER_SM)
                  sD = t_smem(sm + C::OFF_SD);
   int4 *meta = reinterpret_cast<int4 *>(sm + C::OFF_META);
   const uint32_t bar0 = t_smem(sm + C::OFF_BAR);
-  const uint32_t qfull = bar0, qempty = bar0 + 8 * kNQ, kvfull = bar0 + 16 * kNQ,
-                 kvempty = kvfull + 8 * kNS, sfull = kvempty + 8 * kNS, sfree = sfull + 16,
-                 pfull = sfree + 16, pvdone = pfull + 16, ofree = pvdone + 16, drain = ofree + 16,
-                 xbar = drain + 8;
+  const uint32_t qfull = bar0, qempty = bar0 + 8, kvfull = bar0 + 16,
+                 kvempty = kvfull + 8 * kNS, drain = kvempty + 8 * kNS, gbar0 = drain + 8;
+  // the barriers of group x
+  auto sfull = [&](int x, int b) { return gbar0 + 8 * C::GB * x + 8 * b; };
+  auto sfree = [&](int x, int b) { return gbar0 + 8 * C::GB * x + 16 + 8 * b; };
+  auto pfull = [&](int x) { return gbar0 + 8 * C::GB * x + 32; };
+  auto pvdone = [&](int x) { return gbar0 + 8 * C::GB * x + 40; };
+  auto ofree = [&](int x) { return gbar0 + 8 * C::GB * x + 48; };
+  auto xbar = [&](int x, int lg) { return gbar0 + 8 * C::GB * x + 56 + 8 * lg; };
   uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + C::OFF_MISC);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + C::OFF_MISC + 4);
 
   if (tid == 0) {
-    for (int i = 0; i < kNQ; ++i) {
-      t_bar_init(qfull + 8 * i, 1);
-      t_bar_init(qempty + 8 * i, 1);
-    }
+    t_bar_init(qfull, 1);
+    t_bar_init(qempty, 1);
     for (int i = 0; i < kNS; ++i) {
       t_bar_init(kvfull + 8 * i, 1);
       t_bar_init(kvempty + 8 * i, 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      t_bar_init(sfull + 8 * i, 1);
-      t_bar_init(sfree + 8 * i, kSoftWarps);
-      t_bar_init(pfull + 8 * i, kSoftWarps);
-      t_bar_init(pvdone + 8 * i, 1);
-    }
-    t_bar_init(ofree, kSoftWarps);
-    t_bar_init(ofree + 8, kSoftWarps);
     t_bar_init(drain, 1);
-    for (int i = 0; i < 4; ++i) t_bar_init(xbar + 8 * i, kSplit);
+    for (int x = 0; x < kGroups; ++x) {
+      for (int b = 0; b < 2; ++b) {
+        t_bar_init(sfull(x, b), 1);
+        t_bar_init(sfree(x, b), kGroupWarps);
+      }
+      t_bar_init(pfull(x), kGroupWarps);
+      t_bar_init(pvdone(x), 1);
+      t_bar_init(ofree(x), kGroupWarps);
+      for (int i = 0; i < 4; ++i) t_bar_init(xbar(x, i), kSplit);
+    }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -178,8 +203,9 @@ __global__ void __launch_bounds__(kTCThreads, TC<D>::CTAS_PER_SM)
   pkv_allow_next_grid();
 
   const bool pair = pair_heads != 0;
+  const int Hkv = Hq / G;
   const int nq = pair ? nblk : (nblk + 1) / 2;   // row tiles of the items
-  const int n_items = nq * (pair ? Hq / 2 : Hq);
+  const int n_items = nq * items_per_tile(Hkv, G, pair);
 
   if (warp == kProdWarp) {
     // ============================ producer ============================
@@ -187,20 +213,23 @@ __global__ void __launch_bounds__(kTCThreads, TC<D>::CTAS_PER_SM)
       int g = 0, it = 0;
       bool ok = true;
       for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++it) {
-        const Item w = item_of(item, nq, Hq, pair);
-        const int hk = w.h / G;   // = (h + 1) / G when paired (G even, h even)
-        const int qs = it % kNQ;
-        if (it >= kNQ && !t_wait(qempty + 8 * qs, it / kNQ - 1, abort_flag)) break;
-        t_expect_tx(qfull + 8 * qs, C::Q_BYTES);
-        // the tile's two 64-row halves (rows past L read zeros)
+        const Item w = item_of(item, nq, Hkv, G, pair);
+        // both Q tiles of the item (the two groups'), each as two 64-row halves
+        // (rows past L read zeros), once the previous item's last S is done
+        if (it >= 1 && !t_wait(qempty, it - 1, abort_flag)) break;
+        t_expect_tx(qfull, kGroups * C::Q_BYTES);
 #pragma unroll
-        for (int a = 0; a < C::ATOMS; ++a) {
-          const uint32_t dst = sQ + qs * C::Q_BYTES + a * C::Q_ATOM;
-          t_tma_3d(dst, &tmQ, 64 * a, w.row0, w.h, qfull + 8 * qs);
-          t_tma_3d(dst + kKB * 128, &tmQ, 64 * a, pair ? w.row0 : w.row0 + kKB,
-                   pair ? w.h + 1 : w.h, qfull + 8 * qs);
+        for (int x = 0; x < kGroups; ++x) {
+          const int h = x ? w.h1 : w.h0;
+#pragma unroll
+          for (int a = 0; a < C::ATOMS; ++a) {
+            const uint32_t dst = sQ + x * C::Q_BYTES + a * C::Q_ATOM;
+            t_tma_3d(dst, &tmQ, 64 * a, w.row0, h, qfull);
+            t_tma_3d(dst + kKB * 128, &tmQ, 64 * a, pair ? w.row0 : w.row0 + kKB,
+                     pair ? h + 1 : h, qfull);
+          }
         }
-        // the union of the two halves' lists, ascending (paired: one list)
+        // the union of the two query blocks' lists, ascending (paired: one list)
         const int qb0 = w.row0 / kKB, qb1 = pair ? qb0 : qb0 + 1;
         const bool has1 = qb1 < nblk;
         const int32_t *lf0 = full_idx + static_cast<size_t>(qb0) * nblk;
@@ -213,8 +242,8 @@ __global__ void __launch_bounds__(kTCThreads, TC<D>::CTAS_PER_SM)
         int i0 = 0, i1 = 0, i2 = 0, i3 = 0;
         auto head = [&](const int32_t *a, int cnt, int &i) -> int {
           while (i < cnt) {
-            const int x = a[i];
-            if (x >= 0 && x < nblk) return x;
+            const int v = a[i];
+            if (v >= 0 && v < nblk) return v;
             ++i;
           }
           return INT_MAX;
@@ -223,14 +252,14 @@ __global__ void __launch_bounds__(kTCThreads, TC<D>::CTAS_PER_SM)
         auto emit = [&](int kb, int flags) -> bool {
           const int s = g % kNS;
           if (g >= kNS && !t_wait(kvempty + 8 * s, g / kNS - 1, abort_flag)) return false;
-          meta[s] = make_int4(kb, flags, w.row0, w.h);
+          meta[s] = make_int4(kb, flags, w.row0, w.hk);
           t_expect_tx(kvfull + 8 * s, 2 * C::KV_BYTES + kKB * 4);
           t_tma_1d(sD + s * kKB * 4, &tmD, kb * kKB, kvfull + 8 * s);   // past L: zeros
 #pragma unroll
           for (int a = 0; a < C::ATOMS; ++a) {
-            t_tma_3d(sK + s * C::KV_BYTES + a * C::KV_ATOM, &tmK, 64 * a, kb * kKB, hk,
+            t_tma_3d(sK + s * C::KV_BYTES + a * C::KV_ATOM, &tmK, 64 * a, kb * kKB, w.hk,
                      kvfull + 8 * s);
-            t_tma_3d(sV + s * C::KV_BYTES + a * C::KV_ATOM, &tmV, 64 * a, kb * kKB, hk,
+            t_tma_3d(sV + s * C::KV_BYTES + a * C::KV_ATOM, &tmV, 64 * a, kb * kKB, w.hk,
                      kvfull + 8 * s);
           }
           ++g;
@@ -267,33 +296,36 @@ __global__ void __launch_bounds__(kTCThreads, TC<D>::CTAS_PER_SM)
     // ============================== MMA ===============================
     if (lane == 0) {
       constexpr uint32_t idS = t_idesc(kKB, 0), idO = t_idesc(D, 1);
-      int g = 0, it = 0, pv_item = 0, prev_flags = 0;
-      bool ok = true, pv_pending = false;
-      // P V of tile gp into O[item & 1]; an item's first one overwrites that
-      // buffer, once the epilogue of the item two back has read it
-      auto do_pv = [&](int gp, int flags) -> bool {
-        const int bp = gp & 1, sp = gp % kNS;
-        if (!t_wait(pfull + 8 * bp, gp >> 1, abort_flag)) return false;
-        if ((flags & kFirst) && pv_item > 1 &&
-            !t_wait(ofree + 8 * (pv_item & 1), (pv_item - 2) >> 1, abort_flag))
-          return false;
-        t_fence_after();
-        const uint32_t ocol = C::O_COL + C::O_STRIDE * (pv_item & 1);
+      int g = 0, it = 0, npv = 0, nfirst = 0;
+      bool ok = true;
+      // P V of the tile in stage sp for both groups into their O; an item's
+      // first one overwrites O, once the epilogue of the group's previous
+      // item has read it
+      auto do_pv = [&](int sp, int flags) -> bool {
 #pragma unroll
-        for (int k = 0; k < kKB / 16; ++k) {
-          const uint64_t a = t_desc(sP + bp * C::P_BYTES + k * 32, 16, 1024);
-          const uint64_t b = t_desc(sV + sp * C::KV_BYTES + k * 2048, C::KV_ATOM, 1024);
-          t_mma(tmem + ocol, a, b, idO, (k > 0 || !(flags & kFirst)) ? 1u : 0u);
+        for (int x = 0; x < kGroups; ++x) {
+          if (!t_wait(pfull(x), npv, abort_flag)) return false;
+          if ((flags & kFirst) && nfirst >= 1 && !t_wait(ofree(x), nfirst - 1, abort_flag))
+            return false;
+          t_fence_after();
+          const uint32_t ocol = C::GROUP_COLS * x + C::O_COL;
+#pragma unroll
+          for (int k = 0; k < kKB / 16; ++k) {
+            const uint64_t a = t_desc(sP + x * C::P_BYTES + k * 32, 16, 1024);
+            const uint64_t b = t_desc(sV + sp * C::KV_BYTES + k * 2048, C::KV_ATOM, 1024);
+            t_mma(tmem + ocol, a, b, idO, (k > 0 || !(flags & kFirst)) ? 1u : 0u);
+          }
+          t_commit(pvdone(x));
         }
-        t_commit(pvdone + 8 * bp);
         t_commit(kvempty + 8 * sp);
-        if (flags & kLast) ++pv_item;
+        ++npv;
+        if (flags & kFirst) ++nfirst;
         return true;
       };
+      bool pend = false;
+      int pstage = 0, pflags = 0;
       for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++it) {
-        const int qs = it % kNQ;
-        if (!t_wait(qfull + 8 * qs, it / kNQ, abort_flag)) break;
-        const uint32_t sQi = sQ + qs * C::Q_BYTES;
+        if (!t_wait(qfull, it, abort_flag)) break;
         int flags = 0;
         do {
           const int s = g % kNS, b = g & 1;
@@ -302,107 +334,82 @@ __global__ void __launch_bounds__(kTCThreads, TC<D>::CTAS_PER_SM)
             break;
           }
           flags = meta[s].y;
-          if (g >= 2 && !t_wait(sfree + 8 * b, (g >> 1) - 1, abort_flag)) {
-            ok = false;
-            break;
-          }
+#pragma unroll
+          for (int x = 0; x < kGroups; ++x)
+            if (g >= 2 && !t_wait(sfree(x, b), (g >> 1) - 1, abort_flag)) ok = false;
+          if (!ok) break;
           t_fence_after();
 #pragma unroll
-          for (int k = 0; k < D / 16; ++k) {
-            const uint64_t a = t_desc(sQi + (k >> 2) * C::Q_ATOM + (k & 3) * 32, 16, 1024);
-            const uint64_t bd =
-                t_desc(sK + s * C::KV_BYTES + (k >> 2) * C::KV_ATOM + (k & 3) * 32, 16, 1024);
-            t_mma(tmem + C::S_COL + b * kKB, a, bd, idS, k > 0 ? 1u : 0u);
+          for (int x = 0; x < kGroups; ++x) {
+            const uint32_t sQi = sQ + x * C::Q_BYTES;
+#pragma unroll
+            for (int k = 0; k < D / 16; ++k) {
+              const uint64_t a = t_desc(sQi + (k >> 2) * C::Q_ATOM + (k & 3) * 32, 16, 1024);
+              const uint64_t bd =
+                  t_desc(sK + s * C::KV_BYTES + (k >> 2) * C::KV_ATOM + (k & 3) * 32, 16, 1024);
+              t_mma(tmem + C::GROUP_COLS * x + C::S_COL + b * kKB, a, bd, idS, k > 0 ? 1u : 0u);
+            }
+            t_commit(sfull(x, b));
           }
-          t_commit(sfull + 8 * b);
-          if (flags & kLast) t_commit(qempty + 8 * qs);
-          // P V one tile behind S (across items too: the next item's first S
-          // goes in before the previous item's last P V)
-          if (pv_pending && !do_pv(g - 1, prev_flags)) {
+          if (flags & kLast) t_commit(qempty);
+          // P V one tile behind S, so that the groups' softmax of this tile
+          // overlaps the tensor core; an item's last tile goes at once (its
+          // epilogue must not wait for the next item's Q tiles)
+          if (pend && !do_pv(pstage, pflags)) {
             ok = false;
             break;
           }
-          pv_pending = true;
-          prev_flags = flags;
+          pend = !(flags & kLast);
+          if (pend) {
+            pstage = s;
+            pflags = flags;
+          } else if (!do_pv(s, flags)) {
+            ok = false;
+            break;
+          }
           ++g;
         } while (!(flags & kLast));
       }
-      if (ok && pv_pending) do_pv(g - 1, prev_flags);
       // every issued MMA completes before the TMEM is released
       t_commit(drain);
       t_wait_drain(drain);
     }
   } else {
     // ============================ softmax =============================
-    const int lg = warp & 3, hf = warp >> 2;          // lane group, key / column quarter
+    const int x = warp / kGroupWarps;                           // this warp's group
+    const int lg = warp & 3, hf = (warp >> 2) & (kSplit - 1);   // lane group, key / column half
     const int row = 32 * lg + lane;
-    const uint32_t trow = tmem + (static_cast<uint32_t>(32 * lg) << 16);
-    float *xch = reinterpret_cast<float *>(sm + C::OFF_XCH);   // [2 slots][kSplit][128]
-    // exchange number xn of the group (the kSplit warps on these rows): each
-    // publishes a per-row value, all wait (bounded) for the group's arrivals
-    // and read every value; slots alternate, so a slot is rewritten only
-    // after every member has read it
+    const uint32_t trow = tmem + (static_cast<uint32_t>(32 * lg) << 16) + C::GROUP_COLS * x;
+    float *xch = reinterpret_cast<float *>(sm + C::OFF_XCH) + x * 2 * kSplit * kQR;
+    // exchange number xn of the lane group (the kSplit warps on these rows):
+    // each publishes a per-row value, all wait (bounded) for the group's
+    // arrivals and read every value; slots alternate, so a slot is rewritten
+    // only after every member has read it
     int xn = 0;
     auto exchange = [&](float mine, float (&all)[kSplit]) -> bool {
       const int slot = xn & 1;
       xch[(slot * kSplit + hf) * kQR + row] = mine;
       __syncwarp();
-      if (lane == 0) t_arrive(xbar + 8 * lg);
-      if (!t_wait_warp(xbar + 8 * lg, xn, abort_flag)) return false;
+      if (lane == 0) t_arrive(xbar(x, lg));
+      if (!t_wait_warp(xbar(x, lg), xn, abort_flag)) return false;
 #pragma unroll
       for (int q = 0; q < kSplit; ++q) all[q] = xch[(slot * kSplit + q) * kQR + row];
       ++xn;
       return true;
     };
     constexpr int OH = D / kSplit;                                // O columns of this warp
-    // the epilogue of an item (O / l to global memory) runs after the next
-    // item's first tile, when that item's last P V is long done
-    bool ep = false;
-    int ep_g = 0, ep_it = 0, ep_qi = 0, ep_h = 0;
-    float ep_il = 0.f;
-    auto epilogue = [&]() -> bool {
-      if (!t_wait_warp(pvdone + 8 * (ep_g & 1), ep_g >> 1, abort_flag)) return false;
-      t_fence_after();
-      const bool valid = ep_qi < L;
-      const uint32_t ocol = C::O_COL + C::O_STRIDE * (ep_it & 1) + OH * hf;
-      __nv_bfloat16 *orow = out + (static_cast<size_t>(ep_h) * L + (valid ? ep_qi : 0)) * D + OH * hf;
-      const float il = ep_il;
-#pragma unroll
-      for (int c = 0; c < OH / 16; ++c) {
-        uint32_t r[16];
-        t_ld16(trow + ocol + 16 * c, r);
-        t_wait_ld();
-        if (valid) {
-          uint4 v0, v1;
-          v0.x = t_pack(__uint_as_float(r[0]) * il, __uint_as_float(r[1]) * il);
-          v0.y = t_pack(__uint_as_float(r[2]) * il, __uint_as_float(r[3]) * il);
-          v0.z = t_pack(__uint_as_float(r[4]) * il, __uint_as_float(r[5]) * il);
-          v0.w = t_pack(__uint_as_float(r[6]) * il, __uint_as_float(r[7]) * il);
-          v1.x = t_pack(__uint_as_float(r[8]) * il, __uint_as_float(r[9]) * il);
-          v1.y = t_pack(__uint_as_float(r[10]) * il, __uint_as_float(r[11]) * il);
-          v1.z = t_pack(__uint_as_float(r[12]) * il, __uint_as_float(r[13]) * il);
-          v1.w = t_pack(__uint_as_float(r[14]) * il, __uint_as_float(r[15]) * il);
-          *reinterpret_cast<uint4 *>(orow + 16 * c) = v0;
-          *reinterpret_cast<uint4 *>(orow + 16 * c + 8) = v1;
-        }
-      }
-      t_fence_before();
-      __syncwarp();
-      if (lane == 0) t_arrive(ofree + 8 * (ep_it & 1));
-      ep = false;
-      return true;
-    };
-    int g = 0, it = -1;
+    const uint32_t ocol = C::O_COL + OH * hf;
+    int g = 0;
     bool ok = true;
     for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
-      ++it;
-      const Item w = item_of(item, nq, Hq, pair);
-      const uint32_t ocol_it = C::O_COL + C::O_STRIDE * (it & 1) + OH * hf;
+      const Item w = item_of(item, nq, Hkv, G, pair);
+      const int hx = x ? w.h1 : w.h0;
+      const bool write = x == 0 || w.two;   // a repeated sub-item is not written
       const int qi = pair ? w.row0 + (row & (kKB - 1)) : w.row0 + row;
-      const int hrow = pair ? w.h + (row >> 6) : w.h;   // this row's query head
+      const int hrow = pair ? hx + (row >> 6) : hx;   // this row's query head
       const bool valid = qi < L;
       const int dq = valid ? docs[qi] : 0;
-      float m = -INFINITY, l = 0.f;   // l: this half's share of the row sum
+      float m = -INFINITY, l = 0.f;   // l: this warp's share of the row sum
       int flags = 0;
       do {
         const int s = g % kNS, b = g & 1;
@@ -414,11 +421,11 @@ __global__ void __launch_bounds__(kTCThreads, TC<D>::CTAS_PER_SM)
         flags = md.y;
         const int j0 = md.x * kKB + kKW * hf;   // first key of this warp
         const bool partial = !(flags & kFull);
-        if (!t_wait_warp(sfull + 8 * b, g >> 1, abort_flag)) {
+        const int *dks = reinterpret_cast<const int *>(sm + C::OFF_SD) + s * kKB + kKW * hf;
+        if (!t_wait_warp(sfull(x, b), g >> 1, abort_flag)) {
           ok = false;
           break;
         }
-        const int *dks = reinterpret_cast<const int *>(sm + C::OFF_SD) + s * kKB + kKW * hf;
         t_fence_after();
         float sv[kKW];
         {
@@ -429,160 +436,166 @@ __global__ void __launch_bounds__(kTCThreads, TC<D>::CTAS_PER_SM)
                    *reinterpret_cast<uint32_t(*)[16]>(r + 16 * c));
           t_wait_ld();
 #pragma unroll
-          for (int j = 0; j < kKW; ++j) sv[j] = __uint_as_float(r[j]);
+          for (int c = 0; c < kKW; ++c) sv[c] = __uint_as_float(r[c]);
         }
         t_fence_before();   // S buffer b may be overwritten from here
         __syncwarp();
-        if (lane == 0) t_arrive(sfree + 8 * b);
+        if (lane == 0) t_arrive(sfree(x, b));
         // a block not listed for this lane group's query block keeps nothing
         // for its rows: P = 0 there, no exchange, no softmax update (all warps
-        // of the group take this branch together)
+        // of the lane group take this branch together)
         const bool need = (flags & (lg < 2 ? kNeed0 : kNeed1)) != 0;
-        if (!need) {
-          if (g >= 2 && !t_wait_warp(pvdone + 8 * b, (g >> 1) - 1, abort_flag)) {
+        float alpha = 1.f;
+        bool resc = false;
+        if (need) {
+          if (flags & kMaskAll) {
+#pragma unroll
+            for (int c = 0; c < kKW; ++c) sv[c] = -INFINITY;
+          } else if (partial && window == 0 && j0 + kKW <= w.row0 && valid) {
+            // keys all before the item's rows and inside L: the document test alone
+#pragma unroll
+            for (int c = 0; c < kKW; ++c) sv[c] = dks[c] == dq ? sv[c] : -INFINITY;
+          } else if (partial) {
+#pragma unroll
+            for (int c = 0; c < kKW; ++c) {
+              const int key = j0 + c;   // every term evaluated: no branch per element
+              const bool keep = valid & (key <= qi) & (key < L) & (dks[c] == dq) &
+                                ((window == 0) | (qi - key < window));
+              sv[c] = keep ? sv[c] : -INFINITY;
+            }
+          }
+          // raw-score maximum of this warp's keys (four chains), then of the row
+          float x0 = sv[0], x1 = sv[1], x2 = sv[2], x3 = sv[3];
+#pragma unroll
+          for (int c = 4; c < kKW; c += 4) {
+            x0 = fmaxf(x0, sv[c]);
+            x1 = fmaxf(x1, sv[c + 1]);
+            x2 = fmaxf(x2, sv[c + 2]);
+            x3 = fmaxf(x3, sv[c + 3]);
+          }
+          float mall[kSplit];
+          if (!exchange(fmaxf(fmaxf(x0, x1), fmaxf(x2, x3)), mall)) {
             ok = false;
             break;
           }
-          uint8_t *prow = sm + C::OFF_P + b * C::P_BYTES + row * 128;
+          float mraw = mall[0];
 #pragma unroll
-          for (int q4 = 0; q4 < kKW / 8; ++q4) {
-            const int ch = (kKW / 8) * hf + q4;
-            *reinterpret_cast<uint4 *>(prow + ((ch ^ (row & 7)) << 4)) = make_uint4(0, 0, 0, 0);
+          for (int q = 1; q < kSplit; ++q) mraw = fmaxf(mraw, mall[q]);
+          const float mt = mraw * scale_log2;   // -inf stays -inf (scale > 0)
+          // lazy online softmax: a stale maximum is kept unless the new one
+          // exceeds it by more than 2^8 (O and l use the same maximum, so the
+          // result is exact either way); the lane group's warps decide alike
+          if (mt != -INFINITY) {
+            if (m == -INFINITY) {
+              m = mt;
+            } else if (mt > m + kLazyLog2) {
+              alpha = exp2f(m - mt);
+              m = mt;
+              resc = true;
+            }
           }
-        } else {
-        if (flags & kMaskAll) {
+          const float mneg = m == -INFINITY ? 0.f : -m;
+          float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
 #pragma unroll
-          for (int c = 0; c < kKW; ++c) sv[c] = -INFINITY;
-        } else if (partial && window == 0 && j0 + kKW <= w.row0 && valid) {
-          // keys all before the item's rows and inside L: the document test alone
-#pragma unroll
-          for (int c = 0; c < kKW; ++c) sv[c] = dks[c] == dq ? sv[c] : -INFINITY;
-        } else if (partial) {
-#pragma unroll
-          for (int c = 0; c < kKW; ++c) {
-            const int key = j0 + c;   // every term evaluated: no branch per element
-            const bool keep = valid & (key <= qi) & (key < L) & (dks[c] == dq) &
-                              ((window == 0) | (qi - key < window));
-            sv[c] = keep ? sv[c] : -INFINITY;
+          for (int c = 0; c < kKW; c += 4) {   // masked scores are -inf: exp2 gives 0
+            sv[c] = t_ex2(fmaf(sv[c], scale_log2, mneg));
+            sv[c + 1] = t_ex2(fmaf(sv[c + 1], scale_log2, mneg));
+            sv[c + 2] = t_ex2(fmaf(sv[c + 2], scale_log2, mneg));
+            sv[c + 3] = t_ex2(fmaf(sv[c + 3], scale_log2, mneg));
+            s0 += sv[c];
+            s1 += sv[c + 1];
+            s2 += sv[c + 2];
+            s3 += sv[c + 3];
           }
+          l = l * alpha + ((s0 + s1) + (s2 + s3));
         }
-        // raw-score maximum of this warp's keys (four chains), then of the row
-        float x0 = sv[0], x1 = sv[1], x2 = sv[2], x3 = sv[3];
-#pragma unroll
-        for (int c = 4; c < kKW; c += 4) {
-          x0 = fmaxf(x0, sv[c]);
-          x1 = fmaxf(x1, sv[c + 1]);
-          x2 = fmaxf(x2, sv[c + 2]);
-          x3 = fmaxf(x3, sv[c + 3]);
-        }
-        float mall[kSplit];
-        if (!exchange(fmaxf(fmaxf(x0, x1), fmaxf(x2, x3)), mall)) {
+        // the group's P buffer and O are free once its previous P V is done
+        if (g >= 1 && !t_wait_warp(pvdone(x), g - 1, abort_flag)) {
           ok = false;
           break;
         }
-        float mraw = mall[0];
-#pragma unroll
-        for (int q = 1; q < kSplit; ++q) mraw = fmaxf(mraw, mall[q]);
-        const float mt = mraw * scale_log2;   // -inf stays -inf (scale > 0)
-        // lazy online softmax: a stale maximum is kept unless the new one
-        // exceeds it by more than 2^8 (O and l use the same maximum, so the
-        // result is exact either way); the group's warps decide alike
-        float alpha = 1.f;
-        bool resc = false;
-        if (mt != -INFINITY) {
-          if (m == -INFINITY) {
-            m = mt;
-          } else if (mt > m + kLazyLog2) {
-            alpha = exp2f(m - mt);
-            m = mt;
-            resc = true;
-          }
-        }
-        const float mneg = m == -INFINITY ? 0.f : -m;
-        float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-#pragma unroll
-        for (int c = 0; c < kKW; c += 4) {   // masked scores are -inf: exp2 gives 0
-          sv[c] = t_ex2(fmaf(sv[c], scale_log2, mneg));
-          sv[c + 1] = t_ex2(fmaf(sv[c + 1], scale_log2, mneg));
-          sv[c + 2] = t_ex2(fmaf(sv[c + 2], scale_log2, mneg));
-          sv[c + 3] = t_ex2(fmaf(sv[c + 3], scale_log2, mneg));
-          s0 += sv[c];
-          s1 += sv[c + 1];
-          s2 += sv[c + 2];
-          s3 += sv[c + 3];
-        }
-        l = l * alpha + ((s0 + s1) + (s2 + s3));
         if (__any_sync(0xffffffffu, resc)) {   // this warp's columns of O *= alpha
-          if (!t_wait_warp(pvdone + 8 * ((g - 1) & 1), (g - 1) >> 1, abort_flag)) {
-            ok = false;
-            break;
-          }
           t_fence_after();
 #pragma unroll
           for (int c = 0; c < OH / 16; ++c) {
             uint32_t r[16];
-            t_ld16(trow + ocol_it + 16 * c, r);
+            t_ld16(trow + ocol + 16 * c, r);
             t_wait_ld();
 #pragma unroll
-            for (int j = 0; j < 16; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * alpha);
-            t_st16(trow + ocol_it + 16 * c, r);
+            for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+            t_st16(trow + ocol + 16 * c, r);
           }
           t_wait_st();
         }
-        // P into buffer b (free once the P V of tile g - 2 is done): this
-        // warp's 16 keys are 16-byte chunks 2 hf and 2 hf + 1 of the row
-        if (g >= 2 && !t_wait_warp(pvdone + 8 * b, (g >> 1) - 1, abort_flag)) {
-          ok = false;
-          break;
-        }
-        {
-          uint8_t *prow = sm + C::OFF_P + b * C::P_BYTES + row * 128;
+        {   // this warp's keys are 16-byte chunks (kKW / 8) hf .. of the row
+          uint8_t *prow = sm + C::OFF_P + x * C::P_BYTES + row * 128;
 #pragma unroll
           for (int q4 = 0; q4 < kKW / 8; ++q4) {
             const int ch = (kKW / 8) * hf + q4;
-            uint4 v;
-            v.x = t_pack(sv[8 * q4 + 0], sv[8 * q4 + 1]);
-            v.y = t_pack(sv[8 * q4 + 2], sv[8 * q4 + 3]);
-            v.z = t_pack(sv[8 * q4 + 4], sv[8 * q4 + 5]);
-            v.w = t_pack(sv[8 * q4 + 6], sv[8 * q4 + 7]);
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            if (need) {
+              v.x = t_pack(sv[8 * q4 + 0], sv[8 * q4 + 1]);
+              v.y = t_pack(sv[8 * q4 + 2], sv[8 * q4 + 3]);
+              v.z = t_pack(sv[8 * q4 + 4], sv[8 * q4 + 5]);
+              v.w = t_pack(sv[8 * q4 + 6], sv[8 * q4 + 7]);
+            }
             *reinterpret_cast<uint4 *>(prow + ((ch ^ (row & 7)) << 4)) = v;
           }
         }
-        }   // need
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         t_fence_before();
         __syncwarp();
-        if (lane == 0) t_arrive(pfull + 8 * b);
-        if (ep && !epilogue()) {   // the previous item's output
-          ok = false;
-          break;
-        }
-        if (flags & kLast) {   // this item's row sum; its output comes after the next tile
+        if (lane == 0) t_arrive(pfull(x));
+        if (flags & kLast) {   // the row sum, then O / l once this last P V is done
           float lall[kSplit];
           if (!exchange(l, lall)) {
             ok = false;
             break;
           }
-          float lt = lall[0];   // the same order in every warp of the group
+          float lt = lall[0];   // the same order in every warp of the lane group
 #pragma unroll
           for (int q = 1; q < kSplit; ++q) lt += lall[q];
-          ep = true;
-          ep_g = g;
-          ep_it = it;
-          ep_qi = qi;
-          ep_h = hrow;
-          ep_il = lt > 0.f ? 1.f / lt : 0.f;
+          const float il = lt > 0.f ? 1.f / lt : 0.f;
+          if (!t_wait_warp(pvdone(x), g, abort_flag)) {
+            ok = false;
+            break;
+          }
+          t_fence_after();
+          __nv_bfloat16 *orow =
+              out + (static_cast<size_t>(hrow) * L + (valid ? qi : 0)) * D + OH * hf;
+#pragma unroll
+          for (int c = 0; c < OH / 16; ++c) {
+            uint32_t r[16];
+            t_ld16(trow + ocol + 16 * c, r);
+            t_wait_ld();
+            if (valid && write) {
+              uint4 v0, v1;
+              v0.x = t_pack(__uint_as_float(r[0]) * il, __uint_as_float(r[1]) * il);
+              v0.y = t_pack(__uint_as_float(r[2]) * il, __uint_as_float(r[3]) * il);
+              v0.z = t_pack(__uint_as_float(r[4]) * il, __uint_as_float(r[5]) * il);
+              v0.w = t_pack(__uint_as_float(r[6]) * il, __uint_as_float(r[7]) * il);
+              v1.x = t_pack(__uint_as_float(r[8]) * il, __uint_as_float(r[9]) * il);
+              v1.y = t_pack(__uint_as_float(r[10]) * il, __uint_as_float(r[11]) * il);
+              v1.z = t_pack(__uint_as_float(r[12]) * il, __uint_as_float(r[13]) * il);
+              v1.w = t_pack(__uint_as_float(r[14]) * il, __uint_as_float(r[15]) * il);
+              *reinterpret_cast<uint4 *>(orow + 16 * c) = v0;
+              *reinterpret_cast<uint4 *>(orow + 16 * c + 8) = v1;
+            }
+          }
+          t_fence_before();
+          __syncwarp();
+          if (lane == 0) t_arrive(ofree(x));
         }
         ++g;
       } while (!(flags & kLast));
     }
-    if (ok && ep && !epilogue()) ok = false;
-    if (!ok || *abort_flag) {   // a wait gave up: mark this CTA's rows as failed
+    if (!ok || *abort_flag) {   // a wait gave up: mark this group's rows as failed
       for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
-        const Item w = item_of(item, nq, Hq, pair);
+        const Item w = item_of(item, nq, Hkv, G, pair);
+        if (x == 1 && !w.two) continue;
         const int qi = pair ? w.row0 + (row & (kKB - 1)) : w.row0 + row;
         if (qi >= L) continue;
-        const int hrow = pair ? w.h + (row >> 6) : w.h;
+        const int hrow = pair ? (x ? w.h1 : w.h0) + (row >> 6) : (x ? w.h1 : w.h0);
         __nv_bfloat16 *orow = out + (static_cast<size_t>(hrow) * L + qi) * D + OH * hf;
         for (int c = 0; c < OH; ++c) orow[c] = __float2bfloat16_rn(NAN);
       }
@@ -686,7 +699,7 @@ int launch_prefill_tc(const pkv_bf16 *q, const pkv_bf16 *k, const pkv_bf16 *v,
   const int n = (L + kKB - 1) / kKB;
   const int G = Hq / Hkv;
   const bool pair = G % 2 == 0;
-  const long long items = pair ? 1LL * n * (Hq / 2) : 1LL * ((n + 1) / 2) * Hq;
+  const long long items = 1LL * (pair ? n : (n + 1) / 2) * items_per_tile(Hkv, G, pair);
   const long long cap = 1LL * TC<D>::CTAS_PER_SM * pkv::sm_count();
   const int grid = static_cast<int>(items < cap ? items : cap);
   PKV_CUDA_CHECK(pkv::launch_pdl(prefill_tc_kernel<D>, dim3(grid), dim3(kTCThreads), TC<D>::SMEM,

@@ -43,6 +43,18 @@ __device__ __forceinline__ bool t_wait(uint32_t bar, int k, volatile int *abort_
   *abort_flag = 1;
   return false;
 }
+// whether completion number k of the barrier's phases has happened (one
+// test, no wait)
+__device__ __forceinline__ bool t_test(uint32_t bar, int k) {
+  uint32_t done;
+  asm volatile(
+      "{\n.reg .pred q;\nmbarrier.test_wait.parity.shared::cta.b64 q, [%1], %2;\n"
+      "selp.u32 %0, 1, 0, q;\n}\n"
+      : "=r"(done)
+      : "r"(bar), "r"(static_cast<uint32_t>(k) & 1u)
+      : "memory");
+  return done != 0;
+}
 // the same, by every lane of a warp, with one result for the warp (so the
 // warp-collective TMEM accesses that follow are never reached by part of it)
 __device__ __forceinline__ bool t_wait_warp(uint32_t bar, int k, volatile int *abort_flag) {
