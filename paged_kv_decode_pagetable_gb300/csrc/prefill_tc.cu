@@ -563,23 +563,29 @@ __global__ void __launch_bounds__(kTCThreads, TC<D>::CTAS_PER_SM)
           t_fence_after();
           __nv_bfloat16 *orow =
               out + (static_cast<size_t>(hrow) * L + (valid ? qi : 0)) * D + OH * hf;
+          // this warp's O columns in two halves, each loaded with one wait
+          constexpr int EC = OH / 16 < 2 ? OH / 16 : 2;   // 16-column loads per wait
 #pragma unroll
-          for (int c = 0; c < OH / 16; ++c) {
-            uint32_t r[16];
-            t_ld16(trow + ocol + 16 * c, r);
+          for (int c0 = 0; c0 < OH / 16; c0 += EC) {
+            uint32_t r[EC][16];
+#pragma unroll
+            for (int e = 0; e < EC; ++e) t_ld16(trow + ocol + 16 * (c0 + e), r[e]);
             t_wait_ld();
             if (valid && write) {
-              uint4 v0, v1;
-              v0.x = t_pack(__uint_as_float(r[0]) * il, __uint_as_float(r[1]) * il);
-              v0.y = t_pack(__uint_as_float(r[2]) * il, __uint_as_float(r[3]) * il);
-              v0.z = t_pack(__uint_as_float(r[4]) * il, __uint_as_float(r[5]) * il);
-              v0.w = t_pack(__uint_as_float(r[6]) * il, __uint_as_float(r[7]) * il);
-              v1.x = t_pack(__uint_as_float(r[8]) * il, __uint_as_float(r[9]) * il);
-              v1.y = t_pack(__uint_as_float(r[10]) * il, __uint_as_float(r[11]) * il);
-              v1.z = t_pack(__uint_as_float(r[12]) * il, __uint_as_float(r[13]) * il);
-              v1.w = t_pack(__uint_as_float(r[14]) * il, __uint_as_float(r[15]) * il);
-              *reinterpret_cast<uint4 *>(orow + 16 * c) = v0;
-              *reinterpret_cast<uint4 *>(orow + 16 * c + 8) = v1;
+#pragma unroll
+              for (int e = 0; e < EC; ++e) {
+                uint4 v0, v1;
+                v0.x = t_pack(__uint_as_float(r[e][0]) * il, __uint_as_float(r[e][1]) * il);
+                v0.y = t_pack(__uint_as_float(r[e][2]) * il, __uint_as_float(r[e][3]) * il);
+                v0.z = t_pack(__uint_as_float(r[e][4]) * il, __uint_as_float(r[e][5]) * il);
+                v0.w = t_pack(__uint_as_float(r[e][6]) * il, __uint_as_float(r[e][7]) * il);
+                v1.x = t_pack(__uint_as_float(r[e][8]) * il, __uint_as_float(r[e][9]) * il);
+                v1.y = t_pack(__uint_as_float(r[e][10]) * il, __uint_as_float(r[e][11]) * il);
+                v1.z = t_pack(__uint_as_float(r[e][12]) * il, __uint_as_float(r[e][13]) * il);
+                v1.w = t_pack(__uint_as_float(r[e][14]) * il, __uint_as_float(r[e][15]) * il);
+                *reinterpret_cast<uint4 *>(orow + 16 * (c0 + e)) = v0;
+                *reinterpret_cast<uint4 *>(orow + 16 * (c0 + e) + 8) = v1;
+              }
             }
           }
           t_fence_before();
