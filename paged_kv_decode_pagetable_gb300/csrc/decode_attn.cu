@@ -687,9 +687,10 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
   // coherence).
   //
   // The set-up below (row cache, prefix sums, the producer's share of the
-  // cost line and its first unit's page entries) runs before the grid
-  // dependency wait and reads only seq_lens, batch_idx, the page table and
-  // shared memory. That is safe because the kernels that may still be
+  // cost line and its first unit's page entries; in the fused step the
+  // consumers' loads of the norm gains) runs before the grid dependency wait
+  // and reads only seq_lens, batch_idx, the page table, the gains and shared
+  // memory. That is safe because the kernels that may still be
   // running when this grid starts never write those: a kernel without
   // programmatic launch completes before its successor starts; the kernels
   // of this library release their dependents only after their own wait
@@ -765,11 +766,42 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
       locate_range(p, pre, prc, share_bound(itp.sh, c, cost), share_bound(itp.sh, c + 1, cost),
                    lane, itp);
     }
+    // fused step, consumers: the norm gains are loaded before the dependency
+    // wait (like the row metadata, no kernel that can still run writes them)
+    // and stored to shared memory after it and after the next grid's release
+    // (read after the first unit's barrier)
+    constexpr int GPT = (D + kCThreads - 1) / kCThreads;   // gain elements per thread
+    __nv_bfloat16 gqv[GPT], gkv[GPT];
+    if constexpr (STEP) {
+      if (warp < kCWarps && sa.gamma_q) {
+#pragma unroll
+        for (int e = 0; e < GPT; ++e) {
+          const int i = tid + e * kCThreads;
+          if (i < D) {
+            gqv[e] = sa.gamma_q[i];
+            gkv[e] = sa.gamma_k[i];
+          }
+        }
+      }
+    }
     // the consumer warps wait here; the producer warp also looks up its first
     // unit and that unit's pages first, and waits just before its first copy
     if (warp < kCWarps) {
       pkv_wait_prior_grid();
       pkv_allow_next_grid();
+    }
+    if constexpr (STEP) {
+      if (warp < kCWarps && sa.gamma_q) {
+        __nv_bfloat16 *gs = reinterpret_cast<__nv_bfloat16 *>(sm + Cf::OFF_GAM);
+#pragma unroll
+        for (int e = 0; e < GPT; ++e) {
+          const int i = tid + e * kCThreads;
+          if (i < D) {
+            gs[i] = gqv[e];
+            gs[D + i] = gkv[e];
+          }
+        }
+      }
     }
     if (parts_out && warp < kCWarps) {  // fixed mode: parts per (row, kv head) for the combine
       for (int rh = blockIdx.x + gridDim.x * tid; rh < p.B * p.Hkv; rh += gridDim.x * kCThreads) {
@@ -780,14 +812,6 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::CTAS_PER_SM)
   }
 
   if constexpr (STEP) {
-    // consumers: the norm gains (read after the first unit's barrier)
-    if (warp < kCWarps && sa.gamma_q) {
-      __nv_bfloat16 *gs = reinterpret_cast<__nv_bfloat16 *>(sm + Cf::OFF_GAM);
-      for (int i = tid; i < D; i += kCThreads) {
-        gs[i] = sa.gamma_q[i];
-        gs[D + i] = sa.gamma_k[i];
-      }
-    }
   }
 
   // rows with no key: zero output (rows spread over the CTAs); in the fused
