@@ -448,13 +448,29 @@ __global__ void __launch_bounds__(kTCThreads, TC<D>::CTAS_PER_SM)
         float alpha = 1.f;
         bool resc = false;
         if (need) {
+          // whether this warp's 32 keys belong to one document (lane l reads
+          // key j0 + l's; the whole warp votes, before any per-row branch)
+          static_assert(kKW == 32, "one key per lane for the document vote");
+          bool one_doc = false;
+          int d0 = 0;
+          if (partial && !(flags & kMaskAll)) {
+            const int dl = dks[lane];
+            d0 = __shfl_sync(0xffffffffu, dl, 0);
+            one_doc = __all_sync(0xffffffffu, dl == d0);
+          }
           if (flags & kMaskAll) {
 #pragma unroll
             for (int c = 0; c < kKW; ++c) sv[c] = -INFINITY;
-          } else if (partial && window == 0 && j0 + kKW <= w.row0 && valid) {
-            // keys all before the item's rows and inside L: the document test alone
+          } else if (partial && one_doc) {
+            // one document: the row keeps a contiguous range of these keys,
+            // [clo, chi] (causal, inside L, inside the window), or none
+            const int chi = min(qi, L - 1) - j0;
+            const int clo = (window > 0 ? qi - window + 1 : 0) - j0;
+            const bool any = valid && d0 == dq && chi >= clo;
+            const unsigned span = any ? static_cast<unsigned>(chi - clo) : 0u;
 #pragma unroll
-            for (int c = 0; c < kKW; ++c) sv[c] = dks[c] == dq ? sv[c] : -INFINITY;
+            for (int c = 0; c < kKW; ++c)
+              sv[c] = (any && static_cast<unsigned>(c - clo) <= span) ? sv[c] : -INFINITY;
           } else if (partial) {
 #pragma unroll
             for (int c = 0; c < kKW; ++c) {
