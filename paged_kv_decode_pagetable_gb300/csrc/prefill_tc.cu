@@ -42,6 +42,7 @@
 #include <mutex>
 
 #include "pkv_internal.h"
+#include "prefill_sched.cuh"
 #include "tcgen05.cuh"
 
 namespace {
@@ -85,7 +86,8 @@ struct TC {
   static constexpr int GB = 11;
   static constexpr int N_BAR = 2 + 2 * kNS + 1 + kGroups * GB;
   static constexpr int OFF_MISC = OFF_BAR + N_BAR * 8;       // tmem address, abort flag
-  static constexpr int SMEM = OFF_MISC + 16 + 1024;          // + slack to align to 1024
+  static constexpr int OFF_SCHED = OFF_MISC + 16;            // SchedSmem: this CTA's items
+  static constexpr int SMEM = OFF_SCHED + static_cast<int>(sizeof(SchedSmem)) + 1024;
   // per group: S[2] (2 x 64 columns) then O (D <= 128 columns)
   static constexpr int TMEM_COLS = 512, GROUP_COLS = 256, S_COL = 0, O_COL = 128;
   static constexpr int CTAS_PER_SM = 1;
@@ -206,13 +208,19 @@ __global__ void __launch_bounds__(kTCThreads, TC<D>::CTAS_PER_SM)
   const int Hkv = Hq / G;
   const int nq = pair ? nblk : (nblk + 1) / 2;   // row tiles of the items
   const int n_items = nq * items_per_tile(Hkv, G, pair);
+  SchedSmem &sched = *reinterpret_cast<SchedSmem *>(sm + C::OFF_SCHED);
+  if (warp == kProdWarp)
+    sched_build(sched, nq, items_per_tile(Hkv, G, pair), pair, nblk, kv_num, full_num);
+  __syncthreads();
+  const int n_mine = sched_count(sched, n_items);
 
   if (warp == kProdWarp) {
     // ============================ producer ============================
     if (lane == 0) {
       int g = 0, it = 0;
       bool ok = true;
-      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++it) {
+      for (; it < n_mine && ok; ++it) {
+        const int item = sched_item(sched, it);
         const Item w = item_of(item, nq, Hkv, G, pair);
         // both Q tiles of the item (the two groups'), each as two 64-row halves
         // (rows past L read zeros), once the previous item's last S is done
@@ -324,7 +332,7 @@ __global__ void __launch_bounds__(kTCThreads, TC<D>::CTAS_PER_SM)
       };
       bool pend = false;
       int pstage = 0, pflags = 0;
-      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++it) {
+      for (; it < n_mine && ok; ++it) {
         if (!t_wait(qfull, it, abort_flag)) break;
         int flags = 0;
         do {
@@ -401,7 +409,8 @@ __global__ void __launch_bounds__(kTCThreads, TC<D>::CTAS_PER_SM)
     const uint32_t ocol = C::O_COL + OH * hf;
     int g = 0;
     bool ok = true;
-    for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+    for (int it = 0; it < n_mine && ok; ++it) {
+      const int item = sched_item(sched, it);
       const Item w = item_of(item, nq, Hkv, G, pair);
       const int hx = x ? w.h1 : w.h0;
       const bool write = x == 0 || w.two;   // a repeated sub-item is not written
@@ -612,7 +621,8 @@ __global__ void __launch_bounds__(kTCThreads, TC<D>::CTAS_PER_SM)
       } while (!(flags & kLast));
     }
     if (!ok || *abort_flag) {   // a wait gave up: mark this group's rows as failed
-      for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+      for (int it = 0; it < n_mine; ++it) {
+        const int item = sched_item(sched, it);
         const Item w = item_of(item, nq, Hkv, G, pair);
         if (x == 1 && !w.two) continue;
         const int qi = pair ? w.row0 + (row & (kKB - 1)) : w.row0 + row;

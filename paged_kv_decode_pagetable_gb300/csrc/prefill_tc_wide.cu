@@ -33,6 +33,7 @@
 #include <mutex>
 
 #include "pkv_internal.h"
+#include "prefill_sched.cuh"
 #include "tcgen05.cuh"
 
 namespace {
@@ -71,7 +72,8 @@ struct TW {
   // pfull[2] pvdone[2] ofree drain xbar[4]
   static constexpr int N_BAR = 2 * wNSQ + 3 * wNSV + 8 + 2 + 4;
   static constexpr int OFF_MISC = OFF_BAR + N_BAR * 8;
-  static constexpr int SMEM = OFF_MISC + 16 + 1024;
+  static constexpr int OFF_SCHED = OFF_MISC + 16;   // SchedSmem: this CTA's items
+  static constexpr int SMEM = OFF_SCHED + static_cast<int>(sizeof(SchedSmem)) + 1024;
   static constexpr int TMEM_COLS = 512;   // S[2] (2 x 64) + O (256)
   static constexpr int S_COL = 0, O_COL = 128;
   static_assert(OFF_V % 1024 == 0 && OFF_P % 1024 == 0 && QK_STAGE % 1024 == 0, "atoms");
@@ -164,13 +166,19 @@ __global__ void __launch_bounds__(wThreads, 1)
   const bool pair = pair_heads != 0;
   const int nq = pair ? nblk : (nblk + 1) / 2;   // row tiles of the items
   const int n_items = nq * (pair ? Hq / 2 : Hq) * C::NOC;
+  SchedSmem &sched = *reinterpret_cast<SchedSmem *>(sm + C::OFF_SCHED);
+  if (warp == wProdWarp)
+    sched_build(sched, nq, (pair ? Hq / 2 : Hq) * C::NOC, pair, nblk, kv_num, full_num);
+  __syncthreads();
+  const int n_mine = sched_count(sched, n_items);
 
   if (warp == wProdWarp) {
     // ============================ producer ============================
     if (lane == 0) {
       int gq = 0, gv = 0;
       bool ok = true;
-      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+      for (int it = 0; it < n_mine && ok; ++it) {
+        const int item = sched_item(sched, it);
         const WItem w = witem_of(item, nq, Hq, C::NOC, pair);
         const int hk = w.h / G;   // = (h + 1) / G when paired
         // the union of the two halves' lists, ascending (paired: one list)
@@ -275,7 +283,7 @@ __global__ void __launch_bounds__(wThreads, 1)
         if (flags & wLast) ++pv_item;
         return true;
       };
-      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+      for (int it = 0; it < n_mine && ok; ++it) {
         int flags = 0;
         do {
           const int b = g & 1, sv = g % wNSV;
@@ -380,7 +388,8 @@ __global__ void __launch_bounds__(wThreads, 1)
     };
     int g = 0, it = -1;
     bool ok = true;
-    for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+    for (int wi = 0; wi < n_mine && ok; ++wi) {
+      const int item = sched_item(sched, wi);
       ++it;
       const WItem w = witem_of(item, nq, Hq, C::NOC, pair);
       const int qi = pair ? w.row0 + (row & (wKB - 1)) : w.row0 + row;
@@ -551,7 +560,8 @@ __global__ void __launch_bounds__(wThreads, 1)
     }
     if (ok && ep && !epilogue()) ok = false;
     if (!ok || *abort_flag) {   // a wait gave up: mark this CTA's rows as failed
-      for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+      for (int wi = 0; wi < n_mine; ++wi) {
+        const int item = sched_item(sched, wi);
         const WItem w = witem_of(item, nq, Hq, C::NOC, pair);
         const int qi = pair ? w.row0 + (row & (wKB - 1)) : w.row0 + row;
         if (qi >= L) continue;
