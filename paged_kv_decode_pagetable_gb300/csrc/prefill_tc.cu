@@ -586,32 +586,46 @@ __global__ void __launch_bounds__(kTCThreads, TC<D>::CTAS_PER_SM)
             break;
           }
           t_fence_after();
-          __nv_bfloat16 *orow =
-              out + (static_cast<size_t>(hrow) * L + (valid ? qi : 0)) * D + OH * hf;
-          // this warp's O columns in two halves, each loaded with one wait
-          constexpr int EC = OH / 16 < 2 ? OH / 16 : 2;   // 16-column loads per wait
+          // O / l as bf16, 32 columns per round, through this warp's 64
+          // bytes of each of its rows in the group's P buffer (idle until
+          // this warp writes its next P): each lane writes its row's chunks,
+          // then reads back so that four lanes store 64 contiguous bytes of
+          // one row (8 rows per store instead of 32)
+          static_assert(OH % 32 == 0, "32-column rounds");
+          uint8_t *pbuf = sm + C::OFF_P + x * C::P_BYTES;
+#pragma unroll 1
+          for (int c0 = 0; c0 < OH / 16; c0 += 2) {
 #pragma unroll
-          for (int c0 = 0; c0 < OH / 16; c0 += EC) {
-            uint32_t r[EC][16];
+            for (int h = 0; h < 2; ++h) {
+              uint32_t r[16];
+              t_ld16(trow + ocol + 16 * (c0 + h), r);
+              t_wait_ld();
 #pragma unroll
-            for (int e = 0; e < EC; ++e) t_ld16(trow + ocol + 16 * (c0 + e), r[e]);
-            t_wait_ld();
-            if (valid && write) {
-#pragma unroll
-              for (int e = 0; e < EC; ++e) {
-                uint4 v0, v1;
-                v0.x = t_pack(__uint_as_float(r[e][0]) * il, __uint_as_float(r[e][1]) * il);
-                v0.y = t_pack(__uint_as_float(r[e][2]) * il, __uint_as_float(r[e][3]) * il);
-                v0.z = t_pack(__uint_as_float(r[e][4]) * il, __uint_as_float(r[e][5]) * il);
-                v0.w = t_pack(__uint_as_float(r[e][6]) * il, __uint_as_float(r[e][7]) * il);
-                v1.x = t_pack(__uint_as_float(r[e][8]) * il, __uint_as_float(r[e][9]) * il);
-                v1.y = t_pack(__uint_as_float(r[e][10]) * il, __uint_as_float(r[e][11]) * il);
-                v1.z = t_pack(__uint_as_float(r[e][12]) * il, __uint_as_float(r[e][13]) * il);
-                v1.w = t_pack(__uint_as_float(r[e][14]) * il, __uint_as_float(r[e][15]) * il);
-                *reinterpret_cast<uint4 *>(orow + 16 * (c0 + e)) = v0;
-                *reinterpret_cast<uint4 *>(orow + 16 * (c0 + e) + 8) = v1;
+              for (int jj = 0; jj < 2; ++jj) {
+                const uint32_t *e = r + 8 * jj;
+                uint4 v;
+                v.x = t_pack(__uint_as_float(e[0]) * il, __uint_as_float(e[1]) * il);
+                v.y = t_pack(__uint_as_float(e[2]) * il, __uint_as_float(e[3]) * il);
+                v.z = t_pack(__uint_as_float(e[4]) * il, __uint_as_float(e[5]) * il);
+                v.w = t_pack(__uint_as_float(e[6]) * il, __uint_as_float(e[7]) * il);
+                const int j = 2 * h + jj;
+                *reinterpret_cast<uint4 *>(pbuf + row * 128 + (((4 * hf + j) ^ (row & 7)) << 4)) = v;
               }
             }
+            __syncwarp();
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int rr = 32 * lg + 8 * i + (lane >> 2), j = lane & 3;
+              const uint4 v = *reinterpret_cast<const uint4 *>(
+                  pbuf + rr * 128 + (((4 * hf + j) ^ (rr & 7)) << 4));
+              const int qr = __shfl_sync(0xffffffffu, qi, 8 * i + (lane >> 2));   // row rr's
+              const int hr = __shfl_sync(0xffffffffu, hrow, 8 * i + (lane >> 2));
+              if (write && qr < L) {
+                *reinterpret_cast<uint4 *>(out + (static_cast<size_t>(hr) * L + qr) * D + OH * hf +
+                                           16 * c0 + 8 * j) = v;
+              }
+            }
+            __syncwarp();
           }
           t_fence_before();
           __syncwarp();
