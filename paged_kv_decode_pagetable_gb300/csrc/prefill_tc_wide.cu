@@ -356,28 +356,41 @@ __global__ void __launch_bounds__(wThreads, 1)
     auto epilogue = [&]() -> bool {
       if (!t_wait_warp(pvdone + 8 * (ep_g & 1), ep_g >> 1, abort_flag)) return false;
       t_fence_after();
-      const bool valid = ep_qi < L;
-      __nv_bfloat16 *orow = out + (static_cast<size_t>(ep_h) * L + (valid ? ep_qi : 0)) * D +
-                            ep_oc * wDO + OH * hf;
+      // O / l as bf16, 16 columns per round, through this warp's 32 bytes
+      // of each of its rows in the idle P buffer (the previous item's last
+      // tile's, whose P V is done): each lane writes its row's two chunks,
+      // then two lanes store 32 contiguous bytes of one row (16 rows per
+      // store instead of 32)
+      uint8_t *pbuf = sm + C::OFF_P + (ep_g & 1) * C::P_BYTES;
       const float il = ep_il;
-#pragma unroll
+#pragma unroll 1
       for (int c = 0; c < OH / 16; ++c) {
         uint32_t r[16];
         t_ld16(trow + ocol + 16 * c, r);
         t_wait_ld();
-        if (valid) {
-          uint4 v0, v1;
-          v0.x = t_pack(__uint_as_float(r[0]) * il, __uint_as_float(r[1]) * il);
-          v0.y = t_pack(__uint_as_float(r[2]) * il, __uint_as_float(r[3]) * il);
-          v0.z = t_pack(__uint_as_float(r[4]) * il, __uint_as_float(r[5]) * il);
-          v0.w = t_pack(__uint_as_float(r[6]) * il, __uint_as_float(r[7]) * il);
-          v1.x = t_pack(__uint_as_float(r[8]) * il, __uint_as_float(r[9]) * il);
-          v1.y = t_pack(__uint_as_float(r[10]) * il, __uint_as_float(r[11]) * il);
-          v1.z = t_pack(__uint_as_float(r[12]) * il, __uint_as_float(r[13]) * il);
-          v1.w = t_pack(__uint_as_float(r[14]) * il, __uint_as_float(r[15]) * il);
-          *reinterpret_cast<uint4 *>(orow + 16 * c) = v0;
-          *reinterpret_cast<uint4 *>(orow + 16 * c + 8) = v1;
+#pragma unroll
+        for (int jj = 0; jj < 2; ++jj) {
+          const uint32_t *e = r + 8 * jj;
+          uint4 v;
+          v.x = t_pack(__uint_as_float(e[0]) * il, __uint_as_float(e[1]) * il);
+          v.y = t_pack(__uint_as_float(e[2]) * il, __uint_as_float(e[3]) * il);
+          v.z = t_pack(__uint_as_float(e[4]) * il, __uint_as_float(e[5]) * il);
+          v.w = t_pack(__uint_as_float(e[6]) * il, __uint_as_float(e[7]) * il);
+          *reinterpret_cast<uint4 *>(pbuf + row * 128 + (((2 * hf + jj) ^ (row & 7)) << 4)) = v;
         }
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const int src = 16 * i + (lane >> 1), jj = lane & 1, rr = 32 * lg + src;
+          const uint4 v =
+              *reinterpret_cast<const uint4 *>(pbuf + rr * 128 + (((2 * hf + jj) ^ (rr & 7)) << 4));
+          const int qr = __shfl_sync(0xffffffffu, ep_qi, src);   // row rr's
+          const int hr = __shfl_sync(0xffffffffu, ep_h, src);
+          if (qr < L)
+            *reinterpret_cast<uint4 *>(out + (static_cast<size_t>(hr) * L + qr) * D + ep_oc * wDO +
+                                       OH * hf + 16 * c + 8 * jj) = v;
+        }
+        __syncwarp();
       }
       t_fence_before();
       __syncwarp();
