@@ -144,10 +144,12 @@ def measured_peaks():
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
 
 
-def profile_traffic(kernel_key: str, mean_alg_bytes: float):
-    """DRAM bytes per launch from a committed ncu capture (the captured
-    launches' measured/algorithmic ratio scaled to this run's mean launch),
-    or None when the kernel source changed since the capture."""
+def profile_traffic(kernel_key: str, mean_alg_bytes: float | None = None):
+    """DRAM bytes per launch from a committed ncu capture, or None when the
+    kernel source changed since the capture. A record with a measured /
+    algorithmic ratio is scaled to this run's mean launch (decode: the bytes
+    vary from step to step); one with bytes per launch is a capture of the
+    same fixed workload."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
@@ -156,12 +158,15 @@ def profile_traffic(kernel_key: str, mean_alg_bytes: float):
         return None
     if not rec:
         return None
-    src = os.path.join(ROOT, "paged_kv_decode_pagetable_gb300", "csrc", "decode_attn.cu")
+    src = os.path.join(ROOT, "paged_kv_decode_pagetable_gb300", "csrc",
+                       rec.get("source_file", "decode_attn.cu"))
     with open(src, "rb") as f:
         digest = hashlib.sha256(f.read()).hexdigest()[:16]
     if rec.get("source_sha256_16") != digest:
         return None
-    return float(rec["dram_over_algorithmic"]) * mean_alg_bytes
+    if "dram_over_algorithmic" in rec and mean_alg_bytes is not None:
+        return float(rec["dram_over_algorithmic"]) * mean_alg_bytes
+    return float(rec["dram_bytes_per_launch"]) if "dram_bytes_per_launch" in rec else None
 
 
 class ClockSampler:
@@ -915,7 +920,7 @@ def run_prefill(args, world, rank, local):
                          "unit": "TFLOP/s", "frac": achieved / peak, "peak_kind": peak_kind,
                          "kernel": (f"prefill_tc_kernel<{D}>" if D <= 128
                                     else f"prefill_wide_kernel<{D}>") + " (tcgen05)",
-                         "traffic": None},
+                         "traffic": profile_traffic(f"{args.workload}_prefill_{D}")},
             "cpu_baseline": cpu, "gpu_launches": K, "clocks": clocks}), flush=True)
 
 
