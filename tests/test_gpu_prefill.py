@@ -287,3 +287,48 @@ def test_prefill_gemma_layers_sampled_documents(dev, D, window):
         ref = oracle.prefill_attention(q[:, sl].double().numpy(), k[:, sl].double().numpy(),
                                        v[:, sl].double().numpy(), docs[sl], scale, window=window)
         _compare(got[:, sl], ref, v, _kept(docs[sl], window))
+
+
+def test_prefill_more_items_than_the_sorted_schedule_holds(dev):
+    """A launch with more work items per CTA than the cost-sorted schedule's
+    list holds (256), so every CTA walks its items round-robin instead:
+    40,000 packed tokens of U[100, 400]-token documents, 128 q / 64 kv heads
+    (one query block of two heads per item, 64 items per row tile, 40,000
+    items), head_dim 64. Inputs are drawn on the GPU from a seeded generator;
+    sampled rows of every head are compared with the oracle's single-query
+    attention over the row's kept keys."""
+    from oracle.attention import decode_attention_row
+    rng = np.random.default_rng(80)
+    lens = wl.uniform_lengths(rng, 200, 100, 400)
+    docs = np.repeat(np.arange(len(lens)), lens)[:40000].astype(np.int32)
+    L, Hq, Hkv, D = len(docs), 128, 64, 64
+    assert L == 40000 and ((L + 63) // 64) * Hkv > 256 * torch.cuda.get_device_properties(
+        dev).multi_processor_count
+    g = torch.Generator(device=dev)
+    g.manual_seed(81)
+    q, k, v = (torch.randn((h, L, D), generator=g, device=dev).to(torch.bfloat16)
+               for h in (Hq, Hkv, Hkv))
+    scale = D ** -0.5
+    bm = pkv.prefill_block_mask(torch.from_numpy(docs).to(dev), 0)
+    out = torch.full((Hq, L, D), float("nan"), dtype=torch.bfloat16, device=dev)
+    pkv.prefill_attn(q, k, v, bm, scale, out)
+    torch.cuda.synchronize()
+    starts = np.r_[0, np.flatnonzero(np.diff(docs)) + 1]
+    rows = np.r_[0, 63, 64, 20000, 39999, rng.integers(1, L - 1, size=11)]
+    G = Hq // Hkv
+    errs, kept = [], []
+    for i in rows:
+        j0 = int(starts[np.searchsorted(starts, i, side="right") - 1])
+        js = slice(j0, int(i) + 1)
+        qd = q[:, i].double().cpu().numpy()
+        kd, vd = k[:, js].double().cpu().numpy(), v[:, js].double().cpu().numpy()
+        ref = np.stack([decode_attention_row(qd[h], kd[h // G], vd[h // G], scale)[0]
+                        for h in range(Hq)])
+        got = out[:, i].double().cpu().numpy()
+        assert np.isfinite(got).all()
+        errs.append(np.abs(got - ref))
+        kept.append(int(i) + 1 - j0)
+    e = np.stack(errs, axis=1)
+    long_rows = np.array(kept) >= 16
+    assert e[:, long_rows].max() <= 1e-2, float(e[:, long_rows].max())
+    assert e.mean() <= 1e-3, float(e.mean())
