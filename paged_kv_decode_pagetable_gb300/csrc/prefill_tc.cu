@@ -489,17 +489,18 @@ __global__ void __launch_bounds__(kTCThreads, TC<D>::CTAS_PER_SM)
               sv[c] = keep ? sv[c] : -INFINITY;
             }
           }
-          // raw-score maximum of this warp's keys (four chains), then of the row
-          float x0 = sv[0], x1 = sv[1], x2 = sv[2], x3 = sv[3];
+          // raw-score maximum of this warp's keys (two chains of three-input
+          // maxima), then of the row
+          static_assert(kKW % 4 == 0 && kKW >= 8, "max chains");
+          float x0 = t_max3(sv[0], sv[1], sv[2]), x1 = t_max3(sv[3], sv[4], sv[5]);
 #pragma unroll
-          for (int c = 4; c < kKW; c += 4) {
-            x0 = fmaxf(x0, sv[c]);
-            x1 = fmaxf(x1, sv[c + 1]);
-            x2 = fmaxf(x2, sv[c + 2]);
-            x3 = fmaxf(x3, sv[c + 3]);
+          for (int c = 6; c + 3 < kKW; c += 4) {
+            x0 = t_max3(x0, sv[c], sv[c + 1]);
+            x1 = t_max3(x1, sv[c + 2], sv[c + 3]);
           }
+          x0 = t_max3(x0, sv[kKW - 2], sv[kKW - 1]);
           float mall[kSplit];
-          if (!exchange(fmaxf(fmaxf(x0, x1), fmaxf(x2, x3)), mall)) {
+          if (!exchange(fmaxf(x0, x1), mall)) {
             ok = false;
             break;
           }
@@ -520,17 +521,20 @@ __global__ void __launch_bounds__(kTCThreads, TC<D>::CTAS_PER_SM)
             }
           }
           const float mneg = m == -INFINITY ? 0.f : -m;
+          // masked scores are -inf: exp2 gives 0 (the scale and the sums two
+          // lanes per packed instruction, each rounded as the scalar form)
           float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
 #pragma unroll
-          for (int c = 0; c < kKW; c += 4) {   // masked scores are -inf: exp2 gives 0
-            sv[c] = t_ex2(fmaf(sv[c], scale_log2, mneg));
-            sv[c + 1] = t_ex2(fmaf(sv[c + 1], scale_log2, mneg));
-            sv[c + 2] = t_ex2(fmaf(sv[c + 2], scale_log2, mneg));
-            sv[c + 3] = t_ex2(fmaf(sv[c + 3], scale_log2, mneg));
-            s0 += sv[c];
-            s1 += sv[c + 1];
-            s2 += sv[c + 2];
-            s3 += sv[c + 3];
+          for (int c = 0; c < kKW; c += 4) {
+            float y0, y1, y2, y3;
+            t_fma2(y0, y1, sv[c], sv[c + 1], scale_log2, mneg);
+            t_fma2(y2, y3, sv[c + 2], sv[c + 3], scale_log2, mneg);
+            sv[c] = t_ex2(y0);
+            sv[c + 1] = t_ex2(y1);
+            sv[c + 2] = t_ex2(y2);
+            sv[c + 3] = t_ex2(y3);
+            t_add2(s0, s1, sv[c], sv[c + 1]);
+            t_add2(s2, s3, sv[c + 2], sv[c + 3]);
           }
           l = l * alpha + ((s0 + s1) + (s2 + s3));
         }

@@ -145,6 +145,26 @@ __device__ __forceinline__ void t_wait_st() {
 }
 // 2^x on the MUFU unit (the PTX approximate instruction, subnormal results
 // flushed to zero: they are below what the bf16 P can hold anyway)
+// max of three (one instruction on sm_100 and later)
+__device__ __forceinline__ float t_max3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+// (d0, d1) = (a0, a1) * b + c, one packed instruction, each lane rounded as fmaf
+__device__ __forceinline__ void t_fma2(float &d0, float &d1, float a0, float a1, float b, float c) {
+  asm("{\n.reg .b64 ra, rb, rc, rd;\nmov.b64 ra, {%2, %3};\nmov.b64 rb, {%4, %4};\n"
+      "mov.b64 rc, {%5, %5};\nfma.rn.f32x2 rd, ra, rb, rc;\nmov.b64 {%0, %1}, rd;\n}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b), "f"(c));
+}
+// (s0, s1) += (a0, a1), one packed instruction
+__device__ __forceinline__ void t_add2(float &s0, float &s1, float a0, float a1) {
+  asm("{\n.reg .b64 rs, ra;\nmov.b64 rs, {%0, %1};\nmov.b64 ra, {%2, %3};\n"
+      "add.rn.f32x2 rs, rs, ra;\nmov.b64 {%0, %1}, rs;\n}"
+      : "+f"(s0), "+f"(s1)
+      : "f"(a0), "f"(a1));
+}
 __device__ __forceinline__ float t_ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
