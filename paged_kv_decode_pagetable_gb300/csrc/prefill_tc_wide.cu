@@ -466,16 +466,17 @@ __global__ void __launch_bounds__(wThreads, 1)
               svv[c] = keep ? svv[c] : -INFINITY;
             }
           }
-          float x0 = svv[0], x1 = svv[1], x2 = svv[2], x3 = svv[3];
+          // two chains of three-input maxima
+          static_assert(wKW % 4 == 0 && wKW >= 8, "max chains");
+          float x0 = t_max3(svv[0], svv[1], svv[2]), x1 = t_max3(svv[3], svv[4], svv[5]);
 #pragma unroll
-          for (int c = 4; c < wKW; c += 4) {
-            x0 = fmaxf(x0, svv[c]);
-            x1 = fmaxf(x1, svv[c + 1]);
-            x2 = fmaxf(x2, svv[c + 2]);
-            x3 = fmaxf(x3, svv[c + 3]);
+          for (int c = 6; c + 3 < wKW; c += 4) {
+            x0 = t_max3(x0, svv[c], svv[c + 1]);
+            x1 = t_max3(x1, svv[c + 2], svv[c + 3]);
           }
+          x0 = t_max3(x0, svv[wKW - 2], svv[wKW - 1]);
           float mall[wSplit];
-          if (!exchange(fmaxf(fmaxf(x0, x1), fmaxf(x2, x3)), mall)) {
+          if (!exchange(fmaxf(x0, x1), mall)) {
             ok = false;
             break;
           }
@@ -497,15 +498,16 @@ __global__ void __launch_bounds__(wThreads, 1)
           const float mneg = m == -INFINITY ? 0.f : -m;
           float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
 #pragma unroll
-          for (int c = 0; c < wKW; c += 4) {
-            svv[c] = t_ex2(fmaf(svv[c], scale_log2, mneg));
-            svv[c + 1] = t_ex2(fmaf(svv[c + 1], scale_log2, mneg));
-            svv[c + 2] = t_ex2(fmaf(svv[c + 2], scale_log2, mneg));
-            svv[c + 3] = t_ex2(fmaf(svv[c + 3], scale_log2, mneg));
-            s0 += svv[c];
-            s1 += svv[c + 1];
-            s2 += svv[c + 2];
-            s3 += svv[c + 3];
+          for (int c = 0; c < wKW; c += 4) {   // packed scale and sums, as in prefill_tc.cu
+            float y0, y1, y2, y3;
+            t_fma2(y0, y1, svv[c], svv[c + 1], scale_log2, mneg);
+            t_fma2(y2, y3, svv[c + 2], svv[c + 3], scale_log2, mneg);
+            svv[c] = t_ex2(y0);
+            svv[c + 1] = t_ex2(y1);
+            svv[c + 2] = t_ex2(y2);
+            svv[c + 3] = t_ex2(y3);
+            t_add2(s0, s1, svv[c], svv[c + 1]);
+            t_add2(s2, s3, svv[c + 2], svv[c + 3]);
           }
           l = l * alpha + ((s0 + s1) + (s2 + s3));
           if (__any_sync(0xffffffffu, resc)) {   // this warp's columns of O *= alpha
