@@ -460,7 +460,7 @@ __global__ void __launch_bounds__(kTCThreads, TC<D>::CTAS_PER_SM)
           // whether this warp's 32 keys belong to one document (lane l reads
           // key j0 + l's; the whole warp votes, before any per-row branch)
           static_assert(kKW == 32, "one key per lane for the document vote");
-          bool one_doc = false;
+          bool one_doc = false, any_kept = true;
           int d0 = 0;
           if (partial && !(flags & kMaskAll)) {
             const int dl = dks[lane];
@@ -472,14 +472,21 @@ __global__ void __launch_bounds__(kTCThreads, TC<D>::CTAS_PER_SM)
             for (int c = 0; c < kKW; ++c) sv[c] = -INFINITY;
           } else if (partial && one_doc) {
             // one document: the row keeps a contiguous range of these keys,
-            // [clo, chi] (causal, inside L, inside the window), or none
-            const int chi = min(qi, L - 1) - j0;
-            const int clo = (window > 0 ? qi - window + 1 : 0) - j0;
-            const bool any = valid && d0 == dq && chi >= clo;
-            const unsigned span = any ? static_cast<unsigned>(chi - clo) : 0u;
+            // [lo, hi] (causal, inside L, inside the window), or none. On the
+            // FMA pipe: key c is outside iff |c - mid| - half >= 1, so the
+            // saturated difference is exactly 1 there and 0 inside, and the
+            // score moves down by 2^100 (its exponential is 0 as for -inf; a
+            // warp that keeps nothing reports -inf as its maximum, below)
+            const int lo = max((window > 0 ? qi - window + 1 : 0) - j0, 0);
+            const int hi = min(min(qi, L - 1) - j0, kKW - 1);
+            any_kept = valid && d0 == dq && lo <= hi;
+            const float mid = any_kept ? 0.5f * static_cast<float>(lo + hi) : -256.f;
+            const float half = any_kept ? 0.5f * static_cast<float>(hi - lo) : 0.f;
 #pragma unroll
-            for (int c = 0; c < kKW; ++c)
-              sv[c] = (any && static_cast<unsigned>(c - clo) <= span) ? sv[c] : -INFINITY;
+            for (int c = 0; c < kKW; ++c) {
+              const float outside = __saturatef(fabsf(static_cast<float>(c) - mid) - half);
+              sv[c] = fmaf(outside, -0x1p100f, sv[c]);
+            }
           } else if (partial) {
 #pragma unroll
             for (int c = 0; c < kKW; ++c) {
@@ -500,7 +507,7 @@ __global__ void __launch_bounds__(kTCThreads, TC<D>::CTAS_PER_SM)
           }
           x0 = t_max3(x0, sv[kKW - 2], sv[kKW - 1]);
           float mall[kSplit];
-          if (!exchange(fmaxf(x0, x1), mall)) {
+          if (!exchange(any_kept ? fmaxf(x0, x1) : -INFINITY, mall)) {
             ok = false;
             break;
           }
