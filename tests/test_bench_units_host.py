@@ -79,3 +79,34 @@ def test_prefill_flops_with_a_window_equal_kept_pairs_of_the_mask():
     for window in (1, 8, 31, 64):
         kept = int(oracle.keep_matrix(docs, window).sum())
         assert bench.prefill_flops(lens, 8, 256, window) == 4.0 * 256 * 8 * kept, window
+
+
+def test_traffic_records_follow_the_kernel_source(tmp_path, monkeypatch):
+    # a record is used only while the hash of the kernel source it names
+    # matches; a ratio record scales to the run's mean launch, a bytes record
+    # (a fixed workload) is returned as is
+    import hashlib
+    import json
+    csrc = tmp_path / "paged_kv_decode_pagetable_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    (tmp_path / "profiles").mkdir()
+    (csrc / "decode_attn.cu").write_bytes(b"decode source")
+    (csrc / "prefill_tc.cu").write_bytes(b"prefill source")
+    h = {n: hashlib.sha256(n.encode()).hexdigest()[:16]
+         for n in ("decode source", "prefill source")}
+    recs = {"a_decode_attn_128": {"source_sha256_16": h["decode source"],
+                                  "dram_over_algorithmic": 1.5},
+            "b_prefill_128": {"source_file": "prefill_tc.cu",
+                              "source_sha256_16": h["prefill source"],
+                              "dram_bytes_per_launch": 1e6},
+            "c_prefill_128": {"source_file": "prefill_tc.cu",
+                              "source_sha256_16": h["decode source"],
+                              "dram_bytes_per_launch": 1e6}}
+    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps(recs))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.profile_traffic("a_decode_attn_128", 2e6) == 3e6
+    assert bench.profile_traffic("b_prefill_128") == 1e6
+    assert bench.profile_traffic("c_prefill_128") is None      # source changed
+    assert bench.profile_traffic("missing") is None
+    (csrc / "decode_attn.cu").write_bytes(b"decode source, edited")
+    assert bench.profile_traffic("a_decode_attn_128", 2e6) is None
