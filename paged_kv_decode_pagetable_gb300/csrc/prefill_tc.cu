@@ -18,11 +18,13 @@
 //     and its 64 document ids by TMA into a 3-stage ring, with a small
 //     descriptor (block; full / first / last flags; which query block lists
 //     it) in the stage.
-//   warp 17 (MMA, one lane): per tile, S = Q K^T for both groups into their
-//     own TMEM S buffers (two each; M = 128, N = 64, K-major SW128 operands),
-//     then, one tile behind (at once for an item's last tile), O += P V for
-//     both groups into their TMEM O (P K-major from the group's shared
-//     buffer, V MN-major).
+//   warps 17, 18 (MMA, one lane each, one warp per softmax group): per tile,
+//     the group's S = Q K^T into its own TMEM S buffers (two; M = 128, N =
+//     64, K-major SW128 operands), then, one tile behind (at once for an
+//     item's last tile), its O += P V (P K-major from the group's shared
+//     buffer, V MN-major). The groups share the K / V tiles (a ring stage is
+//     free once both groups' P V of it is done) but neither group's MMAs wait
+//     for the other group's softmax.
 //   warps 0-7 / 8-15 (softmax groups 0 / 1): warps w and w + 4 of a group
 //     share the 32 query rows of TMEM lanes 32(w%4)..32(w%4)+31, one row per
 //     thread, and split the 64 keys of a tile and the D columns of O in
@@ -55,8 +57,8 @@ constexpr int kSplit = 2;                         // warps of a group per TMEM l
 constexpr int kGroupWarps = 4 * kSplit;           // each: 32 rows x 32 keys of a tile
 constexpr int kSoftWarps = kGroups * kGroupWarps;
 constexpr int kKW = 64 / kSplit;                  // keys per softmax warp
-constexpr int kProdWarp = kSoftWarps, kMmaWarp = kSoftWarps + 1;
-constexpr int kTCThreads = (kSoftWarps + 2) * 32;
+constexpr int kProdWarp = kSoftWarps, kMmaWarp = kSoftWarps + 1;   // MMA: one warp per group
+constexpr int kTCThreads = (kSoftWarps + 1 + kGroups) * 32;
 constexpr float kLazyLog2 = 8.f;   // rescale O only when a row maximum grows past 2^8
 
 // tile descriptor flags; kNeed0 / kNeed1: the block is listed for the
@@ -80,11 +82,11 @@ struct TC {
   static constexpr int OFF_XCH = OFF_SD + kNS * kKB * 4;      // float [kGroups][2][kSplit][128]
   static constexpr int OFF_META = OFF_XCH + kGroups * 2 * kSplit * kQR * 4;  // int4 [kNS]
   static constexpr int OFF_BAR = OFF_META + kNS * 16;
-  // shared: qfull, qempty, kvfull[NS], kvempty[NS], drain; per group:
+  // shared: qfull, qempty, kvfull[NS], kvempty[NS], drain[kGroups]; per group:
   // sfull[2], sfree[2], pfull, pvdone, ofree (per item, so that no waiter
   // can fall two phases behind), xbar[4] (the lane groups' exchanges)
   static constexpr int GB = 11;
-  static constexpr int N_BAR = 2 + 2 * kNS + 1 + kGroups * GB;
+  static constexpr int N_BAR = 2 + 2 * kNS + kGroups + kGroups * GB;
   static constexpr int OFF_MISC = OFF_BAR + N_BAR * 8;       // tmem address, abort flag
   static constexpr int OFF_SCHED = OFF_MISC + 16;            // SchedSmem: this CTA's items
   static constexpr int SMEM = OFF_SCHED + static_cast<int>(sizeof(SchedSmem)) + 1024;
@@ -159,7 +161,8 @@ __global__ void __launch_bounds__(kTCThreads, TC<D>::CTAS_PER_SM)
   int4 *meta = reinterpret_cast<int4 *>(sm + C::OFF_META);
   const uint32_t bar0 = t_smem(sm + C::OFF_BAR);
   const uint32_t qfull = bar0, qempty = bar0 + 8, kvfull = bar0 + 16,
-                 kvempty = kvfull + 8 * kNS, drain = kvempty + 8 * kNS, gbar0 = drain + 8;
+                 kvempty = kvfull + 8 * kNS, drain = kvempty + 8 * kNS,
+                 gbar0 = drain + 8 * kGroups;
   // the barriers of group x
   auto sfull = [&](int x, int b) { return gbar0 + 8 * C::GB * x + 8 * b; };
   auto sfree = [&](int x, int b) { return gbar0 + 8 * C::GB * x + 16 + 8 * b; };
@@ -172,12 +175,12 @@ __global__ void __launch_bounds__(kTCThreads, TC<D>::CTAS_PER_SM)
 
   if (tid == 0) {
     t_bar_init(qfull, 1);
-    t_bar_init(qempty, 1);
+    t_bar_init(qempty, kGroups);   // each group's MMA warp, after the item's last S
     for (int i = 0; i < kNS; ++i) {
       t_bar_init(kvfull + 8 * i, 1);
-      t_bar_init(kvempty + 8 * i, 1);
+      t_bar_init(kvempty + 8 * i, kGroups);   // each group's P V of the tile
     }
-    t_bar_init(drain, 1);
+    for (int x = 0; x < kGroups; ++x) t_bar_init(drain + 8 * x, 1);
     for (int x = 0; x < kGroups; ++x) {
       for (int b = 0; b < 2; ++b) {
         t_bar_init(sfull(x, b), 1);
@@ -300,31 +303,33 @@ __global__ void __launch_bounds__(kTCThreads, TC<D>::CTAS_PER_SM)
         ok = emit(pend, pend_flags | kLast | (emitted == 0 ? kFirst : 0));
       }
     }
-  } else if (warp == kMmaWarp) {
+  } else if (warp >= kMmaWarp) {
     // ============================== MMA ===============================
+    // one warp per softmax group (one lane issues): the group's S of every
+    // tile and, one tile behind, its P V; the two groups share the tiles
+    // but neither waits for the other's P
+    const int x = warp - kMmaWarp;
     if (lane == 0) {
       constexpr uint32_t idS = t_idesc(kKB, 0), idO = t_idesc(D, 1);
       int g = 0, it = 0, npv = 0, nfirst = 0;
       bool ok = true;
-      // P V of the tile in stage sp for both groups into their O; an item's
-      // first one overwrites O, once the epilogue of the group's previous
-      // item has read it
+      const uint32_t sQx = sQ + x * C::Q_BYTES;
+      const uint32_t scol = C::GROUP_COLS * x + C::S_COL, ocol = C::GROUP_COLS * x + C::O_COL;
+      // P V of the tile in stage sp into the group's O; an item's first one
+      // overwrites O, once the epilogue of the group's previous item has
+      // read it
       auto do_pv = [&](int sp, int flags) -> bool {
+        if (!t_wait(pfull(x), npv, abort_flag)) return false;
+        if ((flags & kFirst) && nfirst >= 1 && !t_wait(ofree(x), nfirst - 1, abort_flag))
+          return false;
+        t_fence_after();
 #pragma unroll
-        for (int x = 0; x < kGroups; ++x) {
-          if (!t_wait(pfull(x), npv, abort_flag)) return false;
-          if ((flags & kFirst) && nfirst >= 1 && !t_wait(ofree(x), nfirst - 1, abort_flag))
-            return false;
-          t_fence_after();
-          const uint32_t ocol = C::GROUP_COLS * x + C::O_COL;
-#pragma unroll
-          for (int k = 0; k < kKB / 16; ++k) {
-            const uint64_t a = t_desc(sP + x * C::P_BYTES + k * 32, 16, 1024);
-            const uint64_t b = t_desc(sV + sp * C::KV_BYTES + k * 2048, C::KV_ATOM, 1024);
-            t_mma(tmem + ocol, a, b, idO, (k > 0 || !(flags & kFirst)) ? 1u : 0u);
-          }
-          t_commit(pvdone(x));
+        for (int k = 0; k < kKB / 16; ++k) {
+          const uint64_t a = t_desc(sP + x * C::P_BYTES + k * 32, 16, 1024);
+          const uint64_t b = t_desc(sV + sp * C::KV_BYTES + k * 2048, C::KV_ATOM, 1024);
+          t_mma(tmem + ocol, a, b, idO, (k > 0 || !(flags & kFirst)) ? 1u : 0u);
         }
+        t_commit(pvdone(x));
         t_commit(kvempty + 8 * sp);
         ++npv;
         if (flags & kFirst) ++nfirst;
@@ -342,27 +347,23 @@ __global__ void __launch_bounds__(kTCThreads, TC<D>::CTAS_PER_SM)
             break;
           }
           flags = meta[s].y;
-#pragma unroll
-          for (int x = 0; x < kGroups; ++x)
-            if (g >= 2 && !t_wait(sfree(x, b), (g >> 1) - 1, abort_flag)) ok = false;
-          if (!ok) break;
+          if (g >= 2 && !t_wait(sfree(x, b), (g >> 1) - 1, abort_flag)) {
+            ok = false;
+            break;
+          }
           t_fence_after();
 #pragma unroll
-          for (int x = 0; x < kGroups; ++x) {
-            const uint32_t sQi = sQ + x * C::Q_BYTES;
-#pragma unroll
-            for (int k = 0; k < D / 16; ++k) {
-              const uint64_t a = t_desc(sQi + (k >> 2) * C::Q_ATOM + (k & 3) * 32, 16, 1024);
-              const uint64_t bd =
-                  t_desc(sK + s * C::KV_BYTES + (k >> 2) * C::KV_ATOM + (k & 3) * 32, 16, 1024);
-              t_mma(tmem + C::GROUP_COLS * x + C::S_COL + b * kKB, a, bd, idS, k > 0 ? 1u : 0u);
-            }
-            t_commit(sfull(x, b));
+          for (int k = 0; k < D / 16; ++k) {
+            const uint64_t a = t_desc(sQx + (k >> 2) * C::Q_ATOM + (k & 3) * 32, 16, 1024);
+            const uint64_t bd =
+                t_desc(sK + s * C::KV_BYTES + (k >> 2) * C::KV_ATOM + (k & 3) * 32, 16, 1024);
+            t_mma(tmem + scol + b * kKB, a, bd, idS, k > 0 ? 1u : 0u);
           }
+          t_commit(sfull(x, b));
           if (flags & kLast) t_commit(qempty);
-          // P V one tile behind S, so that the groups' softmax of this tile
-          // overlaps the tensor core; an item's last tile goes at once (its
-          // epilogue must not wait for the next item's Q tiles)
+          // P V one tile behind S, so that the softmax of this tile overlaps
+          // the tensor core; an item's last tile goes at once (its epilogue
+          // must not wait for the next item's Q tiles)
           if (pend && !do_pv(pstage, pflags)) {
             ok = false;
             break;
@@ -379,8 +380,8 @@ __global__ void __launch_bounds__(kTCThreads, TC<D>::CTAS_PER_SM)
         } while (!(flags & kLast));
       }
       // every issued MMA completes before the TMEM is released
-      t_commit(drain);
-      t_wait_drain(drain);
+      t_commit(drain + 8 * x);
+      t_wait_drain(drain + 8 * x);
     }
   } else {
     // ============================ softmax =============================
