@@ -229,17 +229,11 @@ __global__ void __launch_bounds__(kTCThreads, TC<D>::CTAS_PER_SM)
         // (rows past L read zeros), once the previous item's last S is done
         if (it >= 1 && !t_wait(qempty, it - 1, abort_flag)) break;
         t_expect_tx(qfull, kGroups * C::Q_BYTES);
+        // one copy per group: the map's box is {64 columns, rows, heads,
+        // atoms} and lands atom by atom, each [128 rows][64 columns]
 #pragma unroll
-        for (int x = 0; x < kGroups; ++x) {
-          const int h = x ? w.h1 : w.h0;
-#pragma unroll
-          for (int a = 0; a < C::ATOMS; ++a) {
-            const uint32_t dst = sQ + x * C::Q_BYTES + a * C::Q_ATOM;
-            t_tma_3d(dst, &tmQ, 64 * a, w.row0, h, qfull);
-            t_tma_3d(dst + kKB * 128, &tmQ, 64 * a, pair ? w.row0 : w.row0 + kKB,
-                     pair ? h + 1 : h, qfull);
-          }
-        }
+        for (int x = 0; x < kGroups; ++x)
+          t_tma_4d(sQ + x * C::Q_BYTES, &tmQ, 0, w.row0, x ? w.h1 : w.h0, 0, qfull);
         // the union of the two query blocks' lists, ascending (paired: one list)
         const int qb0 = w.row0 / kKB, qb1 = pair ? qb0 : qb0 + 1;
         const bool has1 = qb1 < nblk;
@@ -266,13 +260,8 @@ __global__ void __launch_bounds__(kTCThreads, TC<D>::CTAS_PER_SM)
           meta[s] = make_int4(kb, flags, w.row0, w.hk);
           t_expect_tx(kvfull + 8 * s, 2 * C::KV_BYTES + kKB * 4);
           t_tma_1d(sD + s * kKB * 4, &tmD, kb * kKB, kvfull + 8 * s);   // past L: zeros
-#pragma unroll
-          for (int a = 0; a < C::ATOMS; ++a) {
-            t_tma_3d(sK + s * C::KV_BYTES + a * C::KV_ATOM, &tmK, 64 * a, kb * kKB, w.hk,
-                     kvfull + 8 * s);
-            t_tma_3d(sV + s * C::KV_BYTES + a * C::KV_ATOM, &tmV, 64 * a, kb * kKB, w.hk,
-                     kvfull + 8 * s);
-          }
+          t_tma_4d(sK + s * C::KV_BYTES, &tmK, 0, kb * kKB, w.hk, 0, kvfull + 8 * s);
+          t_tma_4d(sV + s * C::KV_BYTES, &tmV, 0, kb * kKB, w.hk, 0, kvfull + 8 * s);
           ++g;
           return true;
         };
@@ -726,6 +715,32 @@ int prefill_head_map(CUtensorMap *tm, const void *base, int heads, int L, int D,
 
 }  // namespace pkv
 
+namespace {
+// 4-D map over a [heads][L][D] bf16 tensor as {64 columns, token, head,
+// 64-column atom}: one box of {64, box_rows, box_heads, D / 64} lands in
+// shared memory as D / 64 atoms, each [box_heads][box_rows][64] with the
+// 128-byte swizzle, i.e. the operand layout of one 128-row (or 64-row)
+// tile; tokens past L read zeros
+int atoms_map(CUtensorMap *tm, const void *base, int heads, int L, int D, int box_rows,
+              int box_heads) {
+  EncodeTiledFn fn = tc_encode_fn();
+  if (!fn) return pkv::fail(PKV_E_CUDA, "cuTensorMapEncodeTiled unavailable");
+  cuuint64_t dims[4] = {64u, static_cast<cuuint64_t>(L), static_cast<cuuint64_t>(heads),
+                        static_cast<cuuint64_t>(D / 64)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2,
+                           static_cast<cuuint64_t>(D) * 2 * L, 128u};
+  cuuint32_t box[4] = {64u, static_cast<cuuint32_t>(box_rows),
+                       static_cast<cuuint32_t>(box_heads), static_cast<cuuint32_t>(D / 64)};
+  cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+  CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return pkv::fail(PKV_E_CUDA, "cuTensorMapEncodeTiled (atoms) failed (%d)", static_cast<int>(r));
+  return PKV_OK;
+}
+}  // namespace
+
 // Launch of the tcgen05 prefill kernel (declared in pkv_internal.h); the
 // public entry point prefill_attn validates the arguments first.
 namespace pkv {
@@ -748,15 +763,16 @@ int launch_prefill_tc(const pkv_bf16 *q, const pkv_bf16 *k, const pkv_bf16 *v,
       done[dev] = true;
     }
   }
-  CUtensorMap tmQ, tmK, tmV, tmD;
-  int st = prefill_head_map(&tmQ, q, Hq, L, D, kKB);   // two 64-row boxes per item
-  if (st == PKV_OK) st = prefill_head_map(&tmK, k, Hkv, L, D, kKB);
-  if (st == PKV_OK) st = prefill_head_map(&tmV, v, Hkv, L, D, kKB);
-  if (st == PKV_OK) st = prefill_docs_map(&tmD, docs, L);
-  if (st != PKV_OK) return st;
   const int n = (L + kKB - 1) / kKB;
   const int G = Hq / Hkv;
   const bool pair = G % 2 == 0;
+  // a group's Q tile: paired, 64 rows of two heads; otherwise 128 rows of one
+  CUtensorMap tmQ, tmK, tmV, tmD;
+  int st = atoms_map(&tmQ, q, Hq, L, D, pair ? kKB : kQR, pair ? 2 : 1);
+  if (st == PKV_OK) st = atoms_map(&tmK, k, Hkv, L, D, kKB, 1);
+  if (st == PKV_OK) st = atoms_map(&tmV, v, Hkv, L, D, kKB, 1);
+  if (st == PKV_OK) st = prefill_docs_map(&tmD, docs, L);
+  if (st != PKV_OK) return st;
   const long long items = 1LL * (pair ? n : (n + 1) / 2) * items_per_tile(Hkv, G, pair);
   const long long cap = 1LL * TC<D>::CTAS_PER_SM * pkv::sm_count();
   const int grid = static_cast<int>(items < cap ? items : cap);

@@ -81,6 +81,14 @@ __device__ __forceinline__ void t_tma_1d(uint32_t dst, const CUtensorMap *tm, in
       "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(bar)
       : "memory");
 }
+__device__ __forceinline__ void t_tma_4d(uint32_t dst, const CUtensorMap *tm, int x, int y, int z,
+                                         int w, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar)
+      : "memory");
+}
 __device__ __forceinline__ void t_tma_3d(uint32_t dst, const CUtensorMap *tm, int x, int y, int z,
                                          uint32_t bar) {
   asm volatile(
