@@ -46,8 +46,9 @@ constexpr int wNSV = 2;       // V ring stages
 constexpr int wSplit = 4;                  // softmax warps per TMEM lane group
 constexpr int wSoftWarps = 4 * wSplit;
 constexpr int wKW = 64 / wSplit;           // keys per softmax warp
+// MMA: one warp issuing S, one issuing P V
 constexpr int wProdWarp = wSoftWarps, wMmaWarp = wSoftWarps + 1;
-constexpr int wThreads = (wSoftWarps + 2) * 32;
+constexpr int wThreads = (wSoftWarps + 3) * 32;
 constexpr float wLazyLog2 = 8.f;
 constexpr int wFull = 1, wFirst = 2, wLast = 4, wMaskAll = 8, wNeed0 = 16, wNeed1 = 32;
 
@@ -69,8 +70,8 @@ struct TW {
   static constexpr int OFF_META = OFF_XCH + 2 * wSplit * wQR * 4;  // int4 [wNSV]
   static constexpr int OFF_BAR = OFF_META + wNSV * 16;
   // qkfull[NSQ] qkempty[NSQ] dfull[NSV] vfull[NSV] vempty[NSV] sfull[2] sfree[2]
-  // pfull[2] pvdone[2] ofree drain xbar[4]
-  static constexpr int N_BAR = 2 * wNSQ + 3 * wNSV + 8 + 2 + 4;
+  // pfull[2] pvdone[2] ofree drain[2] xbar[4]
+  static constexpr int N_BAR = 2 * wNSQ + 3 * wNSV + 8 + 3 + 4;
   static constexpr int OFF_MISC = OFF_BAR + N_BAR * 8;
   static constexpr int OFF_SCHED = OFF_MISC + 16;   // SchedSmem: this CTA's items
   static constexpr int SMEM = OFF_SCHED + static_cast<int>(sizeof(SchedSmem)) + 1024;
@@ -124,7 +125,7 @@ __global__ void __launch_bounds__(wThreads, 1)
   const uint32_t qkfull = bar0, qkempty = qkfull + 8 * wNSQ, dfull = qkempty + 8 * wNSQ,
                  vfull = dfull + 8 * wNSV, vempty = vfull + 8 * wNSV, sfull = vempty + 8 * wNSV,
                  sfree = sfull + 16, pfull = sfree + 16, pvdone = pfull + 16, ofree = pvdone + 16,
-                 drain = ofree + 8, xbar = drain + 8;
+                 drain = ofree + 8, xbar = drain + 16;
   uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + C::OFF_MISC);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + C::OFF_MISC + 4);
 
@@ -146,6 +147,7 @@ __global__ void __launch_bounds__(wThreads, 1)
     }
     t_bar_init(ofree, wSoftWarps);
     t_bar_init(drain, 1);
+    t_bar_init(drain + 8, 1);
     for (int i = 0; i < 4; ++i) t_bar_init(xbar + 8 * i, wSplit);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -257,78 +259,91 @@ __global__ void __launch_bounds__(wThreads, 1)
         ok = emit(pend, pend_flags | wLast | (emitted == 0 ? wFirst : 0));
       }
     }
-  } else if (warp == wMmaWarp) {
+  } else if (warp >= wMmaWarp) {
     // ============================== MMA ===============================
+    // one warp (one lane issues) for the S of every tile and one for the
+    // P V, so that a tile's S streams in while the previous P V waits for
+    // its P
+    const bool pv_warp = warp != wMmaWarp;
     if (lane == 0) {
       constexpr uint32_t idS = t_idesc(wKB, 0), idO = t_idesc(wDO, 1);
-      int g = 0, gq = 0, pv_item = 0, prev_flags = 0;
-      bool ok = true, pv_pending = false;
-      // P V of tile gp into O; an item's first one overwrites O once the
-      // previous item's output has been read out of it
-      auto do_pv = [&](int gp, int flags) -> bool {
-        const int bp = gp & 1, sv = gp % wNSV;
-        if (!t_wait(pfull + 8 * bp, gp >> 1, abort_flag)) return false;
-        if ((flags & wFirst) && pv_item > 0 && !t_wait(ofree, pv_item - 1, abort_flag))
-          return false;
-        if (!t_wait(vfull + 8 * sv, gp / wNSV, abort_flag)) return false;
-        t_fence_after();
+      int g = 0;
+      bool ok = true;
+      if (!pv_warp) {
+        int gq = 0;
+        for (int it = 0; it < n_mine && ok; ++it) {
+          int flags = 0;
+          do {
+            const int b = g & 1, sv = g % wNSV;
+            if (g >= 2 && !t_wait(sfree + 8 * b, (g >> 1) - 1, abort_flag)) {
+              ok = false;
+              break;
+            }
+            for (int c = 0; c < C::NCH && ok; ++c) {
+              const int s = gq % wNSQ;
+              if (!t_wait(qkfull + 8 * s, gq / wNSQ, abort_flag)) {
+                ok = false;
+                break;
+              }
+              t_fence_after();
+              const uint32_t base = sQK + s * C::QK_STAGE;
 #pragma unroll
-        for (int k = 0; k < wKB / 16; ++k) {
-          const uint64_t a = t_desc(sP + bp * C::P_BYTES + k * 32, 16, 1024);
-          const uint64_t b = t_desc(sV + sv * C::V_BYTES + k * 2048, C::V_ATOM, 1024);
-          t_mma(tmem + C::O_COL, a, b, idO, (k > 0 || !(flags & wFirst)) ? 1u : 0u);
+              for (int k = 0; k < 4; ++k) {
+                const uint64_t a = t_desc(base + k * 32, 16, 1024);
+                const uint64_t bd = t_desc(base + C::Q_CH + k * 32, 16, 1024);
+                t_mma(tmem + C::S_COL + b * wKB, a, bd, idS, (c > 0 || k > 0) ? 1u : 0u);
+              }
+              t_commit(qkempty + 8 * s);
+              ++gq;
+            }
+            if (!ok) break;
+            t_commit(sfull + 8 * b);
+            // the tile's flags (for the item's end), staged with its V tile
+            if (!t_wait(dfull + 8 * sv, g / wNSV, abort_flag)) {
+              ok = false;
+              break;
+            }
+            flags = meta[sv].y;
+            ++g;
+          } while (!(flags & wLast));
         }
-        t_commit(pvdone + 8 * bp);
-        t_commit(vempty + 8 * sv);
-        if (flags & wLast) ++pv_item;
-        return true;
-      };
-      for (int it = 0; it < n_mine && ok; ++it) {
-        int flags = 0;
-        do {
-          const int b = g & 1, sv = g % wNSV;
-          if (g >= 2 && !t_wait(sfree + 8 * b, (g >> 1) - 1, abort_flag)) {
-            ok = false;
-            break;
-          }
-          for (int c = 0; c < C::NCH && ok; ++c) {
-            const int s = gq % wNSQ;
-            if (!t_wait(qkfull + 8 * s, gq / wNSQ, abort_flag)) {
+      } else {
+        // P V of tile g into O once its P is written; an item's first one
+        // overwrites O once the previous item's output has been read out
+        int pv_item = 0;
+        for (int it = 0; it < n_mine && ok; ++it) {
+          int flags = 0;
+          do {
+            const int bp = g & 1, sv = g % wNSV;
+            if (!t_wait(dfull + 8 * sv, g / wNSV, abort_flag)) {
+              ok = false;
+              break;
+            }
+            flags = meta[sv].y;
+            if (!t_wait(pfull + 8 * bp, g >> 1, abort_flag) ||
+                ((flags & wFirst) && pv_item > 0 && !t_wait(ofree, pv_item - 1, abort_flag)) ||
+                !t_wait(vfull + 8 * sv, g / wNSV, abort_flag)) {
               ok = false;
               break;
             }
             t_fence_after();
-            const uint32_t base = sQK + s * C::QK_STAGE;
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const uint64_t a = t_desc(base + k * 32, 16, 1024);
-              const uint64_t bd = t_desc(base + C::Q_CH + k * 32, 16, 1024);
-              t_mma(tmem + C::S_COL + b * wKB, a, bd, idS, (c > 0 || k > 0) ? 1u : 0u);
+            for (int k = 0; k < wKB / 16; ++k) {
+              const uint64_t a = t_desc(sP + bp * C::P_BYTES + k * 32, 16, 1024);
+              const uint64_t bv = t_desc(sV + sv * C::V_BYTES + k * 2048, C::V_ATOM, 1024);
+              t_mma(tmem + C::O_COL, a, bv, idO, (k > 0 || !(flags & wFirst)) ? 1u : 0u);
             }
-            t_commit(qkempty + 8 * s);
-            ++gq;
-          }
-          if (!ok) break;
-          t_commit(sfull + 8 * b);
-          if (!t_wait(dfull + 8 * sv, g / wNSV, abort_flag)) {
-            ok = false;
-            break;
-          }
-          flags = meta[sv].y;
-          // P V one tile behind S (across items too)
-          if (pv_pending && !do_pv(g - 1, prev_flags)) {
-            ok = false;
-            break;
-          }
-          pv_pending = true;
-          prev_flags = flags;
-          ++g;
-        } while (!(flags & wLast));
+            t_commit(pvdone + 8 * bp);
+            t_commit(vempty + 8 * sv);
+            if (flags & wLast) ++pv_item;
+            ++g;
+          } while (!(flags & wLast));
+        }
       }
-      if (ok && pv_pending) do_pv(g - 1, prev_flags);
       // every issued MMA completes before the TMEM is released
-      t_commit(drain);
-      t_wait_drain(drain);
+      const uint32_t dr = drain + (pv_warp ? 8 : 0);
+      t_commit(dr);
+      t_wait_drain(dr);
     }
   } else {
     // ============================ softmax =============================
