@@ -50,13 +50,18 @@ int launch_prefill_wide(const pkv_bf16 *q, const pkv_bf16 *k, const pkv_bf16 *v,
 
 struct CUtensorMap_st;
 namespace pkv {
-// Tensor maps of the prefill kernels (prefill_tc.cu): a 3-D map {column,
+// Tensor maps of the prefill kernels (defined in prefill_tc.cu): a 3-D map {column,
 // token, head} over a [heads][L][D] bf16 tensor with [box_rows][64] boxes and
 // 128-byte swizzle (tokens past L read zeros), and a 1-D map over the int32
 // document ids in 64-id boxes (ids past L read zeros).
 int prefill_head_map(CUtensorMap_st *tm, const void *base, int heads, int L, int D,
                      int box_rows);
 int prefill_docs_map(CUtensorMap_st *tm, const int32_t *docs, int L);
+// A 4-D map {64 columns, token, head, 64-column atom} over the same tensor:
+// one box of {64, box_rows, box_heads, box_atoms} lands as box_atoms atoms of
+// [box_heads][box_rows][64], 128-byte swizzle (tokens past L read zeros).
+int prefill_atoms_map(CUtensorMap_st *tm, const void *base, int heads, int L, int D,
+                      int box_rows, int box_heads, int box_atoms);
 
 inline bool aligned16(const void *p) {
   return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;

@@ -715,14 +715,14 @@ int prefill_head_map(CUtensorMap *tm, const void *base, int heads, int L, int D,
 
 }  // namespace pkv
 
-namespace {
+namespace pkv {
 // 4-D map over a [heads][L][D] bf16 tensor as {64 columns, token, head,
-// 64-column atom}: one box of {64, box_rows, box_heads, D / 64} lands in
-// shared memory as D / 64 atoms, each [box_heads][box_rows][64] with the
-// 128-byte swizzle, i.e. the operand layout of one 128-row (or 64-row)
-// tile; tokens past L read zeros
-int atoms_map(CUtensorMap *tm, const void *base, int heads, int L, int D, int box_rows,
-              int box_heads) {
+// 64-column atom}: one box of {64, box_rows, box_heads, box_atoms} lands in
+// shared memory as box_atoms atoms, each [box_heads][box_rows][64] with the
+// 128-byte swizzle (the operand layout of a 64- or 128-row tile); tokens
+// past L read zeros
+int prefill_atoms_map(CUtensorMap *tm, const void *base, int heads, int L, int D, int box_rows,
+                      int box_heads, int box_atoms) {
   EncodeTiledFn fn = tc_encode_fn();
   if (!fn) return pkv::fail(PKV_E_CUDA, "cuTensorMapEncodeTiled unavailable");
   cuuint64_t dims[4] = {64u, static_cast<cuuint64_t>(L), static_cast<cuuint64_t>(heads),
@@ -730,7 +730,7 @@ int atoms_map(CUtensorMap *tm, const void *base, int heads, int L, int D, int bo
   cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2,
                            static_cast<cuuint64_t>(D) * 2 * L, 128u};
   cuuint32_t box[4] = {64u, static_cast<cuuint32_t>(box_rows),
-                       static_cast<cuuint32_t>(box_heads), static_cast<cuuint32_t>(D / 64)};
+                       static_cast<cuuint32_t>(box_heads), static_cast<cuuint32_t>(box_atoms)};
   cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
   CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -739,7 +739,7 @@ int atoms_map(CUtensorMap *tm, const void *base, int heads, int L, int D, int bo
     return pkv::fail(PKV_E_CUDA, "cuTensorMapEncodeTiled (atoms) failed (%d)", static_cast<int>(r));
   return PKV_OK;
 }
-}  // namespace
+}  // namespace pkv
 
 // Launch of the tcgen05 prefill kernel (declared in pkv_internal.h); the
 // public entry point prefill_attn validates the arguments first.
@@ -768,9 +768,9 @@ int launch_prefill_tc(const pkv_bf16 *q, const pkv_bf16 *k, const pkv_bf16 *v,
   const bool pair = G % 2 == 0;
   // a group's Q tile: paired, 64 rows of two heads; otherwise 128 rows of one
   CUtensorMap tmQ, tmK, tmV, tmD;
-  int st = atoms_map(&tmQ, q, Hq, L, D, pair ? kKB : kQR, pair ? 2 : 1);
-  if (st == PKV_OK) st = atoms_map(&tmK, k, Hkv, L, D, kKB, 1);
-  if (st == PKV_OK) st = atoms_map(&tmV, v, Hkv, L, D, kKB, 1);
+  int st = prefill_atoms_map(&tmQ, q, Hq, L, D, pair ? kKB : kQR, pair ? 2 : 1, D / 64);
+  if (st == PKV_OK) st = prefill_atoms_map(&tmK, k, Hkv, L, D, kKB, 1, D / 64);
+  if (st == PKV_OK) st = prefill_atoms_map(&tmV, v, Hkv, L, D, kKB, 1, D / 64);
   if (st == PKV_OK) st = prefill_docs_map(&tmD, docs, L);
   if (st != PKV_OK) return st;
   const long long items = 1LL * (pair ? n : (n + 1) / 2) * items_per_tile(Hkv, G, pair);

@@ -211,10 +211,8 @@ __global__ void __launch_bounds__(wThreads, 1)
             if (gq >= wNSQ && !t_wait(qkempty + 8 * s, gq / wNSQ - 1, abort_flag)) return false;
             const uint32_t dst = sQK + s * C::QK_STAGE;
             t_expect_tx(qkfull + 8 * s, C::QK_STAGE);
-            // the chunk's two 64-row halves (rows past L read zeros)
-            t_tma_3d(dst, &tmQ, 64 * c, w.row0, w.h, qkfull + 8 * s);
-            t_tma_3d(dst + wKB * 128, &tmQ, 64 * c, pair ? w.row0 : w.row0 + wKB,
-                     pair ? w.h + 1 : w.h, qkfull + 8 * s);
+            // the chunk's 128 Q rows in one copy (rows past L read zeros)
+            t_tma_4d(dst, &tmQ, 0, w.row0, w.h, c, qkfull + 8 * s);
             t_tma_3d(dst + C::Q_CH, &tmK, 64 * c, kb * wKB, hk, qkfull + 8 * s);
             ++gq;
           }
@@ -224,10 +222,7 @@ __global__ void __launch_bounds__(wThreads, 1)
           t_expect_tx(dfull + 8 * s, wKB * 4);
           t_tma_1d(sD + s * wKB * 4, &tmD, kb * wKB, dfull + 8 * s);   // past L: zeros
           t_expect_tx(vfull + 8 * s, C::V_BYTES);
-#pragma unroll
-          for (int a = 0; a < wDO / 64; ++a)
-            t_tma_3d(sV + s * C::V_BYTES + a * C::V_ATOM, &tmV, w.oc * wDO + 64 * a, kb * wKB, hk,
-                     vfull + 8 * s);
+          t_tma_4d(sV + s * C::V_BYTES, &tmV, 0, kb * wKB, hk, w.oc * (wDO / 64), vfull + 8 * s);
           ++gv;
           return true;
         };
@@ -632,9 +627,12 @@ int launch_prefill_wide(const pkv_bf16 *q, const pkv_bf16 *k, const pkv_bf16 *v,
     }
   }
   CUtensorMap tmQ, tmK, tmV, tmD;
-  int st = prefill_head_map(&tmQ, q, Hq, L, D, wKB);   // two 64-row boxes per chunk
+  const bool pair_q = (Hq / Hkv) % 2 == 0;
+  // a Q chunk: 64 rows of two heads (paired) or 128 rows of one; a V tile:
+  // 64 keys x the 256 columns of an output half
+  int st = prefill_atoms_map(&tmQ, q, Hq, L, D, pair_q ? wKB : wQR, pair_q ? 2 : 1, 1);
   if (st == PKV_OK) st = prefill_head_map(&tmK, k, Hkv, L, D, wKB);
-  if (st == PKV_OK) st = prefill_head_map(&tmV, v, Hkv, L, D, wKB);
+  if (st == PKV_OK) st = prefill_atoms_map(&tmV, v, Hkv, L, D, wKB, 1, wDO / 64);
   if (st == PKV_OK) st = prefill_docs_map(&tmD, docs, L);
   if (st != PKV_OK) return st;
   const int n = (L + wKB - 1) / wKB;
