@@ -290,6 +290,11 @@ __global__ void __launch_bounds__(kTCThreads, TC<D>::CTAS_PER_SM)
           pend_flags = kMaskAll;
         }
         ok = emit(pend, pend_flags | kLast | (emitted == 0 ? kFirst : 0));
+        if (ok && it + 1 < n_mine) {   // the next item's Q tiles into L2 meanwhile
+          const Item wn = item_of(sched_item(sched, it + 1), nq, Hkv, G, pair);
+#pragma unroll
+          for (int x = 0; x < kGroups; ++x) t_prefetch_4d(&tmQ, 0, wn.row0, x ? wn.h1 : wn.h0, 0);
+        }
       }
     }
   } else if (warp >= kMmaWarp) {

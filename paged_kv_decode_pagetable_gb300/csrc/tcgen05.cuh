@@ -81,6 +81,13 @@ __device__ __forceinline__ void t_tma_1d(uint32_t dst, const CUtensorMap *tm, in
       "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(bar)
       : "memory");
 }
+// pulls one box of a 4-D tensor map into L2 only (no destination, no barrier)
+__device__ __forceinline__ void t_prefetch_4d(const CUtensorMap *tm, int x, int y, int z, int w) {
+  asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
+                   reinterpret_cast<uint64_t>(tm)),
+               "r"(x), "r"(y), "r"(z), "r"(w)
+               : "memory");
+}
 __device__ __forceinline__ void t_tma_4d(uint32_t dst, const CUtensorMap *tm, int x, int y, int z,
                                          int w, uint32_t bar) {
   asm volatile(
