@@ -11,13 +11,16 @@
 // each of two softmax groups: both use every K / V tile the item loads, so
 // one group's waits and exchanges overlap the other group's work, and the
 // tiles are loaded once for both.
-//   warp 16 (producer, one lane): per item, the two Q tiles by TMA (3-D map
-//     {column, token, head}: rows past L read zeros) into the groups' Q
-//     buffers, then the union of the item's two query blocks' key-block
-//     lists (merged on the fly, ascending), each key block's K and V tiles
-//     and its 64 document ids by TMA into a 3-stage ring, with a small
-//     descriptor (block; full / first / last flags; which query block lists
-//     it) in the stage.
+//   warp 16 (producer, one lane): per item, the two Q tiles by TMA, one
+//     copy each (4-D map {64 columns, token, head, 64-column atom}: rows
+//     past L read zeros), into the groups' Q buffers, then the union of the
+//     item's two query blocks' key-block lists (merged on the fly,
+//     ascending), each key block's K and V tiles (one copy each) and its 64
+//     document ids by TMA into a 3-stage ring, with a small descriptor
+//     (block; full / first / last flags; which query block lists it) in the
+//     stage; once an item's last tile is issued, the next item's Q tiles are
+//     pulled into L2. Items come in the cost-sorted order of
+//     prefill_sched.cuh.
 //   warps 17, 18 (MMA, one lane each, one warp per softmax group): per tile,
 //     the group's S = Q K^T into its own TMEM S buffers (two; M = 128, N =
 //     64, K-major SW128 operands), then, one tile behind (at once for an

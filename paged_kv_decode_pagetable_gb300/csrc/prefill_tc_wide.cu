@@ -20,9 +20,10 @@
 //   * the V tile (64 keys x DO columns), the tile's 64 document ids and its
 //     descriptor come through a separate 2-stage ring;
 //   * TMEM: S in two 64-column buffers, one O of DO columns (384 of 512).
-// The warp roles, the softmax (16 warps, lazy rescaling, exp2 domain, P as
-// bf16 in a swizzled shared buffer) and the failure handling are those of
-// prefill_tc.cu; an item's output is written after the next item's first
+// The producer, the softmax (16 warps, lazy rescaling, exp2 domain, P as
+// bf16 in a swizzled shared buffer), the work order and the failure handling
+// are those of prefill_tc.cu; two MMA warps issue, one every tile's S and
+// the other its P V; an item's output is written after the next item's first
 // tile, and the next item's first P V waits for it (one O buffer).
 #include <cuda.h>
 #include <cuda_bf16.h>
