@@ -144,6 +144,15 @@ def measured_peaks():
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
 
 
+def hold_stream():
+    """Keeps the current stream busy for some tens of microseconds (torch's
+    spin kernel), issued before a start event: the graph replay that follows
+    is then already queued when the event fires, so the timed region holds
+    the steps' device time and not the host's submission of the graph (which
+    a replay of K steps would otherwise carry once, 10 us or so)."""
+    torch.cuda._sleep(100000)
+
+
 def profile_traffic(kernel_key: str, mean_alg_bytes: float | None = None):
     """DRAM bytes per launch from a committed ncu capture, or None when the
     kernel source changed since the capture. A record with a measured /
@@ -565,6 +574,7 @@ def run_ours(args, world, rank, local):
         gr.replay()                       # the first launch of a graph uploads it
         torch.cuda.synchronize()
         a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        hold_stream()
         a0.record(stream)
         gr.replay()
         a1.record(stream)
@@ -585,6 +595,7 @@ def run_ours(args, world, rank, local):
     barrier(world)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    hold_stream()
     e0.record(stream)
     graph.replay()
     e1.record(stream)
@@ -859,6 +870,7 @@ def run_prefill(args, world, rank, local):
     barrier(world)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     stream = torch.cuda.current_stream()
+    hold_stream()
     e0.record(stream)
     graph.replay()
     e1.record(stream)
@@ -874,6 +886,7 @@ def run_prefill(args, world, rank, local):
             pkv.prefill_block_mask(d_docs, window)
     mgraph.replay()
     torch.cuda.synchronize()
+    hold_stream()
     e0.record(stream)
     mgraph.replay()
     e1.record(stream)
